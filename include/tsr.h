@@ -1,0 +1,313 @@
+/*
+ * tsr.h -- C ABI of the GB300 block-sparse attention forward library
+ *          (libtsr_gb300.so).
+ *
+ * The library computes, on one GPU,
+ *
+ *     O = softmax(Q K^T / sqrt(d) + M) V,      lse = log(sum_j exp(q.k_j / sqrt(d)))
+ *
+ * where M is 0 on the allowed (query, key) pairs of a mask and -inf elsewhere,
+ * with the sum in lse running over the allowed keys only.  The mask comes in
+ * one of four forms:
+ *
+ *   TSR_MASK_UNIFORM  a logical block mask over bq x bk blocks.  "Decoupling
+ *                     Logical Masks from GPU Execution for Dynamic Block-Sparse
+ *                     Attention" (Tessera), abstract: block-sparse attention
+ *                     computes only the blocks that a logical mask selects.
+ *   TSR_MASK_SEGMENTS the same with variable block boundaries (Tessera abstract:
+ *                     logical block geometry differs from mask to mask).
+ *   TSR_MASK_SVG      per-head spatial / temporal patterns ("Accelerating
+ *                     Spatio-Temporal Attention for Video Diffusion on TPUs",
+ *                     sections "Sparse VideoGen" and "Splash Attention").
+ *   TSR_MASK_KEYLIST  M x 1 key slices: one sorted key list per block of M
+ *                     queries ("FG-Attn: Leveraging Fine-Grained Sparsity In
+ *                     Diffusion Transformers", abstract).
+ *
+ * Work is split in two calls, as in Tessera's runtime (abstract: a physical
+ * mapping layer, a task organisation layer and profile-guided regime selection):
+ *
+ *   tsr_plan()         maps the logical mask onto 128-row physical tiles on the
+ *                      GPU (retain / combine / subdivide), marks each tile full or
+ *                      boundary, drops empty tiles, builds the per-query-tile work
+ *                      lists in longest-first order and picks the regime from the
+ *                      offline-profiled lookup table;
+ *   tsr_bsa_forward()  runs the attention over the plan.
+ *
+ * Conventions for every entry point
+ *   - All tensor and mask pointers are DEVICE pointers unless a comment says
+ *     HOST.  The caller owns them; the library never frees them.
+ *   - Q, K, V and O are bf16 [B][H][N][d] row-major (d contiguous) with
+ *     d in {64, 128}; lse is fp32 [B][H][N].  Every base pointer must be
+ *     16-byte aligned.  N = number of queries = number of keys.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is queued
+ *     on it; inputs must stay valid until that work completes.
+ *   - Functions return a tsr_status.  Nothing throws across the ABI.  On failure
+ *     tsr_last_error() returns a message for the calling thread.
+ *   - Argument errors are found on the host before anything is launched.
+ */
+#ifndef TSR_GB300_H
+#define TSR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TSR_ABI_VERSION 1
+
+typedef enum {
+  TSR_OK = 0,
+  TSR_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or mask content      */
+  TSR_ERR_UNSUPPORTED = 2,   /* valid, but outside what this build implements       */
+  TSR_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed                 */
+  TSR_ERR_OOM = 4,           /* device or host allocation failed                    */
+  TSR_ERR_TIMEOUT = 5,       /* a device-side wait gave up (kernel returned early)  */
+  TSR_ERR_INTERNAL = 6       /* a device-side consistency check failed              */
+} tsr_status;
+
+typedef enum {
+  TSR_MASK_UNIFORM = 0,
+  TSR_MASK_SEGMENTS = 1,
+  TSR_MASK_SVG = 2,
+  TSR_MASK_KEYLIST = 3
+} tsr_mask_kind;
+
+typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
+
+/*
+ * Logical mask and geometry.
+ *
+ * UNIFORM : blocks = uint8 [B][H][ceil(N/bq)][ceil(N/bk)], nonzero = allowed.
+ *           allowed(i, j) = blocks[b][h][i / bq][j / bk].  The last block row and
+ *           column are truncated at N.  bq, bk >= 16.
+ * SEGMENTS: q_bounds = int32 [n_qseg + 1] ascending, q_bounds[0] = 0,
+ *           q_bounds[n_qseg] = N (k_bounds likewise), each segment >= 16 tokens;
+ *           blocks = uint8 [B][H][n_qseg][n_kseg];
+ *           allowed(i, j) = blocks[b][h][seg_q(i)][seg_k(j)].
+ * SVG     : head_kind = int8 [H] (tsr_head_kind), N = n_frames * frame_size,
+ *           tokens frame-major (t = f * frame_size + s).
+ *             spatial  head: allowed(i, j) = frame(i) == frame(j) || frame(j) == 0
+ *             temporal head: allowed(i, j) = i mod frame_size == j mod frame_size
+ *           Temporal heads run in temporal-major order (t' = s * n_frames + f);
+ *           the library permutes Q/K/V into plan-owned scratch and writes O and
+ *           lse back in the caller's order.  frame_size >= 16 and n_frames >= 16
+ *           (so that no 128-token tile holds more than 8 segments).
+ * KEYLIST : slice_m in {64, 128}.  indptr = int64 [B*H*ceil(N/slice_m) + 1] (CSR
+ *           over (b, h, query block), indptr[0] = 0), indices = int32 keys, each
+ *           list ascending, unique, in [0, N).  allowed(i, j) = j in the list of
+ *           (b, h, i / slice_m).  Violations give TSR_ERR_INVALID_ARG.
+ *
+ * The device arrays must stay valid until the work tsr_plan() queues completes.
+ */
+typedef struct {
+  int32_t kind;              /* tsr_mask_kind */
+  int32_t B, H, N, d;
+  /* UNIFORM */
+  int32_t bq, bk;
+  /* SEGMENTS */
+  int32_t n_qseg, n_kseg;
+  const int32_t *q_bounds, *k_bounds;
+  /* UNIFORM and SEGMENTS */
+  const uint8_t *blocks;
+  /* SVG */
+  int32_t n_frames, frame_size;
+  const int8_t *head_kind;
+  /* KEYLIST */
+  int32_t slice_m;
+  const int64_t *indptr;
+  const int32_t *indices;
+} tsr_mask;
+
+/* Plan options (pass NULL for defaults). */
+typedef struct {
+  int32_t bn;        /* 0 = from the regime table; 64 or 128 = force KV tile width   */
+  int32_t stages;    /* 0 = from the regime table; else K/V pipeline depth (2..6)    */
+  int32_t ctas_per_sm; /* 0 = from the regime table; 1 or 2                           */
+  int32_t flags;     /* TSR_PLAN_* bits                                              */
+  int64_t seed_reserved;
+} tsr_plan_opts;
+
+#define TSR_PLAN_SYNC_CHECK 1  /* tsr_bsa_forward synchronises and reads the device
+                                  error word (slower; for debugging)               */
+#define TSR_PLAN_NO_LPT     2  /* keep work items in (b, h, q-tile) order          */
+
+typedef struct tsr_plan_s *tsr_plan_t;   /* opaque, library-owned */
+
+/* Statistics of a plan (host copy). */
+typedef struct {
+  int32_t bm, bn, stages, ctas_per_sm;  /* chosen regime                           */
+  int32_t gathered;                     /* 1 = KEYLIST gathered tiles              */
+  int32_t n_temporal_heads;
+  int64_t n_items;                      /* work items (one per 128-row query tile) */
+  int64_t n_entries;                    /* physical K/V tiles over all items       */
+  int64_t n_boundary;                   /* of which boundary (masked) tiles        */
+  int64_t n_logical_on;                 /* allowed logical blocks / slices         */
+  int64_t n_logical_total;
+  int64_t max_item_len;
+  int32_t regime_id;                    /* row of the regime table used (-1: opts) */
+  int32_t reserved;
+} tsr_plan_stats;
+
+/*
+ * tsr_plan -- physical mapping + task organisation + regime selection.
+ *
+ * Tessera abstract: a mapping layer turns logical blocks into physical tiles by
+ * keeping them, merging several into one tile or cutting one into several; a
+ * task layer groups tiles into GPU tasks for data reuse, parallelism and
+ * copy/compute overlap; a table filled by offline profiling picks the execution
+ * plan cheaply.  Splash digest, "Splash Attention": tiles with nothing to compute
+ * are never loaded, and element-exact masking is applied on boundary tiles only.
+ *
+ * Runs as CUDA kernels on `stream`; synchronises `stream` once to size the plan.
+ * On success *out receives a new plan that the caller must release with
+ * tsr_plan_destroy().  The plan owns device memory (tiles, descriptors, work
+ * items, temporal-major scratch) and may be used by any number of
+ * tsr_bsa_forward() calls on the same device with matching B, H, N, d.
+ */
+tsr_status tsr_plan(const tsr_mask *mask, const tsr_plan_opts *opts, tsr_plan_t *out,
+                    void *stream);
+
+/*
+ * tsr_bsa_forward -- the attention over a plan.
+ *
+ * q, k, v: bf16 [B][H][N][d] (device).  out: bf16 [B][H][N][d] (device), lse:
+ * fp32 [B][H][N] (device).  Every row of out and lse is written: rows with no
+ * allowed key get O = 0 and lse = -inf.  out must not alias q, k or v.
+ * Asynchronous on `stream` unless the plan was made with TSR_PLAN_SYNC_CHECK.
+ * Device-side failures (a bounded wait that gave up) are reported by
+ * tsr_plan_device_status().
+ */
+tsr_status tsr_bsa_forward(const void *q, const void *k, const void *v, tsr_plan_t plan,
+                           void *out, float *lse, void *stream);
+
+/* Synchronise `stream` and return the plan's device error word as a status
+   (TSR_OK, TSR_ERR_TIMEOUT or TSR_ERR_INTERNAL); clears it. */
+tsr_status tsr_plan_device_status(tsr_plan_t plan, void *stream);
+
+tsr_status tsr_plan_destroy(tsr_plan_t plan);
+
+tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats *stats /* HOST */);
+
+/*
+ * tsr_plan_export -- copy the plan to HOST memory for inspection.
+ * With host_buf == NULL sets *bytes to the size needed.  Otherwise *bytes must
+ * hold the buffer size; it receives the bytes written.  Synchronises the plan's
+ * stream.  Layout (little-endian):
+ *
+ *   tsr_export_header                              (80 bytes)
+ *   tsr_plan_item   items[n_items]                 (32 bytes each)
+ *   tsr_plan_entry  entries[n_entries]             (8 bytes each)
+ *   tsr_tile_desc   descs[n_desc]                  (32 bytes each)
+ *   int32_t         gidx[n_gidx]                   (gathered key indices)
+ *   int8_t          head_layout[H]                 (0 caller order, 1 temporal-major)
+ */
+tsr_status tsr_plan_export(tsr_plan_t plan, void *host_buf, size_t *bytes);
+
+typedef struct {
+  char magic[4];              /* "TSRP" */
+  int32_t version;            /* 1 */
+  int32_t B, H, N, d;
+  int32_t bm, bn;             /* query rows and key columns per physical tile      */
+  int32_t gathered;           /* 0: entries are contiguous key ranges; 1: gathered */
+  int32_t n_frames, frame_size;   /* temporal-major permutation (SVG), else 0      */
+  int32_t slice_m;            /* KEYLIST query block size, else 0                  */
+  int64_t n_items, n_entries, n_desc, n_gidx;
+} tsr_export_header;          /* 80 bytes */
+
+/*
+ * A work item: all physical tiles of one 128-row query tile.
+ *   q_tile  : rows [q_tile*bm, min(N, q_tile*bm + bm)) of head bh = b*H + h, in the
+ *             head's layout (temporal-major for temporal SVG heads)
+ *   begin/end: its entries are entries[begin .. end)
+ *   layout  : 0 caller order, 1 temporal-major
+ */
+typedef struct {
+  int32_t bh, q_tile, begin, end;
+  int32_t layout, reserved0, reserved1, reserved2;
+} tsr_plan_item;
+
+/*
+ * A physical K/V tile.  kv: first key of bn contiguous keys (gathered = 0), or the
+ * offset into gidx of bn key indices (gathered = 1).  desc: -1 = full tile (all
+ * bm x bn elements allowed and in range), else index of its boundary descriptor.
+ */
+typedef struct {
+  int32_t kv, desc;
+} tsr_plan_entry;
+
+/*
+ * Boundary descriptor (32 bytes).
+ * Contiguous plans (grid form): rows [r_start[r], r_start[r+1]) of the tile form
+ * row segment r (r < n_r, the last one ends at bm), columns [c_start[c],
+ * c_start[c+1]) form column segment c (c < n_c); columns >= c_start[n_c] are out
+ * of range.  Element (row, col) is allowed iff bit (r*8 + c) of `bits` is set.
+ * Gathered plans (list form): n_r = bm / slice_m row segments of slice_m rows;
+ * column c is allowed for row segment r iff bit c of colmask[r] is set.
+ */
+typedef struct {
+  uint8_t n_r, n_c;
+  uint8_t r_start[8];
+  uint8_t c_start[9];
+  uint8_t pad[5];
+  uint64_t bits;
+} tsr_tile_desc;
+
+typedef struct {
+  uint32_t colmask[2][4];
+} tsr_tile_desc_list;
+
+/*
+ * tsr_temporal_permute -- the temporal-major token permutation on its own
+ * (Splash digest, "Splash Attention": token memory permuted into temporal-major
+ * order so the temporal pattern is contiguous).
+ *
+ * For every head h with head_kind[h] == TSR_HEAD_TEMPORAL (head_kind: HOST int8
+ * [H]; NULL = all heads):
+ *   inverse == 0: dst[b][h][s*F + f][:] = src[b][h][f*S + s][:]
+ *   inverse != 0: dst[b][h][f*S + s][:] = src[b][h][s*F + f][:]
+ * with F = n_frames, S = frame_size.  Rows of other heads are not touched.
+ * src, dst: [B][H][F*S][row_bytes] (device, 16-byte aligned, row_bytes % 16 == 0),
+ * must not overlap.
+ */
+tsr_status tsr_temporal_permute(const void *src, void *dst, int32_t B, int32_t H,
+                                int32_t n_frames, int32_t frame_size, int32_t row_bytes,
+                                const int8_t *head_kind, int32_t inverse, void *stream);
+
+/*
+ * tsr_attention_host -- one whole call from HOST memory: copies the mask arrays
+ * and Q, K, V to the device, plans, runs the forward and copies O and lse back,
+ * then synchronises.  Every pointer in `mask` and q, k, v, out, lse are HOST
+ * pointers with the layouts above.  Device buffers are cached per thread between
+ * calls (released by tsr_release_host_buffers()).
+ */
+tsr_status tsr_attention_host(const tsr_mask *mask, const tsr_plan_opts *opts,
+                              const void *q, const void *k, const void *v, void *out,
+                              float *lse);
+
+void tsr_release_host_buffers(void);
+
+/*
+ * Regime table (profile-guided regime selection, Tessera abstract).
+ * tsr_regime_load reads a table file (text, one regime per line; see the file
+ * shipped next to the library); NULL reloads the built-in default.
+ * tsr_regime_lookup returns the regime chosen for a mask class.
+ */
+tsr_status tsr_regime_load(const char *path /* HOST, NULL = built-in */);
+
+typedef struct {
+  int32_t bn, stages, ctas_per_sm, id;
+} tsr_regime;
+
+tsr_status tsr_regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N,
+                             double density, tsr_regime *out /* HOST */);
+
+const char *tsr_status_string(tsr_status s);
+const char *tsr_last_error(void);        /* thread-local; "" when none */
+int32_t tsr_abi_version(void);           /* TSR_ABI_VERSION            */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TSR_GB300_H */
