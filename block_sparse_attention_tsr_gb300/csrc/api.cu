@@ -1,0 +1,593 @@
+// api.cu -- the C ABI declared in include/tsr.h: argument checks, plan
+// lifetime, forward dispatch, plan export, the host-memory entry point and the
+// regime table (Tessera abstract: profile-guided regime selection through a
+// lookup table filled by offline profiling).
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <mutex>
+#include <new>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tsr {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+const char* last_error_cstr() { return g_last_error.c_str(); }
+
+tsr_status fail(tsr_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+tsr_status cuda_fail(cudaError_t e, const char* what) {
+  set_error(std::string(what) + ": " + cudaGetErrorString(e));
+  return e == cudaErrorMemoryAllocation ? TSR_ERR_OOM : TSR_ERR_CUDA;
+}
+
+int num_sms(int device) {
+  static int cache[64] = {0};
+  if (device >= 0 && device < 64 && cache[device]) return cache[device];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+    n = 1;
+  if (device >= 0 && device < 64) cache[device] = n;
+  return n;
+}
+
+// ----------------------------------------------------------- regime table
+//
+// One row per line: kind bq bk n_min n_max dens_min dens_max d  bn stages ctas
+// ("*" = any).  The first matching row wins.  The rows shipped with the
+// library come from timing every kernel variant on this GPU over synthetic
+// masks of each class (the table file next to the library); the built-in rows
+// below are the fallback when no file is loaded.
+namespace {
+
+struct RegimeRow {
+  int kind, bq, bk;
+  int64_t n_min, n_max;
+  double d_min, d_max;
+  int d, bn, stages, ctas;
+};
+
+const char* kBuiltinTable =
+    "# kind bq bk n_min n_max dens_min dens_max d bn stages ctas\n"
+    "* * * * * * * 128 128 3 1\n"
+    "* * * * * * * 64 128 4 1\n";
+
+std::mutex g_table_mu;
+std::vector<RegimeRow> g_table;
+bool g_table_loaded = false;
+
+bool parse_field_i(const std::string& s, int64_t* v) {
+  if (s == "*") {
+    *v = -1;
+    return true;
+  }
+  char* end = nullptr;
+  *v = std::strtoll(s.c_str(), &end, 10);
+  return end && *end == 0;
+}
+bool parse_field_d(const std::string& s, double* v) {
+  if (s == "*") {
+    *v = -1.0;
+    return true;
+  }
+  char* end = nullptr;
+  *v = std::strtod(s.c_str(), &end);
+  return end && *end == 0;
+}
+
+bool parse_table(const std::string& text, std::vector<RegimeRow>* out, std::string* why) {
+  std::istringstream in(text);
+  std::string line;
+  int lineno = 0;
+  std::vector<RegimeRow> rows;
+  while (std::getline(in, line)) {
+    ++lineno;
+    const size_t hash = line.find('#');
+    if (hash != std::string::npos) line = line.substr(0, hash);
+    std::istringstream ls(line);
+    std::vector<std::string> f;
+    std::string tok;
+    while (ls >> tok) f.push_back(tok);
+    if (f.empty()) continue;
+    if (f.size() != 11) {
+      *why = "line " + std::to_string(lineno) + ": expected 11 fields";
+      return false;
+    }
+    int64_t kind, bq, bk, nmin, nmax, d, bn, st, ct;
+    double dmin, dmax;
+    if (!parse_field_i(f[0], &kind) || !parse_field_i(f[1], &bq) || !parse_field_i(f[2], &bk) ||
+        !parse_field_i(f[3], &nmin) || !parse_field_i(f[4], &nmax) ||
+        !parse_field_d(f[5], &dmin) || !parse_field_d(f[6], &dmax) || !parse_field_i(f[7], &d) ||
+        !parse_field_i(f[8], &bn) || !parse_field_i(f[9], &st) || !parse_field_i(f[10], &ct) ||
+        bn < 0 || st < 0 || ct < 0) {
+      *why = "line " + std::to_string(lineno) + ": bad field";
+      return false;
+    }
+    rows.push_back(RegimeRow{static_cast<int>(kind), static_cast<int>(bq), static_cast<int>(bk),
+                             nmin, nmax, dmin, dmax, static_cast<int>(d), static_cast<int>(bn),
+                             static_cast<int>(st), static_cast<int>(ct)});
+  }
+  *out = rows;
+  return true;
+}
+
+bool rows_valid(const std::vector<RegimeRow>& rows) {
+  for (const RegimeRow& r : rows)
+    if ((r.bn != 64 && r.bn != 128) || (r.d != 64 && r.d != 128) ||
+        !variant_exists(r.d, r.bn, r.stages, r.ctas))
+      return false;
+  return true;
+}
+
+void ensure_table() {
+  if (g_table_loaded) return;
+  std::string why;
+  const char* env = std::getenv("TSR_REGIME_TABLE");
+  if (env && *env) {
+    std::ifstream f(env);
+    std::stringstream ss;
+    ss << f.rdbuf();
+    std::vector<RegimeRow> rows;
+    if (f && parse_table(ss.str(), &rows, &why) && rows_valid(rows)) {
+      g_table = rows;
+      g_table_loaded = true;
+      return;
+    }
+  }
+  parse_table(kBuiltinTable, &g_table, &why);
+  g_table_loaded = true;
+}
+
+}  // namespace
+
+Regime regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N, double density, int32_t d) {
+  std::lock_guard<std::mutex> lk(g_table_mu);
+  ensure_table();
+  for (size_t i = 0; i < g_table.size(); ++i) {
+    const RegimeRow& r = g_table[i];
+    if (r.kind >= 0 && r.kind != kind) continue;
+    if (r.bq >= 0 && r.bq != bq) continue;
+    if (r.bk >= 0 && r.bk != bk) continue;
+    if (r.n_min >= 0 && N < r.n_min) continue;
+    if (r.n_max >= 0 && N > r.n_max) continue;
+    if (r.d_min >= 0 && density < r.d_min) continue;
+    if (r.d_max >= 0 && density >= r.d_max) continue;
+    if (r.d >= 0 && r.d != d) continue;
+    return Regime{r.bn, r.stages, r.ctas, static_cast<int32_t>(i)};
+  }
+  return Regime{128, d == 64 ? 4 : 3, 1, -1};
+}
+
+}  // namespace tsr
+
+using namespace tsr;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tsr_status check_mask(const tsr_mask* m) {
+  if (!m) return fail(TSR_ERR_INVALID_ARG, "mask is NULL");
+  if (m->B <= 0 || m->H <= 0 || m->N <= 0) return fail(TSR_ERR_INVALID_ARG, "B, H, N must be > 0");
+  if (m->d != 64 && m->d != 128) return fail(TSR_ERR_INVALID_ARG, "d must be 64 or 128");
+  if (m->N > (1 << 24)) return fail(TSR_ERR_UNSUPPORTED, "N above 2^24");
+  if (static_cast<int64_t>(m->B) * m->H > (1 << 20)) return fail(TSR_ERR_UNSUPPORTED, "B*H above 2^20");
+  switch (m->kind) {
+    case TSR_MASK_UNIFORM:
+      if (m->bq < 16 || m->bk < 16) return fail(TSR_ERR_INVALID_ARG, "bq, bk must be >= 16");
+      if (!m->blocks) return fail(TSR_ERR_INVALID_ARG, "blocks is NULL");
+      return TSR_OK;
+    case TSR_MASK_SEGMENTS:
+      if (m->n_qseg <= 0 || m->n_kseg <= 0 || !m->q_bounds || !m->k_bounds || !m->blocks)
+        return fail(TSR_ERR_INVALID_ARG, "segment bounds / blocks missing");
+      return TSR_OK;
+    case TSR_MASK_SVG:
+      if (m->n_frames <= 0 || m->frame_size <= 0 ||
+          static_cast<int64_t>(m->n_frames) * m->frame_size != m->N || !m->head_kind)
+        return fail(TSR_ERR_INVALID_ARG, "SVG needs N = n_frames * frame_size and head_kind");
+      return TSR_OK;
+    case TSR_MASK_KEYLIST:
+      return fail(TSR_ERR_UNSUPPORTED, "KEYLIST masks are not built in this version");
+    default:
+      return fail(TSR_ERR_INVALID_ARG, "unknown mask kind");
+  }
+}
+
+tsr_status check_bounds(const int32_t* dev, int32_t n, int32_t N, cudaStream_t st) {
+  std::vector<int32_t> h(static_cast<size_t>(n) + 1);
+  TSR_CUDA(cudaMemcpyAsync(h.data(), dev, sizeof(int32_t) * (n + 1), cudaMemcpyDeviceToHost, st));
+  TSR_CUDA(cudaStreamSynchronize(st));
+  if (h[0] != 0 || h[n] != N) return fail(TSR_ERR_INVALID_ARG, "segment bounds must run 0 .. N");
+  for (int32_t i = 0; i < n; ++i)
+    if (h[i + 1] <= h[i]) return fail(TSR_ERR_INVALID_ARG, "segment bounds must ascend");
+  return TSR_OK;
+}
+
+void free_plan(tsr_plan_s* P) {
+  if (!P) return;
+  cudaFree(P->items);
+  cudaFree(P->entries);
+  cudaFree(P->descs);
+  cudaFree(P->gidx);
+  cudaFree(P->counter);
+  cudaFree(P->err);
+  cudaFree(P->head_kind_dev);
+  cudaFree(P->scratch);
+  delete P;
+}
+
+// Device buffers of tsr_attention_host, kept per thread and grown on demand.
+struct HostCache {
+  void* buf[8] = {nullptr};
+  size_t cap[8] = {0};
+  cudaStream_t stream = nullptr;
+  int device = -1;
+  void release() {
+    for (int i = 0; i < 8; ++i) {
+      cudaFree(buf[i]);
+      buf[i] = nullptr;
+      cap[i] = 0;
+    }
+    if (stream) cudaStreamDestroy(stream);
+    stream = nullptr;
+    device = -1;
+  }
+  ~HostCache() { release(); }
+  tsr_status get(int slot, size_t bytes, void** p) {
+    if (bytes == 0) bytes = 16;
+    if (cap[slot] < bytes) {
+      cudaFree(buf[slot]);
+      buf[slot] = nullptr;
+      cap[slot] = 0;
+      const cudaError_t e = cudaMalloc(&buf[slot], bytes);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(TSR_ERR_OOM, "device buffer for host call");
+      }
+      cap[slot] = bytes;
+    }
+    *p = buf[slot];
+    return TSR_OK;
+  }
+};
+thread_local HostCache g_host_cache;
+
+}  // namespace
+
+extern "C" {
+
+int32_t tsr_abi_version(void) { return TSR_ABI_VERSION; }
+
+const char* tsr_status_string(tsr_status s) {
+  switch (s) {
+    case TSR_OK: return "ok";
+    case TSR_ERR_INVALID_ARG: return "invalid argument";
+    case TSR_ERR_UNSUPPORTED: return "unsupported";
+    case TSR_ERR_CUDA: return "CUDA error";
+    case TSR_ERR_OOM: return "out of memory";
+    case TSR_ERR_TIMEOUT: return "device wait timed out";
+    case TSR_ERR_INTERNAL: return "internal error";
+  }
+  return "unknown status";
+}
+
+const char* tsr_last_error(void) { return last_error_cstr(); }
+
+tsr_status tsr_plan(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_t* out,
+                    void* stream) {
+  set_error("");
+  if (!out) return fail(TSR_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (tsr_status s = check_mask(mask)) return s;
+  if (opts && opts->bn && opts->bn != 64 && opts->bn != 128)
+    return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
+  if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
+  struct Guard {
+    tsr_plan_s* p;
+    ~Guard() { free_plan(p); }
+  } guard{P};
+  TSR_CUDA(cudaGetDevice(&P->device));
+  P->B = mask->B;
+  P->H = mask->H;
+  P->N = mask->N;
+  P->d = mask->d;
+  P->kind = mask->kind;
+  P->flags = opts ? opts->flags : 0;
+  P->head_layout.assign(mask->H, 0);
+  if (mask->kind == TSR_MASK_SEGMENTS) {
+    if (tsr_status s = check_bounds(mask->q_bounds, mask->n_qseg, mask->N, st)) return s;
+    if (tsr_status s = check_bounds(mask->k_bounds, mask->n_kseg, mask->N, st)) return s;
+  }
+  if (mask->kind == TSR_MASK_SVG) {
+    TSR_CUDA(cudaMemcpyAsync(P->head_layout.data(), mask->head_kind, mask->H,
+                             cudaMemcpyDeviceToHost, st));
+    TSR_CUDA(cudaStreamSynchronize(st));
+    for (int32_t h = 0; h < mask->H; ++h) {
+      if (P->head_layout[h] != TSR_HEAD_SPATIAL && P->head_layout[h] != TSR_HEAD_TEMPORAL)
+        return fail(TSR_ERR_INVALID_ARG, "head_kind values must be 0 or 1");
+      P->n_temporal += P->head_layout[h];
+    }
+    P->F = mask->n_frames;
+    P->S = mask->frame_size;
+    TSR_CUDA(cudaMalloc(&P->head_kind_dev, mask->H));
+    TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, P->head_layout.data(), mask->H,
+                             cudaMemcpyHostToDevice, st));
+  }
+  TSR_CUDA(cudaMalloc(&P->counter, sizeof(int32_t)));
+  TSR_CUDA(cudaMalloc(&P->err, sizeof(uint32_t)));
+  TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), st));
+  if (tsr_status s = plan_build(mask, opts, P, st)) return s;
+  if (P->n_temporal > 0) {
+    P->scratch_bytes = static_cast<size_t>(P->B) * P->H * P->N * P->d * 2;
+    const cudaError_t e = cudaMalloc(&P->scratch, 3 * P->scratch_bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(TSR_ERR_OOM, "temporal-major scratch allocation failed");
+    }
+  }
+  guard.p = nullptr;
+  *out = P;
+  return TSR_OK;
+}
+
+tsr_status tsr_plan_destroy(tsr_plan_t plan) {
+  free_plan(plan);
+  return TSR_OK;
+}
+
+tsr_status tsr_plan_device_status(tsr_plan_t plan, void* stream) {
+  if (!plan) return fail(TSR_ERR_INVALID_ARG, "plan is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t e = 0;
+  TSR_CUDA(cudaMemcpyAsync(&e, plan->err, sizeof e, cudaMemcpyDeviceToHost, st));
+  TSR_CUDA(cudaMemsetAsync(plan->err, 0, sizeof(uint32_t), st));
+  TSR_CUDA(cudaStreamSynchronize(st));
+  if (e & DEV_ERR_TIMEOUT) return fail(TSR_ERR_TIMEOUT, "a device-side wait timed out");
+  if (e) return fail(TSR_ERR_INTERNAL, "device error word " + std::to_string(e));
+  return TSR_OK;
+}
+
+tsr_status tsr_bsa_forward(const void* q, const void* k, const void* v, tsr_plan_t plan, void* out,
+                           float* lse, void* stream) {
+  if (!plan) return fail(TSR_ERR_INVALID_ARG, "plan is NULL");
+  if (!q || !k || !v || !out || !lse) return fail(TSR_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(TSR_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (out == q || out == k || out == v) return fail(TSR_ERR_INVALID_ARG, "out aliases an input");
+  int dev = 0;
+  TSR_CUDA(cudaGetDevice(&dev));
+  if (dev != plan->device) return fail(TSR_ERR_INVALID_ARG, "plan was made on another device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.qs = a.ks = a.vs = nullptr;
+  a.out = out;
+  a.lse = lse;
+  a.plan = plan;
+  if (plan->n_temporal > 0) {
+    uint8_t* s = static_cast<uint8_t*>(plan->scratch);
+    a.qs = s;
+    a.ks = s + plan->scratch_bytes;
+    a.vs = s + 2 * plan->scratch_bytes;
+    const int32_t rb = plan->d * 2;
+    const int8_t* hk = plan->head_layout.data();
+    if (tsr_status e = launch_permute(q, s, plan->B, plan->H, plan->F, plan->S, rb, hk, 0, st))
+      return e;
+    if (tsr_status e = launch_permute(k, s + plan->scratch_bytes, plan->B, plan->H, plan->F,
+                                      plan->S, rb, hk, 0, st))
+      return e;
+    if (tsr_status e = launch_permute(v, s + 2 * plan->scratch_bytes, plan->B, plan->H, plan->F,
+                                      plan->S, rb, hk, 0, st))
+      return e;
+  }
+  if (tsr_status e = launch_forward(a, st)) return e;
+  if (plan->flags & TSR_PLAN_SYNC_CHECK) return tsr_plan_device_status(plan, stream);
+  return TSR_OK;
+}
+
+tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
+  if (!plan || !s) return fail(TSR_ERR_INVALID_ARG, "NULL argument");
+  memset(s, 0, sizeof *s);
+  s->bm = kBM;
+  s->bn = plan->bn;
+  s->stages = plan->stages;
+  s->ctas_per_sm = plan->ctas;
+  s->gathered = plan->gathered;
+  s->n_temporal_heads = plan->n_temporal;
+  s->n_items = plan->n_items;
+  s->n_entries = plan->n_entries;
+  s->n_boundary = plan->n_desc;
+  s->n_logical_on = plan->n_logical_on;
+  s->n_logical_total = plan->n_logical_total;
+  s->max_item_len = plan->max_item_len;
+  s->regime_id = plan->regime_id;
+  return TSR_OK;
+}
+
+tsr_status tsr_plan_export(tsr_plan_t plan, void* host_buf, size_t* bytes) {
+  if (!plan || !bytes) return fail(TSR_ERR_INVALID_ARG, "NULL argument");
+  const size_t need = sizeof(tsr_export_header) + sizeof(tsr_plan_item) * plan->n_items +
+                      sizeof(tsr_plan_entry) * plan->n_entries +
+                      sizeof(tsr_tile_desc) * plan->n_desc + 4 * plan->n_gidx + plan->H;
+  if (!host_buf) {
+    *bytes = need;
+    return TSR_OK;
+  }
+  if (*bytes < need) return fail(TSR_ERR_INVALID_ARG, "export buffer too small");
+  TSR_CUDA(cudaDeviceSynchronize());
+  uint8_t* o = static_cast<uint8_t*>(host_buf);
+  tsr_export_header h;
+  memset(&h, 0, sizeof h);
+  memcpy(h.magic, "TSRP", 4);
+  h.version = 1;
+  h.B = plan->B;
+  h.H = plan->H;
+  h.N = plan->N;
+  h.d = plan->d;
+  h.bm = kBM;
+  h.bn = plan->bn;
+  h.gathered = plan->gathered;
+  h.n_frames = plan->n_temporal ? plan->F : 0;
+  h.frame_size = plan->n_temporal ? plan->S : 0;
+  h.slice_m = plan->slice_m;
+  h.n_items = plan->n_items;
+  h.n_entries = plan->n_entries;
+  h.n_desc = plan->n_desc;
+  h.n_gidx = plan->n_gidx;
+  memcpy(o, &h, sizeof h);
+  size_t off = sizeof h;
+  auto pull = [&](const void* src, size_t n) -> cudaError_t {
+    cudaError_t e = cudaSuccess;
+    if (n) e = cudaMemcpy(o + off, src, n, cudaMemcpyDeviceToHost);
+    off += n;
+    return e;
+  };
+  TSR_CUDA(pull(plan->items, sizeof(tsr_plan_item) * plan->n_items));
+  TSR_CUDA(pull(plan->entries, sizeof(tsr_plan_entry) * plan->n_entries));
+  TSR_CUDA(pull(plan->descs, sizeof(tsr_tile_desc) * plan->n_desc));
+  TSR_CUDA(pull(plan->gidx, 4 * plan->n_gidx));
+  memcpy(o + off, plan->head_layout.data(), plan->H);
+  off += plan->H;
+  *bytes = off;
+  return TSR_OK;
+}
+
+tsr_status tsr_temporal_permute(const void* src, void* dst, int32_t B, int32_t H,
+                                int32_t n_frames, int32_t frame_size, int32_t row_bytes,
+                                const int8_t* head_kind, int32_t inverse, void* stream) {
+  if (!src || !dst) return fail(TSR_ERR_INVALID_ARG, "NULL pointer");
+  if (B <= 0 || H <= 0 || n_frames <= 0 || frame_size <= 0 || row_bytes <= 0 || row_bytes % 16)
+    return fail(TSR_ERR_INVALID_ARG, "bad shape (row_bytes must be a positive multiple of 16)");
+  if (static_cast<int64_t>(n_frames) * frame_size > (1 << 30))
+    return fail(TSR_ERR_UNSUPPORTED, "too many tokens");
+  if (!aligned16(src) || !aligned16(dst))
+    return fail(TSR_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const size_t bytes = static_cast<size_t>(B) * H * n_frames * frame_size * row_bytes;
+  const uint8_t* a = static_cast<const uint8_t*>(src);
+  const uint8_t* b = static_cast<const uint8_t*>(dst);
+  if (a < b + bytes && b < a + bytes) return fail(TSR_ERR_INVALID_ARG, "src and dst overlap");
+  return launch_permute(src, dst, B, H, n_frames, frame_size, row_bytes, head_kind, inverse,
+                        static_cast<cudaStream_t>(stream));
+}
+
+tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, const void* q,
+                              const void* k, const void* v, void* out, float* lse) {
+  set_error("");
+  if (tsr_status s = check_mask(mask)) return s;
+  if (!q || !k || !v || !out || !lse) return fail(TSR_ERR_INVALID_ARG, "NULL tensor pointer");
+  HostCache& hc = g_host_cache;
+  int dev = 0;
+  TSR_CUDA(cudaGetDevice(&dev));
+  if (hc.device != dev) {
+    hc.release();
+    hc.device = dev;
+  }
+  if (!hc.stream) TSR_CUDA(cudaStreamCreateWithFlags(&hc.stream, cudaStreamNonBlocking));
+  cudaStream_t st = hc.stream;
+  const size_t tb = static_cast<size_t>(mask->B) * mask->H * mask->N * mask->d * 2;
+  const size_t lb = static_cast<size_t>(mask->B) * mask->H * mask->N * 4;
+  void *dq, *dk, *dv, *dout, *dlse;
+  if (tsr_status s = hc.get(0, tb, &dq)) return s;
+  if (tsr_status s = hc.get(1, tb, &dk)) return s;
+  if (tsr_status s = hc.get(2, tb, &dv)) return s;
+  if (tsr_status s = hc.get(3, tb, &dout)) return s;
+  if (tsr_status s = hc.get(4, lb, &dlse)) return s;
+  tsr_mask dm = *mask;
+  if (mask->kind == TSR_MASK_UNIFORM || mask->kind == TSR_MASK_SEGMENTS) {
+    size_t nb;
+    if (mask->kind == TSR_MASK_UNIFORM)
+      nb = static_cast<size_t>(mask->B) * mask->H * ((mask->N + mask->bq - 1) / mask->bq) *
+           ((mask->N + mask->bk - 1) / mask->bk);
+    else
+      nb = static_cast<size_t>(mask->B) * mask->H * mask->n_qseg * mask->n_kseg;
+    void* db;
+    if (tsr_status s = hc.get(5, nb, &db)) return s;
+    TSR_CUDA(cudaMemcpyAsync(db, mask->blocks, nb, cudaMemcpyHostToDevice, st));
+    dm.blocks = static_cast<const uint8_t*>(db);
+    if (mask->kind == TSR_MASK_SEGMENTS) {
+      void* dbnd;
+      const size_t nq = mask->n_qseg + 1, nk = mask->n_kseg + 1;
+      if (tsr_status s = hc.get(6, 4 * (nq + nk), &dbnd)) return s;
+      int32_t* p = static_cast<int32_t*>(dbnd);
+      TSR_CUDA(cudaMemcpyAsync(p, mask->q_bounds, 4 * nq, cudaMemcpyHostToDevice, st));
+      TSR_CUDA(cudaMemcpyAsync(p + nq, mask->k_bounds, 4 * nk, cudaMemcpyHostToDevice, st));
+      dm.q_bounds = p;
+      dm.k_bounds = p + nq;
+    }
+  } else if (mask->kind == TSR_MASK_SVG) {
+    void* dh;
+    if (tsr_status s = hc.get(7, mask->H, &dh)) return s;
+    TSR_CUDA(cudaMemcpyAsync(dh, mask->head_kind, mask->H, cudaMemcpyHostToDevice, st));
+    dm.head_kind = static_cast<const int8_t*>(dh);
+  }
+  TSR_CUDA(cudaMemcpyAsync(dq, q, tb, cudaMemcpyHostToDevice, st));
+  TSR_CUDA(cudaMemcpyAsync(dk, k, tb, cudaMemcpyHostToDevice, st));
+  TSR_CUDA(cudaMemcpyAsync(dv, v, tb, cudaMemcpyHostToDevice, st));
+  tsr_plan_t plan = nullptr;
+  if (tsr_status s = tsr_plan(&dm, opts, &plan, st)) return s;
+  tsr_status s = tsr_bsa_forward(dq, dk, dv, plan, dout, static_cast<float*>(dlse), st);
+  if (s == TSR_OK) {
+    const cudaError_t e1 = cudaMemcpyAsync(out, dout, tb, cudaMemcpyDeviceToHost, st);
+    const cudaError_t e2 = cudaMemcpyAsync(lse, dlse, lb, cudaMemcpyDeviceToHost, st);
+    const cudaError_t e3 = cudaStreamSynchronize(st);
+    if (e1 != cudaSuccess) s = cuda_fail(e1, "copy of out to host");
+    else if (e2 != cudaSuccess) s = cuda_fail(e2, "copy of lse to host");
+    else if (e3 != cudaSuccess) s = cuda_fail(e3, "stream synchronize");
+  }
+  if (s == TSR_OK) s = tsr_plan_device_status(plan, st);
+  tsr_plan_destroy(plan);
+  return s;
+}
+
+void tsr_release_host_buffers(void) { g_host_cache.release(); }
+
+tsr_status tsr_regime_load(const char* path) {
+  std::lock_guard<std::mutex> lk(g_table_mu);
+  std::string why;
+  if (!path) {
+    parse_table(kBuiltinTable, &g_table, &why);
+    g_table_loaded = true;
+    return TSR_OK;
+  }
+  std::ifstream f(path);
+  if (!f) return fail(TSR_ERR_INVALID_ARG, std::string("cannot open regime table ") + path);
+  std::stringstream ss;
+  ss << f.rdbuf();
+  std::vector<RegimeRow> rows;
+  if (!parse_table(ss.str(), &rows, &why)) return fail(TSR_ERR_INVALID_ARG, "regime table: " + why);
+  if (!rows_valid(rows))
+    return fail(TSR_ERR_INVALID_ARG, "regime table names a kernel variant that does not exist");
+  g_table = rows;
+  g_table_loaded = true;
+  return TSR_OK;
+}
+
+tsr_status tsr_regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N, double density,
+                             tsr_regime* out) {
+  if (!out) return fail(TSR_ERR_INVALID_ARG, "out is NULL");
+  const Regime r = regime_lookup(kind, bq, bk, N, density, 128);
+  out->bn = r.bn;
+  out->stages = r.stages;
+  out->ctas_per_sm = r.ctas;
+  out->id = r.id;
+  return TSR_OK;
+}
+
+}  // extern "C"

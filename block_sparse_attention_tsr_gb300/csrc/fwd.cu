@@ -1,0 +1,560 @@
+// fwd.cu -- block-sparse attention forward on tcgen05 tensor cores.
+//
+// One persistent CTA per SM slot pulls work items (one 128-row query tile plus
+// its list of physical K/V tiles, longest first) from an atomic counter.  Inside
+// a CTA three roles run concurrently and hand data over through mbarriers:
+//
+//   warp 0      TMA producer: the query tile once per item, then the K and V
+//               tiles of the item's list through a STAGES-deep shared-memory ring.
+//               Empty tiles are not in the list, so they are never loaded
+//               (Splash digest, "Splash Attention": empty tiles are bypassed).
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (double buffered),
+//               then O += P V with P read from TMEM; QK of tile j+1 is issued
+//               before PV of tile j so the tensor pipe stays busy while the
+//               softmax of tile j runs.
+//   warps 2..5  softmax, one query row per thread (TMEM lane = row): scale,
+//               element mask on boundary tiles only (Splash digest: exact
+//               coordinate masking limited to boundary tiles), online softmax in
+//               fp32 with lazy rescaling, P to TMEM as bf16, and the epilogue
+//               O / l -> bf16, lse = m + ln l.  Rows that see no allowed key get
+//               O = 0 and lse = -inf.
+//
+// The arithmetic is the masked softmax attention of the Tessera abstract (block-
+// sparse attention over the logical mask, every named interaction kept); the
+// online (streaming) softmax is the standard one-pass rewrite of it.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tsr {
+
+namespace {
+
+struct FwdParams {
+  CUtensorMap tq, tk, tv;        // caller layout, 3-D {d, N, B*H}
+  CUtensorMap tq_p, tk_p, tv_p;  // temporal-major scratch copies (same shapes)
+  const int4* items;             // tsr_plan_item, 2 x int4 each
+  const int2* entries;
+  const uint4* descs;            // 32 B each
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* counter;
+  uint32_t* err;
+  int32_t n_items, N, F, S;
+  float scale_log2;              // log2(e) / sqrt(d)
+};
+
+// Rescale the running output only when the running maximum grew by more than
+// this many powers of two: P = 2^(x - m_ref) then stays below 2^8, far inside
+// bf16 and fp32 range, and O / l is unchanged because O and l share the factor.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct alignas(8) Ctrl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[8], v_full[8], kv_empty[8];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done, o_empty;
+  uint64_t item_full[2], item_empty[2];
+  uint64_t final_bar;
+  int32_t item_slot[2];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+template <int D, int BN, int STAGES>
+struct Cfg {
+  static constexpr int BM = kBM;
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int SMEM = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
+  static constexpr int TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
+  static constexpr int O_COL = 2 * BN;
+  static constexpr uint32_t IDESC_QK = idesc_bf16(128, BN, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
+  static_assert(STAGES >= 2 && STAGES <= 8, "stages");
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BN == 64 || BN == 128, "kv tile");
+};
+
+__device__ __forceinline__ int32_t unpermute(int32_t tp, int32_t F, int32_t S) {
+  return (tp % F) * S + tp / F;
+}
+
+__device__ __forceinline__ uint32_t desc_byte(const uint4& a, const uint4& b, int i) {
+  const uint32_t w = (i < 16) ? (&a.x)[i >> 2] : (&b.x)[(i - 16) >> 2];
+  return (w >> ((i & 3) * 8)) & 0xFFu;
+}
+
+// Columns [lo, hi) of a BN-bit mask, added to words[].
+template <int BN>
+__device__ __forceinline__ void add_range(uint32_t (&words)[BN / 32], int lo, int hi) {
+#pragma unroll
+  for (int w = 0; w < BN / 32; ++w) {
+    const int a = max(lo - 32 * w, 0), b = min(hi - 32 * w, 32);
+    if (a < b) {
+      const uint32_t hi_mask = (b == 32) ? 0xFFFFFFFFu : ((1u << b) - 1u);
+      words[w] |= hi_mask & ~((1u << a) - 1u);
+    }
+  }
+}
+
+template <int D, int BN, int STAGES, int CTAS>
+__global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Ctrl ctrl;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sK0 = base + C::Q_BYTES;
+  const uint32_t sV0 = sK0 + STAGES * C::KV_BYTES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int32_t* abort_flag = &ctrl.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctrl.q_full), 1);
+    mbar_init(smem_u32(&ctrl.q_empty), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctrl.k_full[s]), 1);
+      mbar_init(smem_u32(&ctrl.v_full[s]), 1);
+      mbar_init(smem_u32(&ctrl.kv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctrl.s_full[b]), 1);
+      mbar_init(smem_u32(&ctrl.p_full[b]), 4);
+      mbar_init(smem_u32(&ctrl.item_full[b]), 1);
+      mbar_init(smem_u32(&ctrl.item_empty[b]), 5);
+    }
+    mbar_init(smem_u32(&ctrl.pv_done), 1);
+    mbar_init(smem_u32(&ctrl.o_empty), 4);
+    mbar_init(smem_u32(&ctrl.final_bar), 1);
+    ctrl.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctrl.tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tq);
+      tma_prefetch_desc(&p.tk);
+      tma_prefetch_desc(&p.tv);
+    }
+    uint32_t item_seq = 0, kv_cnt = 0, q_cnt = 0;
+    bool ok = true;
+    while (ok) {
+      int32_t it = 0;
+      if (lane == 0) it = atomicAdd(p.counter, 1);
+      it = __shfl_sync(0xFFFFFFFFu, it, 0);
+      const bool done = it >= p.n_items;
+      const int slot = item_seq & 1;
+      if (!mbar_wait(smem_u32(&ctrl.item_empty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+      if (lane == 0) {
+        ctrl.item_slot[slot] = done ? -1 : it;
+        mbar_arrive(smem_u32(&ctrl.item_full[slot]));
+      }
+      ++item_seq;
+      if (done) break;
+      const int4 i0 = __ldg(&p.items[2 * it]);
+      const int4 i1 = __ldg(&p.items[2 * it + 1]);
+      const int32_t bh = i0.x, q_tile = i0.y, begin = i0.z, end = i0.w, layout = i1.x;
+      if (end <= begin) continue;
+      const CUtensorMap* mq = layout ? &p.tq_p : &p.tq;
+      const CUtensorMap* mk = layout ? &p.tk_p : &p.tk;
+      const CUtensorMap* mv = layout ? &p.tv_p : &p.tv;
+      if (!mbar_wait(smem_u32(&ctrl.q_empty), (q_cnt & 1) ^ 1, abort_flag, p.err)) break;
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&ctrl.q_full);
+        mbar_arrive_expect_tx(bar, C::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sQ + c * C::BM * 128, mq, bar, c * 64, q_tile * C::BM, bh);
+      }
+      ++q_cnt;
+      for (int32_t e = begin; e < end; ++e) {
+        const int s = kv_cnt % STAGES;
+        if (!mbar_wait(smem_u32(&ctrl.kv_empty[s]), ((kv_cnt / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const int32_t kv = __ldg(&p.entries[e]).x;
+          const uint32_t kb = smem_u32(&ctrl.k_full[s]), vb = smem_u32(&ctrl.v_full[s]);
+          const uint32_t sk = sK0 + s * C::KV_BYTES, sv = sV0 + s * C::KV_BYTES;
+          mbar_arrive_expect_tx(kb, C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(sk + c * BN * 128, mk, kb, c * 64, kv, bh);
+          mbar_arrive_expect_tx(vb, C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(sv + c * BN * 128, mv, vb, c * 64, kv, bh);
+        }
+        ++kv_cnt;
+      }
+    }
+    // On an abort, let the copies already issued land before the CTA exits.
+    if (*abort_flag) {
+      for (uint32_t k = (kv_cnt > STAGES ? kv_cnt - STAGES : 0); k < kv_cnt; ++k) {
+        const int s = k % STAGES;
+        volatile int32_t dummy = 0;
+        mbar_wait(smem_u32(&ctrl.k_full[s]), (k / STAGES) & 1, &dummy, p.err);
+        mbar_wait(smem_u32(&ctrl.v_full[s]), (k / STAGES) & 1, &dummy, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t item_seq = 0, kv_cnt = 0, t_cnt = 0, q_cnt = 0, o_cnt = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = item_seq & 1;
+        if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err)) break;
+        const int32_t it = ctrl.item_slot[slot];
+        mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
+        ++item_seq;
+        if (it < 0) break;
+        const int4 i0 = __ldg(&p.items[2 * it]);
+        const int32_t n = i0.w - i0.z;
+        if (n <= 0) continue;
+        if (!mbar_wait(smem_u32(&ctrl.q_full), q_cnt & 1, abort_flag, p.err)) break;
+        ++q_cnt;
+        tc_fence_after();
+        // O += P V for tile j of this item
+        auto issue_pv = [&](int32_t j) -> bool {
+          const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
+          const int s = kvi % STAGES;
+          if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err)) return false;
+          if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err)) return false;
+          if (j == 0) {
+            if (!mbar_wait(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1, abort_flag, p.err)) return false;
+            ++o_cnt;
+          }
+          tc_fence_after();
+          const uint32_t sv = sV0 + s * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(sv + kk * 16 * 128, BN * 128, 1024);
+            mma_bf16_ts(tmem + C::O_COL, tmem + (t & 1) * BN + kk * 8, bdesc, C::IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctrl.kv_empty[s]));
+          mma_commit(smem_u32(&ctrl.pv_done));
+          return true;
+        };
+        for (int32_t j = 0; j < n && ok; ++j) {
+          const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
+          const int s = kvi % STAGES;
+          if (!mbar_wait(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sk = sK0 + s * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t adesc = sdesc_sw128(sQ + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = sdesc_sw128(sk + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tmem + (t & 1) * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&ctrl.s_full[t & 1]));
+          if (j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
+          if (j > 0 && !issue_pv(j - 1)) ok = false;
+        }
+        if (ok && !issue_pv(n - 1)) ok = false;
+        t_cnt += n;
+        kv_cnt += n;
+      }
+      // every MMA issued has finished before TMEM is released
+      mma_commit(smem_u32(&ctrl.final_bar));
+      volatile int32_t dummy = 0;
+      mbar_wait(smem_u32(&ctrl.final_bar), 0, &dummy, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- softmax warps
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                    // tile row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t item_seq = 0, t_cnt = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = item_seq & 1;
+      if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err)) break;
+      const int32_t it = ctrl.item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
+      ++item_seq;
+      if (it < 0) break;
+      const int4 i0 = __ldg(&p.items[2 * it]);
+      const int4 i1 = __ldg(&p.items[2 * it + 1]);
+      const int32_t bh = i0.x, q_tile = i0.y, begin = i0.z, n = i0.w - i0.z, layout = i1.x;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int32_t j = 0; j < n; ++j) {
+        const uint32_t t = t_cnt + j;
+        const uint32_t sb = t & 1;
+        if (!mbar_wait(smem_u32(&ctrl.s_full[sb]), (t >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float x[BN];
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + sb * BN + c0, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(rr[i]);
+        }
+        tc_wait_ld();
+        const int32_t desc = __ldg(&p.entries[begin + j]).y;
+        if (desc >= 0) {
+          const uint4 d0 = __ldg(&p.descs[2 * desc]);
+          const uint4 d1 = __ldg(&p.descs[2 * desc + 1]);
+          const int n_r = d0.x & 0xFF, n_c = (d0.x >> 8) & 0xFF;
+          int rs = 0;
+#pragma unroll
+          for (int k = 1; k < 8; ++k)
+            if (k < n_r && static_cast<int>(desc_byte(d0, d1, 2 + k)) <= r) rs = k;
+          const uint64_t bits = (static_cast<uint64_t>(d1.w) << 32) | d1.z;
+          const uint32_t rb = static_cast<uint32_t>(bits >> (rs * 8)) & 0xFFu;
+          uint32_t words[BN / 32];
+#pragma unroll
+          for (int w = 0; w < BN / 32; ++w) words[w] = 0u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c < n_c && ((rb >> c) & 1u))
+              add_range<BN>(words, static_cast<int>(desc_byte(d0, d1, 10 + c)),
+                            static_cast<int>(desc_byte(d0, d1, 11 + c)));
+          }
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) mt = fmaxf(mt, x[c]);
+        mt *= p.scale_log2;
+        const float m_new = fmaxf(m_ref, mt);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        // O holds the sum over earlier tiles only when j > 0; it is exactly 0 for
+        // rows whose earlier tiles were fully masked (m_ref = -inf).
+        const bool fix_o = need && j > 0 && m_ref != -INFINITY;
+        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+        if (__any_sync(0xFFFFFFFFu, fix_o)) {
+          if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = fix_o ? alpha : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lane_off + C::O_COL + c0, rr);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+            tmem_st32(tmem + lane_off + C::O_COL + c0, rr);
+          }
+        }
+        if (need) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = ex2_approx(fmaf(x[c0 + 2 * i], p.scale_log2, -m_use));
+            const float b = ex2_approx(fmaf(x[c0 + 2 * i + 1], p.scale_log2, -m_use));
+            rowsum += a + b;
+            pk[i] = pack_bf16x2(a, b);
+          }
+          tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
+        }
+        l += rowsum;
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl.p_full[sb]));
+      }
+      if (!ok) break;
+      t_cnt += n;
+      // ----------------------------------------------------------- epilogue
+      const int32_t gr = q_tile * kBM + r;
+      const bool valid = gr < p.N;
+      const int32_t orow = layout ? unpermute(gr, p.F, p.S) : gr;
+      const size_t obase = (static_cast<size_t>(bh) * p.N + (valid ? orow : 0)) * D;
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if (n > 0) {
+        if (!mbar_wait(smem_u32(&ctrl.pv_done), (t_cnt - 1) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::O_COL + c0, rr);
+          tc_wait_ld();
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                                  __uint_as_float(rr[2 * i + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + obase + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl.o_empty));
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + obase);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (valid)
+        p.lse[static_cast<size_t>(bh) * p.N + orow] =
+            (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encode() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      fn == nullptr || q != cudaDriverEntryPointSuccess)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+template <int D, int BN, int STAGES, int CTAS>
+tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStream_t stream) {
+  using C = Cfg<D, BN, STAGES>;
+  auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS>;
+  static bool attr_set[64] = {false};
+  if (device < 0 || device >= 64 || !attr_set[device]) {
+    TSR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    if (device >= 0 && device < 64) attr_set[device] = true;
+  }
+  const int grid = std::min(n_items, num_sms(device) * CTAS);
+  if (grid <= 0) return TSR_OK;
+  kern<<<grid, 192, C::SMEM, stream>>>(prm);
+  TSR_CUDA(cudaGetLastError());
+  return TSR_OK;
+}
+
+constexpr int vkey(int d, int bn, int stages, int ctas) {
+  return d * 100000 + bn * 100 + stages * 10 + ctas;
+}
+
+}  // namespace
+
+bool encode_tmap_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool variant_exists(int d, int bn, int stages, int ctas) {
+  switch (vkey(d, bn, stages, ctas)) {
+    case vkey(128, 128, 3, 1):
+    case vkey(128, 128, 2, 1):
+    case vkey(128, 64, 4, 1):
+    case vkey(128, 64, 2, 2):
+    case vkey(64, 128, 4, 1):
+    case vkey(64, 64, 4, 1):
+    case vkey(64, 64, 3, 2):
+      return true;
+    default:
+      return false;
+  }
+}
+
+tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
+  const tsr_plan_impl* P = a.plan;
+  if (P->n_items == 0) return TSR_OK;
+  FwdParams prm;
+  memset(&prm, 0, sizeof prm);
+  const uint64_t D = P->d, N = P->N, BH = static_cast<uint64_t>(P->B) * P->H;
+  bool ok = encode_tmap_3d(&prm.tq, a.q, D, N, BH, 64, kBM) &&
+            encode_tmap_3d(&prm.tk, a.k, D, N, BH, 64, P->bn) &&
+            encode_tmap_3d(&prm.tv, a.v, D, N, BH, 64, P->bn);
+  if (P->n_temporal > 0) {
+    ok = ok && encode_tmap_3d(&prm.tq_p, a.qs, D, N, BH, 64, kBM) &&
+         encode_tmap_3d(&prm.tk_p, a.ks, D, N, BH, 64, P->bn) &&
+         encode_tmap_3d(&prm.tv_p, a.vs, D, N, BH, 64, P->bn);
+  } else {
+    prm.tq_p = prm.tq;
+    prm.tk_p = prm.tk;
+    prm.tv_p = prm.tv;
+  }
+  if (!ok) return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
+  prm.items = static_cast<const int4*>(P->items);
+  prm.entries = static_cast<const int2*>(P->entries);
+  prm.descs = static_cast<const uint4*>(P->descs);
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.lse = a.lse;
+  prm.counter = P->counter;
+  prm.err = P->err;
+  prm.n_items = static_cast<int32_t>(P->n_items);
+  prm.N = P->N;
+  prm.F = P->F;
+  prm.S = P->S;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P->d)));
+  TSR_CUDA(cudaMemsetAsync(P->counter, 0, sizeof(int32_t), stream));
+  const int n = static_cast<int>(P->n_items), dev = P->device;
+  switch (vkey(P->d, P->bn, P->stages, P->ctas)) {
+    case vkey(128, 128, 3, 1): return launch_variant<128, 128, 3, 1>(prm, n, dev, stream);
+    case vkey(128, 128, 2, 1): return launch_variant<128, 128, 2, 1>(prm, n, dev, stream);
+    case vkey(128, 64, 4, 1): return launch_variant<128, 64, 4, 1>(prm, n, dev, stream);
+    case vkey(128, 64, 2, 2): return launch_variant<128, 64, 2, 2>(prm, n, dev, stream);
+    case vkey(64, 128, 4, 1): return launch_variant<64, 128, 4, 1>(prm, n, dev, stream);
+    case vkey(64, 64, 4, 1): return launch_variant<64, 64, 4, 1>(prm, n, dev, stream);
+    case vkey(64, 64, 3, 2): return launch_variant<64, 64, 3, 2>(prm, n, dev, stream);
+    default:
+      return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) +
+                                           " bn=" + std::to_string(P->bn) + " stages=" +
+                                           std::to_string(P->stages) + " ctas=" +
+                                           std::to_string(P->ctas));
+  }
+}
+
+}  // namespace tsr

@@ -1,0 +1,104 @@
+// internal.h -- library-private declarations shared by the .cu files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/tsr.h"
+
+namespace tsr {
+
+constexpr int kBM = 128;  // query rows per physical tile (the tcgen05 M = 128 datapath)
+
+void set_error(const std::string& msg);
+const char* last_error_cstr();
+tsr_status fail(tsr_status s, const std::string& msg);
+tsr_status cuda_fail(cudaError_t e, const char* what);
+
+#define TSR_CUDA(expr)                                  \
+  do {                                                  \
+    cudaError_t e_ = (expr);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+  } while (0)
+
+// Logical mask as the planner kernels see it (device pointers).
+struct MaskDev {
+  int32_t kind, B, H, N;
+  int32_t bq, bk;
+  int32_t n_qseg, n_kseg;
+  const int32_t* q_bounds;
+  const int32_t* k_bounds;
+  const uint8_t* blocks;
+  int32_t F, S;
+  const int8_t* head_kind;   // device copy, [H]
+  int32_t slice_m;
+  const int64_t* indptr;
+  const int32_t* indices;
+};
+
+struct Regime {
+  int32_t bn, stages, ctas, id;
+};
+
+struct tsr_plan_impl {
+  int device = 0;
+  int32_t B = 0, H = 0, N = 0, d = 0;
+  int32_t kind = 0;
+  int32_t bn = 128, stages = 3, ctas = 1, regime_id = -1;
+  int32_t gathered = 0, slice_m = 0;
+  int32_t F = 0, S = 0;
+  int32_t flags = 0;
+  int64_t n_items = 0, n_entries = 0, n_desc = 0, n_gidx = 0;
+  int64_t n_logical_on = 0, n_logical_total = 0, max_item_len = 0;
+  std::vector<int8_t> head_layout;  // host copy: 1 = temporal-major
+  int32_t n_temporal = 0;
+  // device buffers (owned)
+  void* items = nullptr;     // tsr_plan_item [n_items]
+  void* entries = nullptr;   // tsr_plan_entry [n_entries]
+  void* descs = nullptr;     // 32 B [n_desc]
+  int32_t* gidx = nullptr;   // [n_gidx]
+  int32_t* counter = nullptr;
+  uint32_t* err = nullptr;
+  int8_t* head_kind_dev = nullptr;
+  void* scratch = nullptr;   // temporal-major Q, K, V copies: 3 x [B][H][N][d] bf16
+  size_t scratch_bytes = 0;
+};
+
+// planner (plan.cu)
+tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
+                      cudaStream_t stream);
+
+// forward kernels (fwd.cu)
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* qs;   // temporal-major scratch copies (or null)
+  const void* ks;
+  const void* vs;
+  void* out;
+  float* lse;
+  const tsr_plan_impl* plan;
+};
+tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream);
+bool variant_exists(int d, int bn, int stages, int ctas);
+
+// permutation (permute.cu)
+tsr_status launch_permute(const void* src, void* dst, int32_t B, int32_t H, int32_t F, int32_t S,
+                          int32_t row_bytes, const int8_t* head_kind_host, int32_t inverse,
+                          cudaStream_t stream);
+
+// regime table (api.cu)
+Regime regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N, double density, int32_t d);
+
+// tensor maps (fwd.cu)
+bool encode_tmap_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t outer, uint32_t box_inner, uint32_t box_rows);
+
+int num_sms(int device);
+
+}  // namespace tsr
+
+struct tsr_plan_s : tsr::tsr_plan_impl {};

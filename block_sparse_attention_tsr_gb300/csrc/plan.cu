@@ -1,0 +1,440 @@
+// plan.cu -- physical mapping and task organisation on the GPU.
+//
+// Tessera abstract: a mapping layer keeps, merges or cuts logical blocks into
+// physical tiles that suit the mask and the GPU, and a task layer groups the
+// tiles into GPU tasks.  Here every physical tile is 128 query rows (the
+// tcgen05 M = 128 datapath) by BN keys (64 or 128):
+//   * logical blocks of 128 x 128 (BN = 128) map one-to-one (kept),
+//   * smaller blocks (32, 64, frames of 21 tokens) are merged into a tile,
+//   * larger blocks (256, 1,560-token frames) are cut into several tiles.
+// Each tile is classified from the logical segments that overlap it:
+//   empty    -> dropped (never loaded or computed),
+//   full     -> every element allowed and every key in range: no masking,
+//   boundary -> mixed, or crossing N: a 32-byte descriptor (row segments x
+//               column segments bit grid) drives element masking.
+// (Splash digest, "Splash Attention": skip empty tiles, exact masking only on
+// boundary tiles.)  The task layer gives every 128-row query tile one work item
+// holding its tiles in key order; items are ordered longest first so that a
+// persistent grid finishes evenly, and the regime table picks the tile width and
+// pipeline depth.  Three kernels: count (both tile widths, so the regime can be
+// chosen from the counts), schedule (one block: prefix sums + longest-first
+// order), emit (tiles and descriptors).
+#include <algorithm>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tsr {
+
+namespace {
+
+constexpr int kMaxSeg = 8;
+
+// Logical segments of one axis (0 = queries, 1 = keys) that overlap tokens
+// [t0, t1) of head h.  ids[] receive segment ids, starts[] the first token of
+// each relative to t0, starts[n] = t1 - t0.  Returns the count, or -1 if more
+// than kMaxSeg segments overlap.
+__device__ int tile_segments(const MaskDev& m, int h, int axis, int t0, int t1, int* ids,
+                             int* starts) {
+  int n = 0;
+  if (m.kind == TSR_MASK_SEGMENTS) {
+    const int32_t* bd = axis ? m.k_bounds : m.q_bounds;
+    const int ns = axis ? m.n_kseg : m.n_qseg;
+    int lo = 0, hi = ns - 1;  // last segment whose start <= t0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bd[mid] <= t0) lo = mid; else hi = mid - 1;
+    }
+    for (int id = lo; id < ns && bd[id] < t1; ++id) {
+      if (n == kMaxSeg) return -1;
+      ids[n] = id;
+      starts[n] = max(bd[id], t0) - t0;
+      ++n;
+    }
+  } else {
+    int size;
+    if (m.kind == TSR_MASK_UNIFORM) size = axis ? m.bk : m.bq;
+    else size = (m.head_kind[h] == TSR_HEAD_TEMPORAL) ? m.F : m.S;  // SVG
+    for (int id = t0 / size; id * size < t1; ++id) {
+      if (n == kMaxSeg) return -1;
+      ids[n] = id;
+      starts[n] = max(id * size, t0) - t0;
+      ++n;
+    }
+  }
+  starts[n] = t1 - t0;
+  return n;
+}
+
+__device__ __forceinline__ bool seg_allowed(const MaskDev& m, int bh, int h, int qid, int kid,
+                                            int64_t nqs, int64_t nks) {
+  if (m.kind == TSR_MASK_SVG) {
+    if (m.head_kind[h] == TSR_HEAD_TEMPORAL) return qid == kid;  // same spatial index
+    return qid == kid || kid == 0;                                // same frame, or frame 0
+  }
+  return m.blocks[(static_cast<int64_t>(bh) * nqs + qid) * nks + kid] != 0;
+}
+
+struct RowSegs {
+  int n;
+  int ids[kMaxSeg];
+  int starts[kMaxSeg + 1];
+};
+
+// 0 empty, 1 full, 2 boundary, -1 unsupported.  desc is filled for boundary tiles.
+__device__ int classify(const MaskDev& m, int bh, int h, const RowSegs& rs, int k0, int bn,
+                        int64_t nqs, int64_t nks, tsr_tile_desc* desc) {
+  if (k0 >= m.N) return 0;
+  const int k1 = min(m.N, k0 + bn);
+  int cid[kMaxSeg], cst[kMaxSeg + 1];
+  const int nc = tile_segments(m, h, 1, k0, k1, cid, cst);
+  if (nc < 0 || rs.n < 0) return -1;
+  uint64_t bits = 0;
+  bool any = false, all = true;
+  for (int r = 0; r < rs.n; ++r)
+    for (int c = 0; c < nc; ++c) {
+      const bool a = seg_allowed(m, bh, h, rs.ids[r], cid[c], nqs, nks);
+      any |= a;
+      all &= a;
+      if (a) bits |= 1ull << (r * 8 + c);
+    }
+  if (!any) return 0;
+  if (all && k1 - k0 == bn) return 1;
+  if (desc) {
+    memset(desc, 0, sizeof(*desc));
+    desc->n_r = static_cast<uint8_t>(rs.n);
+    desc->n_c = static_cast<uint8_t>(nc);
+    for (int r = 0; r < rs.n; ++r) desc->r_start[r] = static_cast<uint8_t>(rs.starts[r]);
+    for (int c = 0; c <= nc; ++c) desc->c_start[c] = static_cast<uint8_t>(cst[c]);
+    desc->bits = bits;
+  }
+  return 2;
+}
+
+__device__ void grid_dims(const MaskDev& m, int64_t* nqs, int64_t* nks) {
+  if (m.kind == TSR_MASK_UNIFORM) {
+    *nqs = (m.N + m.bq - 1) / m.bq;
+    *nks = (m.N + m.bk - 1) / m.bk;
+  } else if (m.kind == TSR_MASK_SEGMENTS) {
+    *nqs = m.n_qseg;
+    *nks = m.n_kseg;
+  } else {
+    *nqs = *nks = 0;
+  }
+}
+
+// Per query tile: [0] tiles at BN=64, [1] boundary tiles at BN=64, [2] tiles at
+// BN=128, [3] boundary at BN=128.  Totals: the same four sums, then [4], [5] the
+// longest item at BN=64 / 128, [6] allowed logical blocks.
+__global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
+                                  uint32_t* err) {
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
+  if (warp >= n_items) return;
+  const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
+  RowSegs rs;
+  rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
+  int64_t nqs, nks;
+  grid_dims(m, &nqs, &nks);
+  const int nkt128 = (m.N + 127) / 128;
+  int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
+  bool bad = false;
+  for (int kt = lane; kt < nkt128; kt += 32) {
+    const int ca = classify(m, bh, h, rs, kt * 128, 64, nqs, nks, nullptr);
+    const int cb = classify(m, bh, h, rs, kt * 128 + 64, 64, nqs, nks, nullptr);
+    if (ca < 0 || cb < 0) {
+      bad = true;
+      continue;
+    }
+    e64 += (ca != 0) + (cb != 0);
+    b64 += (ca == 2) + (cb == 2);
+    if (ca != 0 || cb != 0) {
+      ++e128;
+      if (!(ca == 1 && cb == 1)) ++b128;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    e64 += __shfl_xor_sync(0xFFFFFFFFu, e64, o);
+    b64 += __shfl_xor_sync(0xFFFFFFFFu, b64, o);
+    e128 += __shfl_xor_sync(0xFFFFFFFFu, e128, o);
+    b128 += __shfl_xor_sync(0xFFFFFFFFu, b128, o);
+  }
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+    if (lane == 0) atomicOr(err, DEV_ERR_UNSUPPORTED);
+    return;
+  }
+  if (lane == 0) {
+    cnt[0 * n_items + warp] = e64;
+    cnt[1 * n_items + warp] = b64;
+    cnt[2 * n_items + warp] = e128;
+    cnt[3 * n_items + warp] = b128;
+    atomicAdd(&tot[0], static_cast<unsigned long long>(e64));
+    atomicAdd(&tot[1], static_cast<unsigned long long>(b64));
+    atomicAdd(&tot[2], static_cast<unsigned long long>(e128));
+    atomicAdd(&tot[3], static_cast<unsigned long long>(b128));
+    atomicMax(&tot[4], static_cast<unsigned long long>(e64));
+    atomicMax(&tot[5], static_cast<unsigned long long>(e128));
+  }
+}
+
+// Number of allowed logical blocks (density for the regime table).
+__global__ void logical_count_kernel(const uint8_t* blocks, int64_t n, unsigned long long* out) {
+  unsigned long long c = 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    c += blocks[i] != 0;
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(out, c);
+}
+
+// Exclusive scan of n values with one block.
+__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int64_t* sh) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int64_t per = (n + T - 1) / T;
+  const int64_t lo = min(n, static_cast<int64_t>(tid) * per), hi = min(n, lo + per);
+  int64_t s = 0;
+  for (int64_t i = lo; i < hi; ++i) s += in[i];
+  sh[tid] = s;
+  __syncthreads();
+  for (int o = 1; o < T; o <<= 1) {
+    const int64_t v = (tid >= o) ? sh[tid - o] : 0;
+    __syncthreads();
+    sh[tid] += v;
+    __syncthreads();
+  }
+  int64_t run = sh[tid] - s;
+  for (int64_t i = lo; i < hi; ++i) {
+    const int32_t v = in[i];
+    out[i] = static_cast<int32_t>(run);
+    run += v;
+  }
+  __syncthreads();
+}
+
+// One block: tile offsets, descriptor offsets and the work items in
+// longest-first order (counting sort on the tile count).
+__global__ void __launch_bounds__(1024) plan_schedule_kernel(
+    const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items, int32_t nqt, int32_t H,
+    const int8_t* head_kind, int32_t is_svg, int32_t max_len, int32_t lpt, int32_t* ebegin,
+    int32_t* dbegin, int32_t* hist, int4* items) {
+  __shared__ int64_t sh[1024];
+  block_exclusive_scan(cnt_e, ebegin, n_items, sh);
+  block_exclusive_scan(cnt_b, dbegin, n_items, sh);
+  const int T = blockDim.x, tid = threadIdx.x;
+  if (lpt) {
+    for (int i = tid; i <= max_len; i += T) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < n_items; i += T) atomicAdd(&hist[cnt_e[i]], 1);
+    __syncthreads();
+    // positions in descending length order: pos[L] = sum of hist[L'] for L' > L
+    if (tid == 0) {
+      int32_t run = 0;
+      for (int L = max_len; L >= 0; --L) {
+        const int32_t c = hist[L];
+        hist[L] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+  }
+  for (int64_t i = tid; i < n_items; i += T) {
+    const int32_t len = cnt_e[i];
+    const int64_t pos = lpt ? atomicAdd(&hist[len], 1) : i;
+    const int32_t bh = static_cast<int32_t>(i / nqt), qt = static_cast<int32_t>(i % nqt);
+    const int32_t layout = (is_svg && head_kind[bh % H] == TSR_HEAD_TEMPORAL) ? 1 : 0;
+    items[2 * pos] = make_int4(bh, qt, ebegin[i], ebegin[i] + len);
+    items[2 * pos + 1] = make_int4(layout, 0, 0, 0);
+  }
+}
+
+__global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32_t* ebegin,
+                                 const int32_t* dbegin, int2* entries, tsr_tile_desc* descs) {
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
+  if (warp >= n_items) return;
+  const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
+  RowSegs rs;
+  rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
+  int64_t nqs, nks;
+  grid_dims(m, &nqs, &nks);
+  const int nkt = (m.N + bn - 1) / bn;
+  int32_t e_pos = ebegin[warp], d_pos = dbegin[warp];
+  for (int base = 0; base < nkt; base += 32) {
+    const int kt = base + lane;
+    tsr_tile_desc d;
+    const int c = (kt < nkt) ? classify(m, bh, h, rs, kt * bn, bn, nqs, nks, &d) : 0;
+    const unsigned nonempty = __ballot_sync(0xFFFFFFFFu, c > 0);
+    const unsigned bnd = __ballot_sync(0xFFFFFFFFu, c == 2);
+    const unsigned below = (1u << lane) - 1u;
+    if (c > 0) {
+      const int32_t ei = e_pos + __popc(nonempty & below);
+      int32_t di = -1;
+      if (c == 2) {
+        di = d_pos + __popc(bnd & below);
+        descs[di] = d;
+      }
+      entries[ei] = make_int2(kt * bn, di);
+    }
+    e_pos += __popc(nonempty);
+    d_pos += __popc(bnd);
+  }
+}
+
+template <class T>
+tsr_status dev_alloc(T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TSR_ERR_OOM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+  }
+  return TSR_OK;
+}
+
+// Temporary device buffers of one planning call.
+struct Scratch {
+  std::vector<void*> ptrs;
+  ~Scratch() {
+    for (void* p : ptrs) cudaFree(p);
+  }
+  template <class T>
+  tsr_status get(T** p, size_t bytes) {
+    const tsr_status s = dev_alloc(p, bytes);
+    if (s == TSR_OK) ptrs.push_back(*p);
+    return s;
+  }
+};
+
+}  // namespace
+
+tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
+                      cudaStream_t stream) {
+  const int32_t B = mask->B, H = mask->H, N = mask->N;
+  const int32_t nqt = (N + kBM - 1) / kBM;
+  const int64_t n_items = static_cast<int64_t>(B) * H * nqt;
+  P->n_items = n_items;
+  if (n_items > (int64_t{1} << 30)) return fail(TSR_ERR_UNSUPPORTED, "too many query tiles");
+
+  MaskDev m;
+  memset(&m, 0, sizeof m);
+  m.kind = mask->kind;
+  m.B = B;
+  m.H = H;
+  m.N = N;
+  m.bq = mask->bq;
+  m.bk = mask->bk;
+  m.n_qseg = mask->n_qseg;
+  m.n_kseg = mask->n_kseg;
+  m.q_bounds = mask->q_bounds;
+  m.k_bounds = mask->k_bounds;
+  m.blocks = mask->blocks;
+  m.F = mask->n_frames;
+  m.S = mask->frame_size;
+  m.head_kind = P->head_kind_dev;
+
+  Scratch tmp;
+  int32_t* cnt = nullptr;
+  unsigned long long* tot = nullptr;
+  if (tsr_status s = tmp.get(&cnt, sizeof(int32_t) * 4 * n_items)) return s;
+  if (tsr_status s = tmp.get(&tot, sizeof(unsigned long long) * 8)) return s;
+  TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
+  TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
+
+  const int threads = 256;
+  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, cnt, tot,
+                                                                             P->err);
+  TSR_CUDA(cudaGetLastError());
+  int64_t n_grid = 0;
+  if (m.kind == TSR_MASK_UNIFORM) {
+    n_grid = static_cast<int64_t>(B) * H * ((N + m.bq - 1) / m.bq) * ((N + m.bk - 1) / m.bk);
+  } else if (m.kind == TSR_MASK_SEGMENTS) {
+    n_grid = static_cast<int64_t>(B) * H * m.n_qseg * m.n_kseg;
+  }
+  if (n_grid > 0) {
+    logical_count_kernel<<<static_cast<unsigned>(std::min<int64_t>(1024, (n_grid + 255) / 256)),
+                           256, 0, stream>>>(m.blocks, n_grid, tot + 6);
+    TSR_CUDA(cudaGetLastError());
+  }
+  unsigned long long host_tot[8];
+  uint32_t host_err = 0;
+  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof host_tot, cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaMemcpyAsync(&host_err, P->err, sizeof host_err, cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+  if (host_err & DEV_ERR_UNSUPPORTED)
+    return fail(TSR_ERR_UNSUPPORTED,
+                "a 128-token tile overlaps more than 8 logical segments (blocks or segments "
+                "smaller than 16 tokens)");
+  if (host_err) return fail(TSR_ERR_INTERNAL, "planner error word " + std::to_string(host_err));
+
+  // density of the logical mask, for the regime table
+  double density = 0.0;
+  if (n_grid > 0) {
+    P->n_logical_on = static_cast<int64_t>(host_tot[6]);
+    P->n_logical_total = n_grid;
+    density = static_cast<double>(host_tot[6]) / static_cast<double>(n_grid);
+  } else if (m.kind == TSR_MASK_SVG) {
+    // allowed elements per head: spatial S^2 (2F - 1), temporal N F
+    const double S = m.S, F = m.F;
+    double on = 0;
+    for (int32_t h = 0; h < H; ++h)
+      on += (P->head_layout[h] ? static_cast<double>(N) * F : S * S * (2 * F - 1));
+    P->n_logical_on = static_cast<int64_t>(on) * B;
+    P->n_logical_total = static_cast<int64_t>(B) * H * N * static_cast<int64_t>(N);
+    density = on / (static_cast<double>(H) * N * static_cast<double>(N));
+  }
+  Regime rg = regime_lookup(m.kind, m.bq, m.bk, N, density, P->d);
+  if (opts) {
+    if (opts->bn) rg.bn = opts->bn, rg.id = -1;
+    if (opts->stages) rg.stages = opts->stages, rg.id = -1;
+    if (opts->ctas_per_sm) rg.ctas = opts->ctas_per_sm, rg.id = -1;
+  }
+  if (rg.bn != 64 && rg.bn != 128) return fail(TSR_ERR_INVALID_ARG, "bn must be 64 or 128");
+  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas))
+    return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) +
+                                         " bn=" + std::to_string(rg.bn) + " stages=" +
+                                         std::to_string(rg.stages) + " ctas=" +
+                                         std::to_string(rg.ctas));
+  P->bn = rg.bn;
+  P->stages = rg.stages;
+  P->ctas = rg.ctas;
+  P->regime_id = rg.id;
+  const int which = (rg.bn == 64) ? 0 : 1;
+  P->n_entries = static_cast<int64_t>(host_tot[2 * which]);
+  P->n_desc = static_cast<int64_t>(host_tot[2 * which + 1]);
+  P->max_item_len = static_cast<int64_t>(host_tot[4 + which]);
+  if (P->n_entries >= (int64_t{1} << 31) || P->n_desc >= (int64_t{1} << 31))
+    return fail(TSR_ERR_UNSUPPORTED, "plan has more than 2^31 tiles");
+
+  if (tsr_status s = dev_alloc(&P->items, sizeof(tsr_plan_item) * n_items)) return s;
+  if (tsr_status s = dev_alloc(&P->entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
+  if (tsr_status s = dev_alloc(&P->descs, sizeof(tsr_tile_desc) * P->n_desc)) return s;
+
+  int32_t *ebegin = nullptr, *dbegin = nullptr, *hist = nullptr;
+  if (tsr_status s = tmp.get(&ebegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = tmp.get(&dbegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = tmp.get(&hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  const int32_t* cnt_e = cnt + (2 * which) * n_items;
+  const int32_t* cnt_b = cnt + (2 * which + 1) * n_items;
+  const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
+  plan_schedule_kernel<<<1, 1024, 0, stream>>>(
+      cnt_e, cnt_b, n_items, nqt, H, P->head_kind_dev, m.kind == TSR_MASK_SVG ? 1 : 0,
+      static_cast<int32_t>(P->max_item_len), lpt, ebegin, dbegin, hist,
+      static_cast<int4*>(P->items));
+  TSR_CUDA(cudaGetLastError());
+  plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
+      m, nqt, rg.bn, ebegin, dbegin, static_cast<int2*>(P->entries),
+      static_cast<tsr_tile_desc*>(P->descs));
+  TSR_CUDA(cudaGetLastError());
+  // The temporary buffers are released when `tmp` goes out of scope; cudaFree
+  // waits for the device, so the kernels above have finished by then.
+  return TSR_OK;
+}
+
+}  // namespace tsr
