@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+entry point that include/tsr.h declares, and rejects bad arguments on the host
+before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_attention_tsr_gb300 as tsr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    tsr.build()
+    return tsr.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "tsr.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(tsr_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    assert "tsr_plan" in names and "tsr_bsa_forward" in names
+    assert len(names) >= 12
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert set(tsr.EXPORTS) <= set(_declared())
+
+
+def test_abi_version_and_strings(L):
+    assert tsr.tsr_abi_version() == 1
+    assert L.tsr_status_string(0) == b"ok"
+    assert L.tsr_status_string(5) == b"device wait timed out"
+
+
+def _mask(**kw):
+    m = tsr._Mask()
+    for k, v in kw.items():
+        setattr(m, k, v)
+    return m
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kind=0, B=1, H=1, N=128, d=96, bq=64, bk=64, blocks=16), 1),      # d not 64/128
+    (dict(kind=0, B=1, H=1, N=128, d=64, bq=8, bk=64, blocks=16), 1),       # block < 16
+    (dict(kind=0, B=1, H=1, N=128, d=64, bq=64, bk=64, blocks=0), 1),       # no blocks
+    (dict(kind=0, B=0, H=1, N=128, d=64, bq=64, bk=64, blocks=16), 1),      # B = 0
+    (dict(kind=2, B=1, H=2, N=100, d=64, n_frames=3, frame_size=30, head_kind=16), 1),  # F*S != N
+    (dict(kind=9, B=1, H=1, N=128, d=64), 1),                               # unknown kind
+])
+def test_plan_rejects_bad_arguments_on_host(L, kw, code):
+    h = ctypes.c_void_p(0)
+    m = _mask(**kw)
+    st = L.tsr_plan(ctypes.byref(m), None, ctypes.byref(h), None)
+    assert st == code
+    assert h.value is None or h.value == 0
+    assert len(L.tsr_last_error()) > 0
+
+
+def test_forward_rejects_null_plan(L):
+    assert L.tsr_bsa_forward(None, None, None, None, None, None, None) == 1
+
+
+def test_regime_table_parsing(L, tmp_path):
+    good = tmp_path / "good.txt"
+    good.write_text("# comment\n0 64 64 * * 0 0.5 128 64 4 1\n* * * * * * * 128 128 3 1\n"
+                    "* * * * * * * 64 128 4 1\n")
+    tsr.tsr_regime_load(str(good))
+    r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.2)
+    assert (r["bn"], r["stages"], r["ctas_per_sm"], r["id"]) == (64, 4, 1, 0)
+    r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.7)
+    assert (r["bn"], r["id"]) == (128, 1)
+    bad = tmp_path / "bad.txt"
+    bad.write_text("* * * * * * * 128 96 3 1\n")            # no such kernel variant
+    with pytest.raises(tsr.TsrError):
+        tsr.tsr_regime_load(str(bad))
+    bad.write_text("* * * 1\n")
+    with pytest.raises(tsr.TsrError):
+        tsr.tsr_regime_load(str(bad))
+    tsr.tsr_regime_load(tsr.REGIME_TABLE if os.path.exists(tsr.REGIME_TABLE) else None)
+
+
+def test_package_has_no_cpu_path():
+    src = open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "__init__.py")).read()
+    assert "import oracle" not in src and "from oracle" not in src
+    for f in os.listdir(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f)).read()

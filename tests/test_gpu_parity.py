@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerances (bf16 output of fp32 arithmetic against fp64): max |dO| <= 2e-2 and
+mean |dO| <= 2e-3 over the non-empty rows, |dlse| <= 1e-3 * max(1, |lse|),
+rows with no allowed key exactly O = 0 and lse = -inf.  Plans are checked
+bit-exactly against the oracle's allowed set by ``oracle.coverage``.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_tsr_gb300 as tsr
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_REL = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    tsr.build()
+    tsr.lib()
+
+
+def run(spec, d, seed, opts=None, scale=1.0, qkv=None):
+    q, k, v = qkv if qkv is not None else W.qkv(spec.B, spec.H, spec.N, d, seed, scale)
+    mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, d, **W.mask_tensors(spec))
+    plan = tsr.tsr_plan(mask, opts)
+    out, lse = tsr.tsr_bsa_forward(q.cuda(), k.cuda(), v.cuda(), plan)
+    torch.cuda.synchronize()
+    tsr.tsr_plan_device_status(plan)
+    return (q, k, v), plan, out.float().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+
+
+def compare(O_ref, L_ref, O, L, where=""):
+    O_ref = O_ref.reshape(-1, O_ref.shape[-1])
+    O = O.reshape(-1, O.shape[-1])
+    L_ref, L = L_ref.reshape(-1), L.reshape(-1)
+    empty = ~np.isfinite(L_ref)
+    assert np.all(L[empty] == -np.inf), f"{where}: empty rows must have lse = -inf"
+    assert np.all(O[empty] == 0.0), f"{where}: empty rows must have O = 0"
+    assert np.all(np.isfinite(L[~empty])), f"{where}: non-empty rows must have finite lse"
+    if (~empty).any():
+        d = np.abs(O[~empty] - O_ref[~empty])
+        assert d.max() <= MAX_ABS, f"{where}: max |dO| = {d.max():.3e}"
+        assert d.mean() <= MEAN_ABS, f"{where}: mean |dO| = {d.mean():.3e}"
+        dl = np.abs(L[~empty] - L_ref[~empty]) / np.maximum(1.0, np.abs(L_ref[~empty]))
+        assert dl.max() <= LSE_REL, f"{where}: lse rel err = {dl.max():.3e}"
+
+
+def check_coverage(spec, plan):
+    n, rep, st = oracle.coverage(spec, plan.export())
+    assert n == 0, f"plan coverage failures: {rep}"
+    assert st["covered"] == st["allowed"]
+    return st
+
+
+# ------------------------------------------------------------------ tiny config
+def test_tiny_config_full_parity():
+    spec = W.tiny_block_mask(seed=1)               # B=1 H=2 N=1024 d=64, 64x64 blocks
+    (q, k, v), plan, O, L = run(spec, 64, seed=1)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "tiny")
+    check_coverage(spec, plan)
+    assert np.sum(~np.isfinite(L)) == 2 * 64       # one masked query block per head
+
+
+UNIFORM_CASES = [
+    # (N, H, d, bq, bk, p, opts)
+    (1000, 2, 128, 64, 64, 0.3, None),
+    (777, 1, 128, 32, 32, 0.4, {"bn": 64, "stages": 4, "ctas_per_sm": 1}),
+    (1024, 2, 128, 128, 128, 0.5, {"bn": 128, "stages": 2}),
+    (900, 1, 128, 64, 256, 0.5, {"bn": 64, "stages": 2, "ctas_per_sm": 2}),
+    (900, 1, 128, 256, 64, 0.5, None),
+    (1100, 2, 64, 64, 64, 0.3, {"bn": 128, "stages": 4}),
+    (1100, 1, 64, 16, 48, 0.3, {"bn": 64, "stages": 4}),
+    (1100, 1, 64, 64, 64, 0.3, {"bn": 64, "stages": 3, "ctas_per_sm": 2}),
+    (200, 1, 128, 64, 64, 1.0, None),
+    (129, 1, 64, 16, 16, 0.5, {"bn": 64, "stages": 4}),
+]
+
+
+@pytest.mark.parametrize("case", UNIFORM_CASES, ids=[str(i) for i in range(len(UNIFORM_CASES))])
+def test_uniform_masks(case):
+    N, H, d, bq, bk, p, opts = case
+    r = np.random.Generator(np.random.PCG64(N + bq))
+    blocks = (r.random((1, H, -(-N // bq), -(-N // bk))) < p).astype(np.uint8)
+    if blocks.shape[2] > 2:
+        blocks[0, 0, 2, :] = 0                       # a fully masked query block
+    spec = W.MaskSpec(W.MASK_UNIFORM, 1, H, N, bq=bq, bk=bk, blocks=blocks)
+    (q, k, v), plan, O, L = run(spec, d, seed=N, opts=opts, scale=1.5)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, f"uniform {case}")
+    check_coverage(spec, plan)
+
+
+def test_segments_mask():
+    spec = W.segment_mask(3, 1, 2, 1500, lo=16, hi=300)
+    (q, k, v), plan, O, L = run(spec, 128, seed=5)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "segments")
+    check_coverage(spec, plan)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_svg_small(d):
+    spec = W.svg_mask(1, 4, n_frames=16, frame_size=48, kinds=np.array([0, 1, 1, 0], np.int8))
+    (q, k, v), plan, O, L = run(spec, d, seed=7)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "svg")
+    st = check_coverage(spec, plan)
+    assert plan.stats()["n_temporal_heads"] == 2
+    assert st["allowed"] == 2 * 48 * 48 * 31 + 2 * 768 * 16
+
+
+def test_q_zero_closed_form_on_gpu():
+    """Q = 0: lse_i = ln |A_i| exactly in fp64; the GPU must reproduce the count
+    of allowed keys, so a tile computed twice or skipped shows up here."""
+    spec = W.tiny_block_mask(seed=4, N=1000)
+    _, k, v = W.qkv(spec.B, spec.H, spec.N, 64, 9)
+    q = torch.zeros_like(k)
+    _, _, O, L = run(spec, 64, seed=0, qkv=(q, k, v))
+    cnt = np.array([[len(oracle.row_keys(spec, 0, h, i)) for i in range(spec.N)]
+                    for h in range(spec.H)])
+    fin = cnt > 0
+    assert np.all(np.isfinite(L[0][fin])) and np.all(L[0][~fin] == -np.inf)
+    assert np.abs(L[0][fin] - np.log(cnt[fin])).max() <= 1e-5
+
+
+def test_rescale_path_large_logits():
+    """Large, growing logits force many running-maximum rescales."""
+    spec = W.tiny_block_mask(seed=6, N=1024)
+    q, k, v = W.qkv(1, 2, 1024, 64, 3, scale=4.0)
+    ramp = torch.linspace(0.1, 3.0, 1024).view(1, 1, -1, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    _, _, O, L = run(spec, 64, seed=0, qkv=(q, k, v))
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "rescale")
+
+
+def test_plan_reuse_and_lpt_off():
+    spec = W.tiny_block_mask(seed=8, N=2048)
+    q, k, v = W.qkv(1, 2, 2048, 128, 8)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    mask = tsr.make_mask(spec.kind, 1, 2, 2048, 128, **W.mask_tensors(spec))
+    for opts in (None, {"flags": tsr.PLAN_NO_LPT}, {"flags": tsr.PLAN_SYNC_CHECK}):
+        plan = tsr.tsr_plan(mask, opts)
+        for _ in range(2):
+            out, lse = tsr.tsr_bsa_forward(q.cuda(), k.cuda(), v.cuda(), plan)
+            compare(O_ref, L_ref, out.float().cpu().numpy(), lse.cpu().double().numpy(), str(opts))
+        tsr.tsr_plan_device_status(plan)
+
+
+def test_temporal_permute_roundtrip_bit_exact():
+    F, S, H = 21, 40, 3
+    x = torch.randn(2, H, F * S, 128, device="cuda").to(torch.bfloat16)
+    y = torch.zeros_like(x)
+    z = torch.zeros_like(x)
+    kinds = [1, 0, 1]
+    tsr.tsr_temporal_permute(x, y, F, S, head_kind=kinds)
+    tsr.tsr_temporal_permute(y, z, F, S, head_kind=kinds, inverse=True)
+    torch.cuda.synchronize()
+    for h, kd in enumerate(kinds):
+        if kd:
+            assert torch.equal(z[:, h], x[:, h])
+            # t' = s*F + f holds token t = f*S + s
+            perm = torch.tensor([(tp % F) * S + tp // F for tp in range(F * S)], device="cuda")
+            assert torch.equal(y[:, h], x[:, h, perm])
+        else:
+            assert torch.count_nonzero(y[:, h]) == 0
+
+
+def test_host_entry_point_matches_device_path():
+    spec = W.tiny_block_mask(seed=2, N=1024)
+    q, k, v = W.qkv(1, 2, 1024, 64, 2)
+    _, _, O, L = run(spec, 64, seed=0, qkv=(q, k, v))
+    out = torch.empty_like(q).pin_memory()
+    lse = torch.empty((1, 2, 1024), dtype=torch.float32).pin_memory()
+    tsr.tsr_attention_host(spec.kind, 1, 2, 1024, 64, q.pin_memory(), k.pin_memory(),
+                           v.pin_memory(), out, lse, bq=64, bk=64, blocks=spec.blocks)
+    assert np.array_equal(out.float().numpy(), O)
+    assert np.array_equal(lse.double().numpy(), L)
+
+
+# -------------------------------------------------------- full-size configs
+def _sample_rows(spec, n_per_head, seed):
+    r = np.random.Generator(np.random.PCG64(seed))
+    rows = []
+    for bh in range(spec.B * spec.H):
+        idx = np.concatenate([r.integers(0, spec.N, n_per_head - 2), [spec.N - 1, 0]])
+        rows.append(bh * spec.N + idx)
+    return np.concatenate(rows)
+
+
+def _sampled_parity(spec, d, seed, opts=None, rows_per_head=24):
+    (q, k, v), plan, O, L = run(spec, d, seed=seed, opts=opts)
+    rows = _sample_rows(spec, rows_per_head, seed)
+    O_ref, L_ref, _ = oracle.attention_rows(spec, q, k, v, rows)
+    compare(O_ref, L_ref, O.reshape(-1, d)[rows], L.reshape(-1)[rows], spec.meta.get("workload", ""))
+    return plan
+
+
+@pytest.mark.slow
+def test_video_480p_block_mask_full_size():
+    spec = W.video_block_mask(seed=2)              # 24 heads x 32,760 tokens, 64x64 blocks
+    plan = _sampled_parity(spec, 128, seed=2)
+    check_coverage(spec, plan)
+
+
+@pytest.mark.slow
+def test_video_480p_block_mask_bn128():
+    spec = W.video_block_mask(seed=2, H=4)
+    _sampled_parity(spec, 128, seed=12, opts={"bn": 128, "stages": 3})
+
+
+@pytest.mark.slow
+def test_svg_480p_full_size():
+    spec = W.svg_mask(1, 24, n_frames=21, frame_size=1560)
+    plan = _sampled_parity(spec, 128, seed=3)
+    st = plan.stats()
+    assert st["n_temporal_heads"] == 12
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("m", [0, 1, 2, 3])
+def test_sweep_members(m):
+    spec = W.sweep_mask(m, H=4)
+    plan = _sampled_parity(spec, 128, seed=100 + m, rows_per_head=16)
+    check_coverage(spec, plan)

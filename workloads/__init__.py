@@ -294,3 +294,26 @@ def random_keylist(seed: int, B: int, H: int, N: int, slice_m: int = 64,
     indices = np.concatenate(lists).astype(np.int32) if lists else np.zeros(0, np.int32)
     return MaskSpec(MASK_KEYLIST, B, H, N, slice_m=slice_m, indptr=indptr, indices=indices,
                     meta={"workload": f"random_keylist_N{N}"})
+
+
+# --------------------------------------------------------------------------
+# marshalling to device tensors (no arithmetic)
+# --------------------------------------------------------------------------
+
+def mask_tensors(spec: MaskSpec, device="cuda") -> dict:
+    """The mask's arrays as contiguous torch tensors on `device`, keyed by the
+    argument names of the library's mask description."""
+    import torch
+
+    def t(x, dt):
+        return None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=dt)).to(device)
+
+    kw = dict(bq=spec.bq, bk=spec.bk, n_frames=spec.n_frames, frame_size=spec.frame_size,
+              slice_m=spec.slice_m)
+    kw["blocks"] = t(spec.blocks, np.uint8)
+    kw["q_bounds"] = t(spec.q_bounds, np.int32)
+    kw["k_bounds"] = t(spec.k_bounds, np.int32)
+    kw["head_kind"] = t(spec.head_kind, np.int8)
+    kw["indptr"] = t(spec.indptr, np.int64)
+    kw["indices"] = t(spec.indices, np.int32)
+    return kw
