@@ -70,6 +70,13 @@ struct tsr_plan_impl {
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream);
 
+tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
+                           uint32_t* err, int64_t n_grid, cudaStream_t stream);
+tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int32_t* cnt_e,
+                            const int32_t* cnt_b, int32_t max_len, int32_t* ebegin,
+                            int32_t* dbegin, int32_t* hist, void* items, void* entries,
+                            void* descs, cudaStream_t stream);
+
 // forward kernels (fwd.cu)
 struct FwdArgs {
   const void* q;

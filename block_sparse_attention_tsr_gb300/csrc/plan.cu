@@ -313,6 +313,40 @@ struct Scratch {
 
 }  // namespace
 
+// Launches of the planner kernels over buffers the caller provides (used by the
+// static-scratch entry point; tsr_plan goes through plan_build below).
+tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
+                           uint32_t* err, int64_t n_grid, cudaStream_t stream) {
+  const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
+  const int threads = 256;
+  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, cnt, tot, err);
+  TSR_CUDA(cudaGetLastError());
+  if (n_grid > 0) {
+    logical_count_kernel<<<static_cast<unsigned>(std::min<int64_t>(1024, (n_grid + 255) / 256)),
+                           256, 0, stream>>>(m.blocks, n_grid, tot + 6);
+    TSR_CUDA(cudaGetLastError());
+  }
+  return TSR_OK;
+}
+
+tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int32_t* cnt_e,
+                            const int32_t* cnt_b, int32_t max_len, int32_t* ebegin,
+                            int32_t* dbegin, int32_t* hist, void* items, void* entries,
+                            void* descs, cudaStream_t stream) {
+  const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
+  const int threads = 256;
+  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, m.H, m.head_kind,
+                                               m.kind == TSR_MASK_SVG ? 1 : 0, max_len, 1, ebegin,
+                                               dbegin, hist, static_cast<int4*>(items));
+  TSR_CUDA(cudaGetLastError());
+  plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
+      m, nqt, bn, ebegin, dbegin, static_cast<int2*>(entries), static_cast<tsr_tile_desc*>(descs));
+  TSR_CUDA(cudaGetLastError());
+  return TSR_OK;
+}
+
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream) {
   const int32_t B = mask->B, H = mask->H, N = mask->N;

@@ -289,6 +289,34 @@ tsr_status tsr_attention_host(const tsr_mask *mask, const tsr_plan_opts *opts,
 void tsr_release_host_buffers(void);
 
 /*
+ * tsr_attention_noalloc -- plan and attention in one call, with no device
+ * allocation.  (The pages have no counterpart; this is a deployment aid.)
+ *
+ * For callers that cannot call cudaMalloc: code that must take every byte of
+ * device memory from its own pool or budget (a server that reserved the GPU up
+ * front, a framework whose allocator forbids raw cudaMalloc), and code on a
+ * latency-critical path where cudaMalloc / cudaFree and the device-wide wait of
+ * cudaFree are not acceptable.  The call plans into, and runs over, one scratch
+ * array compiled into the library; the caller still passes q, k, v, out and lse
+ * (device pointers, layouts as for tsr_bsa_forward) and the mask (device arrays,
+ * UNIFORM or SEGMENTS only; other kinds give TSR_ERR_UNSUPPORTED).
+ *
+ *   - The scratch array is 32 MiB, held on every GPU that loads the library until
+ *     the process exits.  A plan that does not fit (about 512 B + 56 B per
+ *     128-row query tile + 8 B per kept tile + 32 B per boundary tile) is rejected
+ *     with TSR_ERR_UNSUPPORTED before the attention runs; use tsr_plan() then.
+ *   - All calls share the array and it keeps the last call's contents (the call
+ *     clears what must start at zero).  Calls whose GPU work overlaps -- from two
+ *     host threads or on two streams -- race on it and must be serialised.
+ *   - The first call on a device looks up the array's device address; make that
+ *     first call before any stream capture.
+ *   - Synchronises `stream` (to size the plan, and at the end to read the device
+ *     error word, returned as TSR_ERR_TIMEOUT / TSR_ERR_INTERNAL).
+ */
+tsr_status tsr_attention_noalloc(const tsr_mask *mask, const void *q, const void *k,
+                                 const void *v, void *out, float *lse, void *stream);
+
+/*
  * Regime table (profile-guided regime selection, Tessera abstract).
  * tsr_regime_load reads a table file (text, one regime per line; see the file
  * shipped next to the library); NULL reloads the built-in default.
