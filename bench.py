@@ -99,6 +99,10 @@ class ClockSampler:
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
         return self
 
     def __exit__(self, *a):
@@ -188,11 +192,14 @@ def run_reference(args, rank: int, world: int) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tsr", choices=["tsr", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bn", type=int, default=0, help="force the K/V tile width (0 = table)")
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--heads", type=int, default=24,
                     help="heads of the workload (24 = the benchmark; fewer for profiling)")
     args = ap.parse_args()
@@ -230,8 +237,12 @@ def main():
     lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    opts = None
+    if args.bn or args.stages or args.ctas:
+        opts = {"bn": args.bn, "stages": args.stages, "ctas_per_sm": args.ctas}
+
     def step(ev_pair=None):
-        plan = tsr.tsr_plan(mask, None, stream)
+        plan = tsr.tsr_plan(mask, opts, stream)
         if ev_pair is not None:
             ev_pair[0].record(stream)
         tsr.tsr_bsa_forward(qd, kd, vd, plan, out, lse, stream)

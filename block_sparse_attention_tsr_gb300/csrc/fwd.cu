@@ -302,9 +302,29 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       const int4 i1 = __ldg(&p.items[2 * it + 1]);
       const int32_t bh = i0.x, q_tile = i0.y, begin = i0.z, n = i0.w - i0.z, layout = i1.x;
       float m_ref = -INFINITY, l = 0.f;
+      // The tile entry and its boundary descriptor are fetched one tile ahead so
+      // that their global-memory latency hides behind the wait for S.
+      int32_t desc_next = -1;
+      uint4 dn0 = make_uint4(0u, 0u, 0u, 0u), dn1 = dn0;
+      if (n > 0) {
+        desc_next = __ldg(&p.entries[begin]).y;
+        if (desc_next >= 0) {
+          dn0 = __ldg(&p.descs[2 * desc_next]);
+          dn1 = __ldg(&p.descs[2 * desc_next + 1]);
+        }
+      }
       for (int32_t j = 0; j < n; ++j) {
         const uint32_t t = t_cnt + j;
         const uint32_t sb = t & 1;
+        const int32_t desc = desc_next;
+        const uint4 d0 = dn0, d1 = dn1;
+        if (j + 1 < n) {
+          desc_next = __ldg(&p.entries[begin + j + 1]).y;
+          if (desc_next >= 0) {
+            dn0 = __ldg(&p.descs[2 * desc_next]);
+            dn1 = __ldg(&p.descs[2 * desc_next + 1]);
+          }
+        }
         if (!mbar_wait(smem_u32(&ctrl.s_full[sb]), (t >> 1) & 1, abort_flag, p.err)) {
           ok = false;
           break;
@@ -319,10 +339,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(rr[i]);
         }
         tc_wait_ld();
-        const int32_t desc = __ldg(&p.entries[begin + j]).y;
         if (desc >= 0) {
-          const uint4 d0 = __ldg(&p.descs[2 * desc]);
-          const uint4 d1 = __ldg(&p.descs[2 * desc + 1]);
           const int n_r = d0.x & 0xFF, n_c = (d0.x >> 8) & 0xFF;
           int rs = 0;
 #pragma unroll
@@ -343,10 +360,14 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int c = 0; c < BN; ++c)
             if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
         }
-        float mt = -INFINITY;
+        float mx8[8];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mt = fmaxf(mt, x[c]);
-        mt *= p.scale_log2;
+        for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                         p.scale_log2;
         const float m_new = fmaxf(m_ref, mt);
         const bool need = m_new > m_ref + kRescaleThreshold;
         // O holds the sum over earlier tiles only when j > 0; it is exactly 0 for
@@ -375,7 +396,9 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rowsum = 0.f;
+        float rs8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 64) {
           uint32_t pk[32];
@@ -383,12 +406,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int i = 0; i < 32; ++i) {
             const float a = ex2_approx(fmaf(x[c0 + 2 * i], p.scale_log2, -m_use));
             const float b = ex2_approx(fmaf(x[c0 + 2 * i + 1], p.scale_log2, -m_use));
-            rowsum += a + b;
+            rs8[i & 7] += a + b;
             pk[i] = pack_bf16x2(a, b);
           }
           tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
         }
-        l += rowsum;
+        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
