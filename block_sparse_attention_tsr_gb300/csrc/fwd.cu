@@ -61,7 +61,7 @@ struct alignas(8) Ctrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[8], v_full[8], kv_empty[8];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, o_empty;
+  uint64_t pv_done, o_full, o_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t final_bar;
   int32_t item_slot[2];
@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       mbar_init(smem_u32(&ctrl.item_empty[b]), 5);
     }
     mbar_init(smem_u32(&ctrl.pv_done), 1);
+    mbar_init(smem_u32(&ctrl.o_full), 1);
     mbar_init(smem_u32(&ctrl.o_empty), 4);
     mbar_init(smem_u32(&ctrl.final_bar), 1);
     ctrl.abort_flag = 0;
@@ -274,6 +275,8 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           if (j > 0 && !issue_pv(j - 1)) ok = false;
         }
         if (ok && !issue_pv(n - 1)) ok = false;
+        // the item's output accumulator is complete once its last PV finishes
+        if (ok) mma_commit(smem_u32(&ctrl.o_full));
         t_cnt += n;
         kv_cnt += n;
       }
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                    // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t item_seq = 0, t_cnt = 0;
+    uint32_t item_seq = 0, t_cnt = 0, o_seq = 0;
     bool ok = true;
     while (ok) {
       const int slot = item_seq & 1;
@@ -426,7 +429,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       const size_t obase = (static_cast<size_t>(bh) * p.N + (valid ? orow : 0)) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       if (n > 0) {
-        if (!mbar_wait(smem_u32(&ctrl.pv_done), (t_cnt - 1) & 1, abort_flag, p.err)) break;
+        // o_full completes once per non-empty item, after its last PV; the next
+        // item's first PV waits for o_empty, so the phases cannot run ahead.
+        if (!mbar_wait(smem_u32(&ctrl.o_full), o_seq & 1, abort_flag, p.err)) break;
+        ++o_seq;
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
