@@ -88,9 +88,13 @@ __device__ __forceinline__ int32_t unpermute(int32_t tp, int32_t F, int32_t S) {
   return (tp % F) * S + tp / F;
 }
 
+// Byte i of a 32-byte descriptor held in two uint4 registers (selects, no
+// local-memory indexing when i is not a compile-time constant).
 __device__ __forceinline__ uint32_t desc_byte(const uint4& a, const uint4& b, int i) {
-  const uint32_t w = (i < 16) ? (&a.x)[i >> 2] : (&b.x)[(i - 16) >> 2];
-  return (w >> ((i & 3) * 8)) & 0xFFu;
+  const int w = i >> 2;
+  const uint32_t lo = (w & 1) ? ((w & 2) ? a.w : a.y) : ((w & 2) ? a.z : a.x);
+  const uint32_t hi = (w & 1) ? ((w & 2) ? b.w : b.y) : ((w & 2) ? b.z : b.x);
+  return (((w & 4) ? hi : lo) >> ((i & 3) * 8)) & 0xFFu;
 }
 
 // Columns [lo, hi) of a BN-bit mask, added to words[].
@@ -342,6 +346,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(rr[i]);
         }
         tc_wait_ld();
+        // Boundary tiles: this row's column mask.  A row whose segment allows no
+        // column contributes nothing (P = 0, no exponentials); a row whose
+        // segment allows every in-range column needs no per-element masking.
+        bool row_dead = false;
         if (desc >= 0) {
           const int n_r = d0.x & 0xFF, n_c = (d0.x >> 8) & 0xFF;
           int rs = 0;
@@ -349,28 +357,37 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int k = 1; k < 8; ++k)
             if (k < n_r && static_cast<int>(desc_byte(d0, d1, 2 + k)) <= r) rs = k;
           const uint64_t bits = (static_cast<uint64_t>(d1.w) << 32) | d1.z;
-          const uint32_t rb = static_cast<uint32_t>(bits >> (rs * 8)) & 0xFFu;
-          uint32_t words[BN / 32];
+          const uint32_t all_c = (1u << n_c) - 1u;
+          const uint32_t rb = static_cast<uint32_t>(bits >> (rs * 8)) & all_c;
+          const int c_end = static_cast<int>(desc_byte(d0, d1, 10 + n_c));
+          if (rb == 0u) {
+            row_dead = true;
+          } else if (rb != all_c || c_end < BN) {
+            uint32_t words[BN / 32];
 #pragma unroll
-          for (int w = 0; w < BN / 32; ++w) words[w] = 0u;
+            for (int w = 0; w < BN / 32; ++w) words[w] = 0u;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            if (c < n_c && ((rb >> c) & 1u))
-              add_range<BN>(words, static_cast<int>(desc_byte(d0, d1, 10 + c)),
-                            static_cast<int>(desc_byte(d0, d1, 11 + c)));
+            for (int c = 0; c < 8; ++c) {
+              if (c < n_c && ((rb >> c) & 1u))
+                add_range<BN>(words, static_cast<int>(desc_byte(d0, d1, 10 + c)),
+                              static_cast<int>(desc_byte(d0, d1, 11 + c)));
+            }
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
           }
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
         }
-        float mx8[8];
+        float mt = -INFINITY;
+        if (!row_dead) {
+          float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+          for (int i = 0; i < 8; ++i) mx8[i] = x[i];
 #pragma unroll
-        for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                         p.scale_log2;
+          for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+          mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+               p.scale_log2;
+        }
         const float m_new = fmaxf(m_ref, mt);
         const bool need = m_new > m_ref + kRescaleThreshold;
         // O holds the sum over earlier tiles only when j > 0; it is exactly 0 for
@@ -405,12 +422,17 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 64) {
           uint32_t pk[32];
+          if (row_dead) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = ex2_approx(fmaf(x[c0 + 2 * i], p.scale_log2, -m_use));
-            const float b = ex2_approx(fmaf(x[c0 + 2 * i + 1], p.scale_log2, -m_use));
-            rs8[i & 7] += a + b;
-            pk[i] = pack_bf16x2(a, b);
+            for (int i = 0; i < 32; ++i) pk[i] = 0u;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float a = ex2_approx(fmaf(x[c0 + 2 * i], p.scale_log2, -m_use));
+              const float b = ex2_approx(fmaf(x[c0 + 2 * i + 1], p.scale_log2, -m_use));
+              rs8[i & 7] += a + b;
+              pk[i] = pack_bf16x2(a, b);
+            }
           }
           tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
         }
