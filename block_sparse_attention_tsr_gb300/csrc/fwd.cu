@@ -394,23 +394,6 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         // rows whose earlier tiles were fully masked (m_ref = -inf).
         const bool fix_o = need && j > 0 && m_ref != -INFINITY;
         const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-        if (__any_sync(0xFFFFFFFFu, fix_o)) {
-          if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const float f = fix_o ? alpha : 1.f;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tmem + lane_off + C::O_COL + c0, rr);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-            tmem_st32(tmem + lane_off + C::O_COL + c0, rr);
-          }
-        }
         if (need) {
           l *= alpha;
           m_ref = m_new;
@@ -437,6 +420,26 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
         }
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        // Rescale O (the sum over earlier tiles) when the running maximum grew.
+        // Done after P is written, when the S row no longer occupies registers;
+        // PV of this tile starts only after p_full, so it sees the rescaled O.
+        if (__any_sync(0xFFFFFFFFu, fix_o)) {
+          if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = fix_o ? alpha : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lane_off + C::O_COL + c0, rr);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+            tmem_st32(tmem + lane_off + C::O_COL + c0, rr);
+          }
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
