@@ -97,6 +97,25 @@ __device__ __forceinline__ uint32_t desc_byte(const uint4& a, const uint4& b, in
   return (((w & 4) ? hi : lo) >> ((i & 3) * 8)) & 0xFFu;
 }
 
+// Packed fp32 pair arithmetic (two lanes per instruction).
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float s, float b) {
+  asm("{\n\t.reg .b64 xa, sa, ba;\n\tmov.b64 xa, {%2, %3};\n\tmov.b64 sa, {%4, %4};\n\t"
+      "mov.b64 ba, {%5, %5};\n\tfma.rn.f32x2 xa, xa, sa, ba;\n\tmov.b64 {%0, %1}, xa;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(b));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Columns [lo, hi) of a BN-bit mask, added to words[].
 template <int BN>
 __device__ __forceinline__ void add_range(uint32_t (&words)[BN / 32], int lo, int hi) {
@@ -377,52 +396,76 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
               if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
           }
         }
-        float mt = -INFINITY;
-        if (!row_dead) {
-          float mx8[8];
+        // P = 2^(x * scale - m_use) for the row, written to TMEM as bf16 pairs;
+        // returns the row sum.  With track_max the same pass also takes the
+        // row maximum of x (three-input max over column pairs).
+        auto p_pass = [&](float m_use, bool track_max, float& mx) -> float {
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+          for (int c0 = 0; c0 < BN; c0 += 64) {
+            uint32_t pk[32];
+            if (row_dead) {
 #pragma unroll
-          for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-          mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-               p.scale_log2;
-        }
-        const float m_new = fmaxf(m_ref, mt);
-        const bool need = m_new > m_ref + kRescaleThreshold;
-        // O holds the sum over earlier tiles only when j > 0; it is exactly 0 for
-        // rows whose earlier tiles were fully masked (m_ref = -inf).
-        const bool fix_o = need && j > 0 && m_ref != -INFINITY;
-        const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-        if (need) {
-          l *= alpha;
-          m_ref = m_new;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs8[8];
+              for (int i = 0; i < 32; ++i) pk[i] = 0u;
+            } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          uint32_t pk[32];
-          if (row_dead) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = 0u;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float a = ex2_approx(fmaf(x[c0 + 2 * i], p.scale_log2, -m_use));
-              const float b = ex2_approx(fmaf(x[c0 + 2 * i + 1], p.scale_log2, -m_use));
-              rs8[i & 7] += a + b;
-              pk[i] = pack_bf16x2(a, b);
+              for (int i = 0; i < 32; ++i) {
+                const float x0 = x[c0 + 2 * i], x1 = x[c0 + 2 * i + 1];
+                float y0, y1;
+                fma2(y0, y1, x0, x1, p.scale_log2, -m_use);
+                const float a = ex2_approx(y0), b = ex2_approx(y1);
+                if ((i & 3) == 0) add2(s0, s1, a, b);
+                else if ((i & 3) == 1) add2(s2, s3, a, b);
+                else if ((i & 3) == 2) add2(s4, s5, a, b);
+                else add2(s6, s7, a, b);
+                if (track_max) mx = max3f(mx, x0, x1);
+                pk[i] = pack_bf16x2(a, b);
+              }
             }
+            tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
           }
-          tmem_st32(tmem + lane_off + sb * BN + c0 / 2, pk);
+          return ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        };
+        // A row with no finite maximum yet takes its reference maximum from this
+        // tile first.  Otherwise P is computed against the current reference
+        // maximum while the tile maximum is taken in the same pass; only if the
+        // maximum grew by more than the threshold is P recomputed (whole warp,
+        // since the TMEM store is warp-collective) and O rescaled.
+        const bool first = (m_ref == -INFINITY);
+        if (first && !row_dead) {
+          float a0 = fmaxf(x[0], x[1]), a1 = fmaxf(x[2], x[3]), a2 = fmaxf(x[4], x[5]),
+                a3 = fmaxf(x[6], x[7]);
+#pragma unroll
+          for (int c = 8; c < BN; c += 8) {
+            a0 = max3f(a0, x[c], x[c + 1]);
+            a1 = max3f(a1, x[c + 2], x[c + 3]);
+            a2 = max3f(a2, x[c + 4], x[c + 5]);
+            a3 = max3f(a3, x[c + 6], x[c + 7]);
+          }
+          m_ref = fmaxf(max3f(a0, a1, a2), a3) * p.scale_log2;   // stays -inf if all masked
         }
-        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        // Rescale O (the sum over earlier tiles) when the running maximum grew.
-        // Done after P is written, when the S row no longer occupies registers;
-        // PV of this tile starts only after p_full, so it sees the rescaled O.
+        float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float mx = -INFINITY;
+        float rowsum = p_pass(m_use, true, mx);
+        bool fix = false;
+        float alpha = 1.f;
+        if (!first && !row_dead) {
+          const float mt = mx * p.scale_log2;
+          if (mt > m_ref + kRescaleThreshold) {
+            fix = true;
+            alpha = ex2_approx(m_ref - mt);
+            m_ref = mt;
+            m_use = mt;
+          }
+        }
+        if (__any_sync(0xFFFFFFFFu, fix)) {
+          float unused = 0.f;
+          rowsum = p_pass(m_use, false, unused);
+        }
+        l = l * alpha + rowsum;
+        // Rescale O (the sum over earlier tiles) when the reference maximum grew.
+        // Rows that had no finite maximum before hold O = 0 and need nothing.
+        const bool fix_o = fix && j > 0;
         if (__any_sync(0xFFFFFFFFu, fix_o)) {
           if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err)) {
             ok = false;
