@@ -59,7 +59,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 struct alignas(8) Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[8], v_full[8], kv_empty[8];
+  uint64_t k_full[8], v_full[8], k_empty[8], v_empty[8];
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_full, o_empty;
   uint64_t item_full[2], item_empty[2];
@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctrl.k_full[s]), 1);
       mbar_init(smem_u32(&ctrl.v_full[s]), 1);
-      mbar_init(smem_u32(&ctrl.kv_empty[s]), 1);
+      mbar_init(smem_u32(&ctrl.k_empty[s]), 1);
+      mbar_init(smem_u32(&ctrl.v_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctrl.s_full[b]), 1);
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
     }
-    uint32_t item_seq = 0, kv_cnt = 0, q_cnt = 0;
+    uint32_t item_seq = 0, kv_cnt = 0, q_cnt = 0, k_iss = 0, v_iss = 0;
     bool ok = true;
     while (ok) {
       int32_t it = 0;
@@ -209,34 +210,56 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           tma_load_3d(sQ + c * C::BM * 128, mq, bar, c * 64, q_tile * C::BM, bh);
       }
       ++q_cnt;
-      for (int32_t e = begin; e < end; ++e) {
-        const int s = kv_cnt % STAGES;
-        if (!mbar_wait(smem_u32(&ctrl.kv_empty[s]), ((kv_cnt / STAGES) & 1) ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const int32_t kv = __ldg(&p.entries[e]).x;
-          const uint32_t kb = smem_u32(&ctrl.k_full[s]), vb = smem_u32(&ctrl.v_full[s]);
-          const uint32_t sk = sK0 + s * C::KV_BYTES, sv = sV0 + s * C::KV_BYTES;
-          mbar_arrive_expect_tx(kb, C::KV_BYTES);
+      // K runs one tile ahead of V: K of tile i is needed by QK(i), which the
+      // MMA issuer runs before PV(i-1); a K stage is released by its QK, a V
+      // stage by its PV, so the K stream never waits behind a PV.
+      const int32_t n = end - begin;
+      for (int32_t i = 0; i <= n && ok; ++i) {
+        if (i < n) {
+          const uint32_t kvi = kv_cnt + i;
+          const int s = kvi % STAGES;
+          if (!mbar_wait(smem_u32(&ctrl.k_empty[s]), ((kvi / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const int32_t kv = __ldg(&p.entries[begin + i]).x;
+            const uint32_t kb = smem_u32(&ctrl.k_full[s]);
+            const uint32_t sk = sK0 + s * C::KV_BYTES;
+            mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(sk + c * BN * 128, mk, kb, c * 64, kv, bh);
-          mbar_arrive_expect_tx(vb, C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(sv + c * BN * 128, mv, vb, c * 64, kv, bh);
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(sk + c * BN * 128, mk, kb, c * 64, kv, bh);
+          }
+          ++k_iss;
         }
-        ++kv_cnt;
+        if (i >= 1) {
+          const uint32_t kvi = kv_cnt + i - 1;
+          const int s = kvi % STAGES;
+          if (!mbar_wait(smem_u32(&ctrl.v_empty[s]), ((kvi / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const int32_t kv = __ldg(&p.entries[begin + i - 1]).x;
+            const uint32_t vb = smem_u32(&ctrl.v_full[s]);
+            const uint32_t sv = sV0 + s * C::KV_BYTES;
+            mbar_arrive_expect_tx(vb, C::KV_BYTES);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(sv + c * BN * 128, mv, vb, c * 64, kv, bh);
+          }
+          ++v_iss;
+        }
       }
+      kv_cnt += n;
     }
-    // On an abort, let the copies already issued land before the CTA exits.
+    // On an abort, let the copies already issued land before the CTA exits
+    // (the last STAGES of each stream; earlier ones were consumed).
     if (*abort_flag) {
-      for (uint32_t k = (kv_cnt > STAGES ? kv_cnt - STAGES : 0); k < kv_cnt; ++k) {
-        const int s = k % STAGES;
-        volatile int32_t dummy = 0;
-        mbar_wait(smem_u32(&ctrl.k_full[s]), (k / STAGES) & 1, &dummy, p.err);
-        mbar_wait(smem_u32(&ctrl.v_full[s]), (k / STAGES) & 1, &dummy, p.err);
-      }
+      volatile int32_t dummy = 0;
+      for (uint32_t k = (k_iss > STAGES ? k_iss - STAGES : 0); k < k_iss; ++k)
+        mbar_wait(smem_u32(&ctrl.k_full[k % STAGES]), (k / STAGES) & 1, &dummy, p.err);
+      for (uint32_t k = (v_iss > STAGES ? v_iss - STAGES : 0); k < v_iss; ++k)
+        mbar_wait(smem_u32(&ctrl.v_full[k % STAGES]), (k / STAGES) & 1, &dummy, p.err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -274,7 +297,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             mma_bf16_ts(tmem + C::O_COL, tmem + (t & 1) * BN + kk * 8, bdesc, C::IDESC_PV,
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(smem_u32(&ctrl.kv_empty[s]));
+          mma_commit(smem_u32(&ctrl.v_empty[s]));
           mma_commit(smem_u32(&ctrl.pv_done));
           return true;
         };
@@ -294,6 +317,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             mma_bf16_ss(tmem + (t & 1) * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&ctrl.s_full[t & 1]));
+          mma_commit(smem_u32(&ctrl.k_empty[s]));
           if (j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
           if (j > 0 && !issue_pv(j - 1)) ok = false;
         }
