@@ -21,7 +21,8 @@ import torch
 from . import _build
 
 __all__ = [
-    "TsrError", "build", "lib", "make_mask", "Mask", "Plan", "tsr_plan", "tsr_bsa_forward",
+    "TsrError", "build", "lib", "make_mask", "Mask", "Plan", "tsr_plan", "tsr_plan_update",
+    "tsr_bsa_forward",
     "tsr_plan_device_status", "tsr_temporal_permute", "tsr_attention_host", "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
     "PLAN_SYNC_CHECK", "PLAN_NO_LPT",
@@ -78,7 +79,7 @@ class _Regime(ctypes.Structure):
 
 
 _LIB = None
-EXPORTS = ("tsr_abi_version", "tsr_status_string", "tsr_last_error", "tsr_plan",
+EXPORTS = ("tsr_abi_version", "tsr_status_string", "tsr_last_error", "tsr_plan", "tsr_plan_update",
            "tsr_bsa_forward", "tsr_plan_device_status", "tsr_plan_destroy", "tsr_plan_get_stats",
            "tsr_plan_export", "tsr_temporal_permute", "tsr_attention_host",
            "tsr_release_host_buffers", "tsr_regime_load", "tsr_regime_lookup")
@@ -108,6 +109,7 @@ def lib():
         "tsr_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "tsr_last_error": ([], ctypes.c_char_p),
         "tsr_plan": ([P, P, P, P], ctypes.c_int),
+        "tsr_plan_update": ([P, P, P], ctypes.c_int),
         "tsr_bsa_forward": ([P, P, P, P, P, P, P], ctypes.c_int),
         "tsr_plan_device_status": ([P, P], ctypes.c_int),
         "tsr_plan_destroy": ([P], ctypes.c_int),
@@ -186,6 +188,12 @@ class Plan:
         self.mask = mask
         self.B, self.H, self.N, self.d = mask.B, mask.H, mask.N, mask.d
 
+    def update(self, mask: "Mask", stream=None) -> "Plan":
+        """Re-plan for a new mask of the same shape, reusing the plan's storage."""
+        _check(lib().tsr_plan_update(self.handle, ctypes.byref(mask.struct), _stream_ptr(stream)))
+        self.mask = mask
+        return self
+
     def stats(self) -> dict:
         st = _Stats()
         _check(lib().tsr_plan_get_stats(self.handle, ctypes.byref(st)))
@@ -229,6 +237,10 @@ def tsr_plan(mask: Mask, opts: Optional[dict] = None, stream=None) -> Plan:
     _check(L.tsr_plan(ctypes.byref(mask.struct), ctypes.byref(o) if o is not None else None,
                       ctypes.byref(h), _stream_ptr(stream)))
     return Plan(h.value, mask)
+
+
+def tsr_plan_update(plan: Plan, mask: Mask, stream=None) -> Plan:
+    return plan.update(mask, stream)
 
 
 def tsr_bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, plan: Plan,

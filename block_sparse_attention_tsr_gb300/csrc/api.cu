@@ -218,15 +218,53 @@ tsr_status check_bounds(const int32_t* dev, int32_t n, int32_t N, cudaStream_t s
 
 void free_plan(tsr_plan_s* P) {
   if (!P) return;
-  cudaFree(P->items);
-  cudaFree(P->entries);
-  cudaFree(P->descs);
+  for (DevBuf* b : {&P->b_items, &P->b_entries, &P->b_descs, &P->b_cnt, &P->b_tot, &P->b_ebegin,
+                    &P->b_dbegin, &P->b_hist})
+    devbuf_free(*b);
   cudaFree(P->gidx);
   cudaFree(P->counter);
   cudaFree(P->err);
   cudaFree(P->head_kind_dev);
   cudaFree(P->scratch);
+  if (P->host_tot) cudaFreeHost(P->host_tot);
   delete P;
+}
+
+// Mask-dependent part of planning, shared by tsr_plan and tsr_plan_update.
+tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
+  P->kind = mask->kind;
+  P->n_temporal = 0;
+  P->head_layout.assign(mask->H, 0);
+  if (mask->kind == TSR_MASK_SEGMENTS) {
+    if (tsr_status s = check_bounds(mask->q_bounds, mask->n_qseg, mask->N, st)) return s;
+    if (tsr_status s = check_bounds(mask->k_bounds, mask->n_kseg, mask->N, st)) return s;
+  }
+  if (mask->kind == TSR_MASK_SVG) {
+    TSR_CUDA(cudaMemcpyAsync(P->head_layout.data(), mask->head_kind, mask->H,
+                             cudaMemcpyDeviceToHost, st));
+    TSR_CUDA(cudaStreamSynchronize(st));
+    for (int32_t h = 0; h < mask->H; ++h) {
+      if (P->head_layout[h] != TSR_HEAD_SPATIAL && P->head_layout[h] != TSR_HEAD_TEMPORAL)
+        return fail(TSR_ERR_INVALID_ARG, "head_kind values must be 0 or 1");
+      P->n_temporal += P->head_layout[h];
+    }
+    P->F = mask->n_frames;
+    P->S = mask->frame_size;
+    if (!P->head_kind_dev) TSR_CUDA(cudaMalloc(&P->head_kind_dev, mask->H));
+    TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, P->head_layout.data(), mask->H,
+                             cudaMemcpyHostToDevice, st));
+  }
+  if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) return s;
+  if (P->n_temporal > 0 && !P->scratch) {
+    P->scratch_bytes = static_cast<size_t>(P->B) * P->H * P->N * P->d * 2;
+    const cudaError_t e = cudaMalloc(&P->scratch, 3 * P->scratch_bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      P->scratch = nullptr;
+      return fail(TSR_ERR_OOM, "temporal-major scratch allocation failed");
+    }
+  }
+  return TSR_OK;
 }
 
 // Device buffers of tsr_attention_host, kept per thread and grown on demand.
@@ -306,43 +344,30 @@ tsr_status tsr_plan(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_t*
   P->H = mask->H;
   P->N = mask->N;
   P->d = mask->d;
-  P->kind = mask->kind;
   P->flags = opts ? opts->flags : 0;
-  P->head_layout.assign(mask->H, 0);
-  if (mask->kind == TSR_MASK_SEGMENTS) {
-    if (tsr_status s = check_bounds(mask->q_bounds, mask->n_qseg, mask->N, st)) return s;
-    if (tsr_status s = check_bounds(mask->k_bounds, mask->n_kseg, mask->N, st)) return s;
-  }
-  if (mask->kind == TSR_MASK_SVG) {
-    TSR_CUDA(cudaMemcpyAsync(P->head_layout.data(), mask->head_kind, mask->H,
-                             cudaMemcpyDeviceToHost, st));
-    TSR_CUDA(cudaStreamSynchronize(st));
-    for (int32_t h = 0; h < mask->H; ++h) {
-      if (P->head_layout[h] != TSR_HEAD_SPATIAL && P->head_layout[h] != TSR_HEAD_TEMPORAL)
-        return fail(TSR_ERR_INVALID_ARG, "head_kind values must be 0 or 1");
-      P->n_temporal += P->head_layout[h];
-    }
-    P->F = mask->n_frames;
-    P->S = mask->frame_size;
-    TSR_CUDA(cudaMalloc(&P->head_kind_dev, mask->H));
-    TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, P->head_layout.data(), mask->H,
-                             cudaMemcpyHostToDevice, st));
+  if (opts) {
+    P->has_opts = true;
+    P->opts = *opts;
   }
   TSR_CUDA(cudaMalloc(&P->counter, sizeof(int32_t)));
   TSR_CUDA(cudaMalloc(&P->err, sizeof(uint32_t)));
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), st));
-  if (tsr_status s = plan_build(mask, opts, P, st)) return s;
-  if (P->n_temporal > 0) {
-    P->scratch_bytes = static_cast<size_t>(P->B) * P->H * P->N * P->d * 2;
-    const cudaError_t e = cudaMalloc(&P->scratch, 3 * P->scratch_bytes);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return fail(TSR_ERR_OOM, "temporal-major scratch allocation failed");
-    }
-  }
+  if (tsr_status s = plan_fill(P, mask, st)) return s;
   guard.p = nullptr;
   *out = P;
   return TSR_OK;
+}
+
+tsr_status tsr_plan_update(tsr_plan_t plan, const tsr_mask* mask, void* stream) {
+  set_error("");
+  if (!plan) return fail(TSR_ERR_INVALID_ARG, "plan is NULL");
+  if (tsr_status s = check_mask(mask)) return s;
+  if (mask->B != plan->B || mask->H != plan->H || mask->N != plan->N || mask->d != plan->d)
+    return fail(TSR_ERR_INVALID_ARG, "tsr_plan_update needs the plan's B, H, N and d");
+  int dev = 0;
+  TSR_CUDA(cudaGetDevice(&dev));
+  if (dev != plan->device) return fail(TSR_ERR_INVALID_ARG, "plan was made on another device");
+  return plan_fill(plan, mask, static_cast<cudaStream_t>(stream));
 }
 
 tsr_status tsr_plan_destroy(tsr_plan_t plan) {

@@ -42,6 +42,12 @@ struct Regime {
   int32_t bn, stages, ctas, id;
 };
 
+// A grow-only device buffer owned by a plan.
+struct DevBuf {
+  void* p = nullptr;
+  size_t cap = 0;
+};
+
 struct tsr_plan_impl {
   int device = 0;
   int32_t B = 0, H = 0, N = 0, d = 0;
@@ -64,7 +70,16 @@ struct tsr_plan_impl {
   int8_t* head_kind_dev = nullptr;
   void* scratch = nullptr;   // temporal-major Q, K, V copies: 3 x [B][H][N][d] bf16
   size_t scratch_bytes = 0;
+  // storage reused when the plan is rebuilt for a new mask (tsr_plan_update)
+  DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist;
+  unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
+  bool has_opts = false;
+  tsr_plan_opts opts{};
 };
+
+// Make `b` hold at least `bytes` (contents are not preserved when it grows).
+tsr_status devbuf_reserve(DevBuf& b, size_t bytes);
+void devbuf_free(DevBuf& b);
 
 // planner (plan.cu)
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,

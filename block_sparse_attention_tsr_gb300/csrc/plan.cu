@@ -285,32 +285,6 @@ __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32
   }
 }
 
-template <class T>
-tsr_status dev_alloc(T** p, size_t bytes) {
-  *p = nullptr;
-  if (bytes == 0) bytes = 16;
-  const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(TSR_ERR_OOM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
-  }
-  return TSR_OK;
-}
-
-// Temporary device buffers of one planning call.
-struct Scratch {
-  std::vector<void*> ptrs;
-  ~Scratch() {
-    for (void* p : ptrs) cudaFree(p);
-  }
-  template <class T>
-  tsr_status get(T** p, size_t bytes) {
-    const tsr_status s = dev_alloc(p, bytes);
-    if (s == TSR_OK) ptrs.push_back(*p);
-    return s;
-  }
-};
-
 }  // namespace
 
 // Launches of the planner kernels over buffers the caller provides (used by the
@@ -347,6 +321,28 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
   return TSR_OK;
 }
 
+tsr_status devbuf_reserve(DevBuf& b, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  if (b.cap >= bytes) return TSR_OK;
+  cudaFree(b.p);
+  b.p = nullptr;
+  b.cap = 0;
+  const size_t want = bytes + bytes / 4;   // headroom for the next, slightly larger mask
+  const cudaError_t e = cudaMalloc(&b.p, want);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(TSR_ERR_OOM, "cudaMalloc of " + std::to_string(want) + " bytes failed");
+  }
+  b.cap = want;
+  return TSR_OK;
+}
+
+void devbuf_free(DevBuf& b) {
+  cudaFree(b.p);
+  b.p = nullptr;
+  b.cap = 0;
+}
+
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream) {
   const int32_t B = mask->B, H = mask->H, N = mask->N;
@@ -372,11 +368,11 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   m.S = mask->frame_size;
   m.head_kind = P->head_kind_dev;
 
-  Scratch tmp;
-  int32_t* cnt = nullptr;
-  unsigned long long* tot = nullptr;
-  if (tsr_status s = tmp.get(&cnt, sizeof(int32_t) * 4 * n_items)) return s;
-  if (tsr_status s = tmp.get(&tot, sizeof(unsigned long long) * 8)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_tot, sizeof(unsigned long long) * 8)) return s;
+  if (!P->host_tot) TSR_CUDA(cudaMallocHost(&P->host_tot, sizeof(unsigned long long) * 9));
+  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
+  unsigned long long* tot = static_cast<unsigned long long*>(P->b_tot.p);
   TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
 
@@ -396,11 +392,12 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
                            256, 0, stream>>>(m.blocks, n_grid, tot + 6);
     TSR_CUDA(cudaGetLastError());
   }
-  unsigned long long host_tot[8];
-  uint32_t host_err = 0;
-  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof host_tot, cudaMemcpyDeviceToHost, stream));
-  TSR_CUDA(cudaMemcpyAsync(&host_err, P->err, sizeof host_err, cudaMemcpyDeviceToHost, stream));
+  unsigned long long* host_tot = P->host_tot;
+  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost,
+                           stream));
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
   TSR_CUDA(cudaStreamSynchronize(stream));
+  const uint32_t host_err = static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull);
   if (host_err & DEV_ERR_UNSUPPORTED)
     return fail(TSR_ERR_UNSUPPORTED,
                 "a 128-token tile overlaps more than 8 logical segments (blocks or segments "
@@ -446,14 +443,18 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   if (P->n_entries >= (int64_t{1} << 31) || P->n_desc >= (int64_t{1} << 31))
     return fail(TSR_ERR_UNSUPPORTED, "plan has more than 2^31 tiles");
 
-  if (tsr_status s = dev_alloc(&P->items, sizeof(tsr_plan_item) * n_items)) return s;
-  if (tsr_status s = dev_alloc(&P->entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
-  if (tsr_status s = dev_alloc(&P->descs, sizeof(tsr_tile_desc) * P->n_desc)) return s;
-
-  int32_t *ebegin = nullptr, *dbegin = nullptr, *hist = nullptr;
-  if (tsr_status s = tmp.get(&ebegin, sizeof(int32_t) * n_items)) return s;
-  if (tsr_status s = tmp.get(&dbegin, sizeof(int32_t) * n_items)) return s;
-  if (tsr_status s = tmp.get(&hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  if (tsr_status s = devbuf_reserve(P->b_items, sizeof(tsr_plan_item) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_descs, sizeof(tsr_tile_desc) * P->n_desc)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  P->items = P->b_items.p;
+  P->entries = P->b_entries.p;
+  P->descs = P->b_descs.p;
+  int32_t* ebegin = static_cast<int32_t*>(P->b_ebegin.p);
+  int32_t* dbegin = static_cast<int32_t*>(P->b_dbegin.p);
+  int32_t* hist = static_cast<int32_t*>(P->b_hist.p);
   const int32_t* cnt_e = cnt + (2 * which) * n_items;
   const int32_t* cnt_b = cnt + (2 * which + 1) * n_items;
   const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
@@ -466,8 +467,6 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
       m, nqt, rg.bn, ebegin, dbegin, static_cast<int2*>(P->entries),
       static_cast<tsr_tile_desc*>(P->descs));
   TSR_CUDA(cudaGetLastError());
-  // The temporary buffers are released when `tmp` goes out of scope; cudaFree
-  // waits for the device, so the kernels above have finished by then.
   return TSR_OK;
 }
 

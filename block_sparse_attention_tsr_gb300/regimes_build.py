@@ -1,0 +1,111 @@
+"""Offline profiling that fills the regime table (Tessera abstract:
+profile-guided regime selection through a lookup table built by offline
+profiling).
+
+For every mask class -- logical block shape, density bucket, sequence-length
+bucket, head dimension -- a few seeded synthetic masks of that class are planned
+and run with every kernel variant (tile width, pipeline depth, CTAs per SM); the
+fastest variant (median over the masks of plan + forward time) becomes the row
+of that class.  Run on the target GPU:
+
+    python -m block_sparse_attention_tsr_gb300.regimes_build [--out PATH] [--quick]
+
+and commit the written table (``regimes_gb300.txt`` next to this file), which
+the binding loads at start-up.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import block_sparse_attention_tsr_gb300 as tsr  # noqa: E402
+import workloads as W  # noqa: E402
+
+SHAPES = ((32, 32), (64, 64), (128, 128), (64, 256), (256, 64))
+DENSITY_EDGES = (0.0, 0.15, 0.30, 0.45, 0.60, 1.01)
+N_BUCKETS = ((0, 8191, 4096), (8192, 1 << 24, 32760))   # (n_min, n_max, N used to profile)
+VARIANTS = {128: ((128, 3, 1), (128, 2, 1), (64, 4, 1), (64, 2, 2)),
+            64: ((128, 4, 1), (64, 4, 1), (64, 3, 2))}
+
+
+def time_variant(mask, q, k, v, out, lse, variant, reps):
+    bn, stages, ctas = variant
+    plan = tsr.tsr_plan(mask, {"bn": bn, "stages": stages, "ctas_per_sm": ctas})
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        plan.update(mask)
+        tsr.tsr_bsa_forward(q, k, v, plan, out, lse)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        plan.update(mask)
+        tsr.tsr_bsa_forward(q, k, v, plan, out, lse)
+    b.record(stream)
+    torch.cuda.synchronize()
+    tsr.tsr_plan_device_status(plan)
+    plan.destroy()
+    return a.elapsed_time(b) / reps
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                  "regimes_gb300.txt"))
+    ap.add_argument("--heads", type=int, default=8)
+    ap.add_argument("--masks", type=int, default=2, help="seeded masks per class")
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--quick", action="store_true", help="d = 128, long sequences only")
+    args = ap.parse_args()
+    tsr.build()
+    tsr.lib()
+    tsr.tsr_regime_load(None)
+    rows = []
+    t0 = time.time()
+    dims = (128,) if args.quick else (128, 64)
+    nbs = N_BUCKETS[1:] if args.quick else N_BUCKETS
+    for d in dims:
+        for n_min, n_max, N in nbs:
+            q, k, v = (x.cuda() for x in W.qkv(1, args.heads, N, d, seed=5))
+            out = torch.empty_like(q)
+            lse = torch.empty((1, args.heads, N), device="cuda")
+            for bq, bk in SHAPES:
+                for lo, hi in zip(DENSITY_EDGES[:-1], DENSITY_EDGES[1:]):
+                    times = {vv: [] for vv in VARIANTS[d]}
+                    for m in range(args.masks):
+                        r = np.random.Generator(np.random.PCG64(1000 * bq + bk + 7919 * m))
+                        dens = np.clip(r.uniform(lo, min(hi, 1.0), size=(1, args.heads)), 0.01, 1.0)
+                        blocks = W.banded_blocks(1, args.heads, W.cdiv(N, bq), W.cdiv(N, bk), dens, r)
+                        spec = W.MaskSpec(W.MASK_UNIFORM, 1, args.heads, N, bq=bq, bk=bk, blocks=blocks)
+                        mask = tsr.make_mask(spec.kind, 1, args.heads, N, d, **W.mask_tensors(spec))
+                        for vv in VARIANTS[d]:
+                            times[vv].append(time_variant(mask, q, k, v, out, lse, vv, args.reps))
+                    med = {vv: float(np.median(t)) for vv, t in times.items()}
+                    best = min(med, key=med.get)
+                    rows.append((W.MASK_UNIFORM, bq, bk, n_min, n_max, lo, hi, d) + best)
+                    print(f"d={d} N={N} {bq}x{bk} dens[{lo:.2f},{hi:.2f}) -> {best}  " +
+                          " ".join(f"{vv}:{t:.3f}ms" for vv, t in med.items()), flush=True)
+            # masks of the other kinds: one default row per head dimension
+    rows.append(("*", "*", "*", "*", "*", "*", "*", 128, 64, 2, 2))
+    rows.append(("*", "*", "*", "*", "*", "*", "*", 64, 64, 3, 2))
+    with open(args.out, "w") as f:
+        f.write("# Regime table for GB300 (sm_103a), written by regimes_build.py\n")
+        f.write(f"# {time.strftime('%Y-%m-%d')}: {args.masks} seeded banded-plus-random masks per "
+                f"class, {args.heads} heads, median of plan + forward time\n")
+        f.write("# kind bq bk n_min n_max dens_min dens_max d bn stages ctas\n")
+        for r in rows:
+            f.write(" ".join(f"{x:.2f}" if isinstance(x, float) else str(x) for x in r) + "\n")
+    print(f"wrote {len(rows)} rows to {args.out} in {time.time() - t0:.0f} s")
+
+
+if __name__ == "__main__":
+    main()

@@ -170,6 +170,17 @@ tsr_status tsr_plan(const tsr_mask *mask, const tsr_plan_opts *opts, tsr_plan_t 
                     void *stream);
 
 /*
+ * tsr_plan_update -- rebuild an existing plan for a new mask with the same B, H,
+ * N and d (any mask kind), reusing the plan's device storage; it grows only when
+ * the new mask needs more tiles than any mask planned before.  Tessera abstract:
+ * masks change from request to request, so planning cost is part of every call.
+ * Same synchronisation and errors as tsr_plan(); on failure the plan must not be
+ * used for tsr_bsa_forward until a later update succeeds.  The plan must not be
+ * in use by queued tsr_bsa_forward work on another stream.
+ */
+tsr_status tsr_plan_update(tsr_plan_t plan, const tsr_mask *mask, void *stream);
+
+/*
  * tsr_bsa_forward -- the attention over a plan.
  *
  * q, k, v: bf16 [B][H][N][d] (device).  out: bf16 [B][H][N][d] (device), lse:

@@ -240,3 +240,29 @@ def test_sweep_members(m):
     spec = W.sweep_mask(m, H=4)
     plan = _sampled_parity(spec, 128, seed=100 + m, rows_per_head=16)
     check_coverage(spec, plan)
+
+
+def test_plan_update_across_masks():
+    """One plan re-planned for masks of different density, block shape and kind
+    (storage grows and is reused); every result and plan matches the oracle."""
+    N, H, d = 1500, 2, 128
+    q, k, v = W.qkv(1, H, N, d, 21)
+    r = np.random.Generator(np.random.PCG64(21))
+    specs = [
+        W.MaskSpec(W.MASK_UNIFORM, 1, H, N, bq=64, bk=64,
+                   blocks=(r.random((1, H, 24, 24)) < 0.1).astype(np.uint8)),
+        W.MaskSpec(W.MASK_UNIFORM, 1, H, N, bq=32, bk=32,
+                   blocks=(r.random((1, H, 47, 47)) < 0.7).astype(np.uint8)),
+        W.segment_mask(9, 1, H, N, lo=16, hi=200),
+        W.MaskSpec(W.MASK_UNIFORM, 1, H, N, bq=128, bk=64,
+                   blocks=(r.random((1, H, 12, 24)) < 0.3).astype(np.uint8)),
+    ]
+    plan = None
+    for spec in specs:
+        mask = tsr.make_mask(spec.kind, 1, H, N, d, **W.mask_tensors(spec))
+        plan = tsr.tsr_plan(mask) if plan is None else plan.update(mask)
+        out, lse = tsr.tsr_bsa_forward(q.cuda(), k.cuda(), v.cuda(), plan)
+        O_ref, L_ref = oracle.attention(spec, q, k, v)
+        compare(O_ref, L_ref, out.float().cpu().numpy(), lse.cpu().double().numpy(), "update")
+        check_coverage(spec, plan)
+    tsr.tsr_plan_device_status(plan)
