@@ -127,7 +127,7 @@ bool parse_table(const std::string& text, std::vector<RegimeRow>* out, std::stri
 bool rows_valid(const std::vector<RegimeRow>& rows) {
   for (const RegimeRow& r : rows)
     if ((r.bn != 64 && r.bn != 128) || (r.d != 64 && r.d != 128) ||
-        !variant_exists(r.d, r.bn, r.stages, r.ctas))
+        !variant_exists(r.d, r.bn, r.stages, r.ctas, r.kind == TSR_MASK_KEYLIST))
       return false;
   return true;
 }
@@ -200,7 +200,10 @@ tsr_status check_mask(const tsr_mask* m) {
         return fail(TSR_ERR_INVALID_ARG, "SVG needs N = n_frames * frame_size and head_kind");
       return TSR_OK;
     case TSR_MASK_KEYLIST:
-      return fail(TSR_ERR_UNSUPPORTED, "KEYLIST masks are not built in this version");
+      if (m->slice_m != 64 && m->slice_m != 128)
+        return fail(TSR_ERR_UNSUPPORTED, "KEYLIST slice_m must be 64 or 128");
+      if (!m->indptr || !m->indices) return fail(TSR_ERR_INVALID_ARG, "indptr / indices missing");
+      return TSR_OK;
     default:
       return fail(TSR_ERR_INVALID_ARG, "unknown mask kind");
   }
@@ -219,9 +222,8 @@ tsr_status check_bounds(const int32_t* dev, int32_t n, int32_t N, cudaStream_t s
 void free_plan(tsr_plan_s* P) {
   if (!P) return;
   for (DevBuf* b : {&P->b_items, &P->b_entries, &P->b_descs, &P->b_cnt, &P->b_tot, &P->b_ebegin,
-                    &P->b_dbegin, &P->b_hist})
+                    &P->b_dbegin, &P->b_hist, &P->b_gidx})
     devbuf_free(*b);
-  cudaFree(P->gidx);
   cudaFree(P->counter);
   cudaFree(P->err);
   cudaFree(P->head_kind_dev);
@@ -254,7 +256,14 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
     TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, P->head_layout.data(), mask->H,
                              cudaMemcpyHostToDevice, st));
   }
-  if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) return s;
+  P->gathered = 0;
+  P->slice_m = 0;
+  P->n_gidx = 0;
+  if (mask->kind == TSR_MASK_KEYLIST) {
+    if (tsr_status s = plan_build_keylist(mask, P->has_opts ? &P->opts : nullptr, P, st)) return s;
+  } else if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) {
+    return s;
+  }
   if (P->n_temporal > 0 && !P->scratch) {
     P->scratch_bytes = static_cast<size_t>(P->B) * P->H * P->N * P->d * 2;
     const cudaError_t e = cudaMalloc(&P->scratch, 3 * P->scratch_bytes);
@@ -556,6 +565,20 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       dm.q_bounds = p;
       dm.k_bounds = p + nq;
     }
+  } else if (mask->kind == TSR_MASK_KEYLIST) {
+    const int64_t n_lists = static_cast<int64_t>(mask->B) * mask->H *
+                            ((mask->N + mask->slice_m - 1) / mask->slice_m);
+    const int64_t n_idx = mask->indptr[n_lists];   // HOST array here
+    if (n_idx < 0) return fail(TSR_ERR_INVALID_ARG, "indptr must not decrease");
+    void *dp, *di;
+    if (tsr_status s = hc.get(5, sizeof(int64_t) * (n_lists + 1), &dp)) return s;
+    if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &di)) return s;
+    TSR_CUDA(cudaMemcpyAsync(dp, mask->indptr, sizeof(int64_t) * (n_lists + 1),
+                             cudaMemcpyHostToDevice, st));
+    if (n_idx)
+      TSR_CUDA(cudaMemcpyAsync(di, mask->indices, sizeof(int32_t) * n_idx, cudaMemcpyHostToDevice, st));
+    dm.indptr = static_cast<const int64_t*>(dp);
+    dm.indices = static_cast<const int32_t*>(di);
   } else if (mask->kind == TSR_MASK_SVG) {
     void* dh;
     if (tsr_status s = hc.get(7, mask->H, &dh)) return s;

@@ -49,6 +49,11 @@ struct FwdParams {
   uint32_t* err;
   int32_t n_items, N, F, S;
   float scale_log2;              // log2(e) / sqrt(d)
+  // gathered (KEYLIST) plans: K / V rows named by gidx, loaded by index
+  const __nv_bfloat16* kg;
+  const __nv_bfloat16* vg;
+  const int32_t* gidx;
+  int32_t slice_m;
 };
 
 // Rescale the running output only when the running maximum grew by more than
@@ -129,7 +134,7 @@ __device__ __forceinline__ void add_range(uint32_t (&words)[BN / 32], int lo, in
   }
 }
 
-template <int D, int BN, int STAGES, int CTAS>
+template <int D, int BN, int STAGES, int CTAS, bool GATHER>
 __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D, BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -181,6 +186,49 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     }
     uint32_t item_seq = 0, kv_cnt = 0, q_cnt = 0, k_iss = 0, v_iss = 0;
     bool ok = true;
+    // Gathered tiles (FG-Attn abstract: only the listed keys of a query block are
+    // loaded, packed into dense tiles in shared memory).  The warp copies the
+    // listed K or V rows with 16-byte cp.async straight into the 128-byte
+    // swizzled layout the MMA reads; one copy group per tile.  A group is
+    // published (proxy fence, then the tile's full barrier) once the next group
+    // has been issued, so one tile's copies are always in flight.
+    uint32_t pend_bar = 0;
+    bool pending = false;
+    auto gather_rows = [&](const __nv_bfloat16* head_base, int32_t kv, uint32_t dst) {
+      constexpr int UNITS = D / 8;        // 16-byte units per row
+      constexpr int RPI = 32 / UNITS;     // rows per warp instruction
+      int32_t my_idx[BN / 32];
+#pragma unroll
+      for (int m = 0; m < BN / 32; ++m) my_idx[m] = __ldg(p.gidx + kv + 32 * m + lane);
+#pragma unroll
+      for (int m = 0; m < BN / RPI; ++m) {
+        const int row = RPI * m + lane / UNITS;
+        const int key = __shfl_sync(0xFFFFFFFFu, my_idx[(RPI * m) / 32], row & 31);
+        const int j = lane % UNITS, c = j >> 3, u = j & 7;
+        const void* src = reinterpret_cast<const uint8_t*>(head_base + static_cast<size_t>(key) * D) + j * 16;
+        cp_async_16(dst + c * BN * 128 + row * 128 + ((u ^ (row & 7)) << 4), src);
+      }
+      cp_async_commit();
+    };
+    auto retire_push = [&](uint32_t bar) {
+      if (pending) {
+        cp_async_wait_1();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pend_bar);
+      }
+      pend_bar = bar;
+      pending = true;
+    };
+    auto drain = [&]() {
+      if (pending) {
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pend_bar);
+        pending = false;
+      }
+    };
     while (ok) {
       int32_t it = 0;
       if (lane == 0) it = atomicAdd(p.counter, 1);
@@ -201,6 +249,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       const CUtensorMap* mq = layout ? &p.tq_p : &p.tq;
       const CUtensorMap* mk = layout ? &p.tk_p : &p.tk;
       const CUtensorMap* mv = layout ? &p.tv_p : &p.tv;
+      const size_t head_off = static_cast<size_t>(bh) * p.N * D;
       if (!mbar_wait(smem_u32(&ctrl.q_empty), (q_cnt & 1) ^ 1, abort_flag, p.err)) break;
       if (lane == 0) {
         const uint32_t bar = smem_u32(&ctrl.q_full);
@@ -222,10 +271,13 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             ok = false;
             break;
           }
-          if (lane == 0) {
+          const uint32_t kb = smem_u32(&ctrl.k_full[s]);
+          const uint32_t sk = sK0 + s * C::KV_BYTES;
+          if constexpr (GATHER) {
+            gather_rows(p.kg + head_off, __ldg(&p.entries[begin + i]).x, sk);
+            retire_push(kb);
+          } else if (lane == 0) {
             const int32_t kv = __ldg(&p.entries[begin + i]).x;
-            const uint32_t kb = smem_u32(&ctrl.k_full[s]);
-            const uint32_t sk = sK0 + s * C::KV_BYTES;
             mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tma_load_3d(sk + c * BN * 128, mk, kb, c * 64, kv, bh);
@@ -239,10 +291,13 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             ok = false;
             break;
           }
-          if (lane == 0) {
+          const uint32_t vb = smem_u32(&ctrl.v_full[s]);
+          const uint32_t sv = sV0 + s * C::KV_BYTES;
+          if constexpr (GATHER) {
+            gather_rows(p.vg + head_off, __ldg(&p.entries[begin + i - 1]).x, sv);
+            retire_push(vb);
+          } else if (lane == 0) {
             const int32_t kv = __ldg(&p.entries[begin + i - 1]).x;
-            const uint32_t vb = smem_u32(&ctrl.v_full[s]);
-            const uint32_t sv = sV0 + s * C::KV_BYTES;
             mbar_arrive_expect_tx(vb, C::KV_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tma_load_3d(sv + c * BN * 128, mv, vb, c * 64, kv, bh);
@@ -251,10 +306,14 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         }
       }
       kv_cnt += n;
+      // the item's last gathered copies are published before the producer can
+      // block on the work-item queue
+      if constexpr (GATHER) drain();
     }
+    if constexpr (GATHER) cp_async_wait_all();
     // On an abort, let the copies already issued land before the CTA exits
     // (the last STAGES of each stream; earlier ones were consumed).
-    if (*abort_flag) {
+    if (!GATHER && *abort_flag) {
       volatile int32_t dummy = 0;
       for (uint32_t k = (k_iss > STAGES ? k_iss - STAGES : 0); k < k_iss; ++k)
         mbar_wait(smem_u32(&ctrl.k_full[k % STAGES]), (k / STAGES) & 1, &dummy, p.err);
@@ -393,7 +452,25 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         // column contributes nothing (P = 0, no exponentials); a row whose
         // segment allows every in-range column needs no per-element masking.
         bool row_dead = false;
-        if (desc >= 0) {
+        if (GATHER && desc >= 0) {
+          // list form: one BN-bit column mask per slice_m-row segment
+          const bool hi = (p.slice_m == 64) && (r >= 64);
+          const uint32_t w4[4] = {hi ? d1.x : d0.x, hi ? d1.y : d0.y, hi ? d1.z : d0.z,
+                                  hi ? d1.w : d0.w};
+          uint32_t any = 0u, all = 0xFFFFFFFFu;
+#pragma unroll
+          for (int w = 0; w < BN / 32; ++w) {
+            any |= w4[w];
+            all &= w4[w];
+          }
+          if (any == 0u) {
+            row_dead = true;
+          } else if (all != 0xFFFFFFFFu) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (!((w4[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+          }
+        } else if (desc >= 0) {
           const int n_r = d0.x & 0xFF, n_c = (d0.x >> 8) & 0xFF;
           int rs = 0;
 #pragma unroll
@@ -579,10 +656,10 @@ bool get_encode() {
   return true;
 }
 
-template <int D, int BN, int STAGES, int CTAS>
+template <int D, int BN, int STAGES, int CTAS, bool GATHER>
 tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStream_t stream) {
   using C = Cfg<D, BN, STAGES>;
-  auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS>;
+  auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS, GATHER>;
   static bool attr_set[64] = {false};
   if (device < 0 || device >= 64 || !attr_set[device]) {
     TSR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
@@ -595,8 +672,8 @@ tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStr
   return TSR_OK;
 }
 
-constexpr int vkey(int d, int bn, int stages, int ctas) {
-  return d * 100000 + bn * 100 + stages * 10 + ctas;
+constexpr int vkey(int d, int bn, int stages, int ctas, int gathered = 0) {
+  return gathered * 10000000 + d * 100000 + bn * 100 + stages * 10 + ctas;
 }
 
 }  // namespace
@@ -614,19 +691,22 @@ bool encode_tmap_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool variant_exists(int d, int bn, int stages, int ctas) {
-  switch (vkey(d, bn, stages, ctas)) {
-    case vkey(128, 128, 3, 1):
-    case vkey(128, 128, 2, 1):
-    case vkey(128, 64, 4, 1):
-    case vkey(128, 64, 2, 2):
-    case vkey(64, 128, 4, 1):
-    case vkey(64, 64, 4, 1):
-    case vkey(64, 64, 3, 2):
-      return true;
-    default:
-      return false;
-  }
+// Kernel variants compiled into the library: (d, BN, stages, CTAs per SM) for
+// contiguous tiles, and a subset for gathered (KEYLIST) tiles.
+#define TSR_VARIANTS_CONTIGUOUS(X) \
+  X(128, 128, 3, 1) X(128, 128, 2, 1) X(128, 64, 4, 1) X(128, 64, 2, 2) \
+  X(64, 128, 4, 1) X(64, 64, 4, 1) X(64, 64, 3, 2)
+#define TSR_VARIANTS_GATHERED(X) X(128, 128, 3, 1) X(128, 64, 2, 2) X(64, 128, 4, 1) X(64, 64, 3, 2)
+
+bool variant_exists(int d, int bn, int stages, int ctas, bool gathered) {
+  const int key = vkey(d, bn, stages, ctas, gathered ? 1 : 0);
+#define TSR_CHECK_C(D_, BN_, S_, C_) if (key == vkey(D_, BN_, S_, C_, 0)) return true;
+#define TSR_CHECK_G(D_, BN_, S_, C_) if (key == vkey(D_, BN_, S_, C_, 1)) return true;
+  TSR_VARIANTS_CONTIGUOUS(TSR_CHECK_C)
+  TSR_VARIANTS_GATHERED(TSR_CHECK_G)
+#undef TSR_CHECK_C
+#undef TSR_CHECK_G
+  return false;
 }
 
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
@@ -660,22 +740,26 @@ tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
   prm.F = P->F;
   prm.S = P->S;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P->d)));
+  prm.kg = static_cast<const __nv_bfloat16*>(a.k);
+  prm.vg = static_cast<const __nv_bfloat16*>(a.v);
+  prm.gidx = P->gidx;
+  prm.slice_m = P->slice_m;
   TSR_CUDA(cudaMemsetAsync(P->counter, 0, sizeof(int32_t), stream));
   const int n = static_cast<int>(P->n_items), dev = P->device;
-  switch (vkey(P->d, P->bn, P->stages, P->ctas)) {
-    case vkey(128, 128, 3, 1): return launch_variant<128, 128, 3, 1>(prm, n, dev, stream);
-    case vkey(128, 128, 2, 1): return launch_variant<128, 128, 2, 1>(prm, n, dev, stream);
-    case vkey(128, 64, 4, 1): return launch_variant<128, 64, 4, 1>(prm, n, dev, stream);
-    case vkey(128, 64, 2, 2): return launch_variant<128, 64, 2, 2>(prm, n, dev, stream);
-    case vkey(64, 128, 4, 1): return launch_variant<64, 128, 4, 1>(prm, n, dev, stream);
-    case vkey(64, 64, 4, 1): return launch_variant<64, 64, 4, 1>(prm, n, dev, stream);
-    case vkey(64, 64, 3, 2): return launch_variant<64, 64, 3, 2>(prm, n, dev, stream);
-    default:
-      return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) +
-                                           " bn=" + std::to_string(P->bn) + " stages=" +
-                                           std::to_string(P->stages) + " ctas=" +
-                                           std::to_string(P->ctas));
-  }
+  const int key = vkey(P->d, P->bn, P->stages, P->ctas, P->gathered ? 1 : 0);
+#define TSR_LAUNCH_C(D_, BN_, S_, C_) \
+  if (key == vkey(D_, BN_, S_, C_, 0)) return launch_variant<D_, BN_, S_, C_, false>(prm, n, dev, stream);
+#define TSR_LAUNCH_G(D_, BN_, S_, C_) \
+  if (key == vkey(D_, BN_, S_, C_, 1)) return launch_variant<D_, BN_, S_, C_, true>(prm, n, dev, stream);
+  TSR_VARIANTS_CONTIGUOUS(TSR_LAUNCH_C)
+  TSR_VARIANTS_GATHERED(TSR_LAUNCH_G)
+#undef TSR_LAUNCH_C
+#undef TSR_LAUNCH_G
+  return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) + " bn=" +
+                                       std::to_string(P->bn) + " stages=" +
+                                       std::to_string(P->stages) + " ctas=" +
+                                       std::to_string(P->ctas) +
+                                       (P->gathered ? " (gathered)" : ""));
 }
 
 }  // namespace tsr

@@ -71,7 +71,7 @@ struct tsr_plan_impl {
   void* scratch = nullptr;   // temporal-major Q, K, V copies: 3 x [B][H][N][d] bf16
   size_t scratch_bytes = 0;
   // storage reused when the plan is rebuilt for a new mask (tsr_plan_update)
-  DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist;
+  DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist, b_gidx;
   unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
   bool has_opts = false;
   tsr_plan_opts opts{};
@@ -85,6 +85,12 @@ void devbuf_free(DevBuf& b);
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream);
 
+tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
+                              cudaStream_t stream);
+tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items,
+                              int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
+                              int32_t* ebegin, int32_t* dbegin, int32_t* hist, void* items,
+                              cudaStream_t stream);
 tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
                            uint32_t* err, int64_t n_grid, cudaStream_t stream);
 tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int32_t* cnt_e,
@@ -105,7 +111,7 @@ struct FwdArgs {
   const tsr_plan_impl* plan;
 };
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream);
-bool variant_exists(int d, int bn, int stages, int ctas);
+bool variant_exists(int d, int bn, int stages, int ctas, bool gathered);
 
 // permutation (permute.cu)
 tsr_status launch_permute(const void* src, void* dst, int32_t B, int32_t H, int32_t F, int32_t S,

@@ -343,6 +343,17 @@ void devbuf_free(DevBuf& b) {
   b.cap = 0;
 }
 
+tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items,
+                              int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
+                              int32_t* ebegin, int32_t* dbegin, int32_t* hist, void* items,
+                              cudaStream_t stream) {
+  plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, H, nullptr, 0, max_len,
+                                               lpt, ebegin, dbegin, hist,
+                                               static_cast<int4*>(items));
+  TSR_CUDA(cudaGetLastError());
+  return TSR_OK;
+}
+
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream) {
   const int32_t B = mask->B, H = mask->H, N = mask->N;
@@ -427,7 +438,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     if (opts->ctas_per_sm) rg.ctas = opts->ctas_per_sm, rg.id = -1;
   }
   if (rg.bn != 64 && rg.bn != 128) return fail(TSR_ERR_INVALID_ARG, "bn must be 64 or 128");
-  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas))
+  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas, false))
     return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) +
                                          " bn=" + std::to_string(rg.bn) + " stages=" +
                                          std::to_string(rg.stages) + " ctas=" +

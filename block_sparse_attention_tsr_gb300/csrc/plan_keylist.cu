@@ -1,0 +1,304 @@
+// plan_keylist.cu -- planning of M x 1 key-slice (KEYLIST) masks.
+//
+// FG-Attn abstract: attention is skipped at the granularity of M x 1 slices (a
+// block of M = 64 queries times one key); for each query block only its listed
+// keys are loaded, gathered into packed tiles in shared memory.  Physical tiles
+// are 128 query rows, so a query tile holds two 64-query blocks (or one block
+// when M = 128).  The tile's key stream is the sorted union of its blocks'
+// lists, cut into BN-key gathered tiles; each gathered tile carries the key
+// indices (gidx) and a list descriptor with one BN-bit column mask per query
+// block (a key of the union that one block does not list is masked for that
+// block's rows).  Tiles where both blocks list every key are marked full.
+//
+// Kernels: validate (lists sorted, unique, in range), count (union sizes for
+// both tile widths), the shared schedule kernel (longest first), emit (one
+// block per query tile merges the two lists).
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tsr {
+
+namespace {
+
+__device__ __forceinline__ int64_t lower_bound_i32(const int32_t* a, int64_t n, int32_t x) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// One warp per list.
+__global__ void keylist_validate_kernel(const int64_t* indptr, const int32_t* indices,
+                                        int64_t n_lists, int32_t N, uint32_t* err) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n_lists) return;
+  const int64_t b = indptr[w], e = indptr[w + 1];
+  bool bad = (w == 0 && b != 0) || e < b;
+  if (!bad) {
+    for (int64_t q = b + lane; q < e; q += 32) {
+      const int32_t k = indices[q];
+      if (k < 0 || k >= N || (q + 1 < e && indices[q + 1] <= k)) bad = true;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(err, DEV_ERR_BAD_INPUT);
+}
+
+struct Lists {
+  const int32_t* a;
+  const int32_t* b;
+  int64_t na, nb;
+  bool b_rows;   // rows of the second block exist (inside [0, N))
+};
+
+__device__ __forceinline__ Lists tile_lists(const int64_t* indptr, const int32_t* indices,
+                                            int64_t item, int32_t nqt, int32_t nqb, int32_t slice_m,
+                                            int32_t N) {
+  const int64_t bh = item / nqt, qt = item % nqt;
+  Lists L;
+  const int64_t qa = (slice_m == 64) ? 2 * qt : qt;
+  const int64_t ra = bh * nqb + qa;
+  L.a = indices + indptr[ra];
+  L.na = indptr[ra + 1] - indptr[ra];
+  L.b = L.a;
+  L.nb = 0;
+  L.b_rows = false;
+  if (slice_m == 64 && qa + 1 < nqb) {
+    L.b = indices + indptr[ra + 1];
+    L.nb = indptr[ra + 2] - indptr[ra + 1];
+    L.b_rows = true;
+  }
+  return L;
+}
+
+// Per query tile: [0] tiles at BN=64, [1] tiles at BN=128, [2] union size.
+// Totals: [0] tiles BN=64, [1] tiles BN=128, [2] max BN=64, [3] max BN=128,
+// [4] sum of list lengths.
+__global__ void keylist_count_kernel(const int64_t* indptr, const int32_t* indices, int64_t n_items,
+                                     int32_t nqt, int32_t nqb, int32_t slice_m, int32_t N,
+                                     int32_t* cnt, unsigned long long* tot) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n_items) return;
+  const Lists L = tile_lists(indptr, indices, w, nqt, nqb, slice_m, N);
+  // common keys: search the shorter list's keys in the longer one
+  const int32_t* s = L.na <= L.nb ? L.a : L.b;
+  const int32_t* g = L.na <= L.nb ? L.b : L.a;
+  const int64_t ns = L.na <= L.nb ? L.na : L.nb, ng = L.na <= L.nb ? L.nb : L.na;
+  int64_t common = 0;
+  for (int64_t i = lane; i < ns; i += 32) {
+    const int64_t k = lower_bound_i32(g, ng, s[i]);
+    common += (k < ng && g[k] == s[i]);
+  }
+  for (int o = 16; o > 0; o >>= 1) common += __shfl_xor_sync(0xFFFFFFFFu, common, o);
+  if (lane == 0) {
+    const int64_t u = L.na + L.nb - common;
+    const int32_t e64 = static_cast<int32_t>((u + 63) / 64), e128 = static_cast<int32_t>((u + 127) / 128);
+    cnt[w] = e64;
+    cnt[n_items + w] = e128;
+    cnt[2 * n_items + w] = static_cast<int32_t>(u);
+    atomicAdd(&tot[0], static_cast<unsigned long long>(e64));
+    atomicAdd(&tot[1], static_cast<unsigned long long>(e128));
+    atomicMax(&tot[2], static_cast<unsigned long long>(e64));
+    atomicMax(&tot[3], static_cast<unsigned long long>(e128));
+    atomicAdd(&tot[4], static_cast<unsigned long long>(L.na + L.nb));
+  }
+}
+
+// Exclusive prefix sum of one flag per thread over the block (blockDim = 256);
+// returns this thread's prefix and adds the block total to *carry (uniform).
+__device__ __forceinline__ int block_scan_flags(int flag, int* warp_tot, int* carry) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xFFFFFFFFu, flag);
+  const int in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) warp_tot[warp] = __popc(bal);
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int i = 0; i < 8; ++i) {
+    const int t = warp_tot[i];
+    if (i < warp) before += t;
+    total += t;
+  }
+  const int res = *carry + before + in_warp;
+  __syncthreads();
+  if (threadIdx.x == 0) *carry += total;
+  __syncthreads();
+  return res;
+}
+
+// One block of 256 threads per query tile: merge the two sorted lists into the
+// union, write each union key at its rank into gidx, set its column bit for the
+// block(s) that list it, pad the last tile, then mark full tiles.
+__global__ void __launch_bounds__(256) keylist_emit_kernel(
+    const int64_t* indptr, const int32_t* indices, int32_t nqt, int32_t nqb, int32_t slice_m,
+    int32_t N, int32_t bn, const int32_t* cnt_e, const int32_t* cnt_u, const int32_t* ebegin,
+    int2* entries, uint32_t* descs, int32_t* gidx) {
+  __shared__ int warp_tot[8];
+  __shared__ int carry;
+  const int64_t item = blockIdx.x;
+  const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
+  const int64_t e0 = ebegin[item];
+  const int32_t ne = cnt_e[item];
+  const int64_t u = cnt_u[item];
+  uint32_t* dw = descs + e0 * 8;                 // 8 words (32 bytes) per tile
+  for (int64_t i = threadIdx.x; i < static_cast<int64_t>(ne) * 8; i += blockDim.x) dw[i] = 0u;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  int32_t* gx = gidx + e0 * bn;
+  // keys of the first list: rank = i + #{b < a} - #{common keys before a}
+  for (int64_t base = 0; base < L.na; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    int32_t a = 0;
+    int64_t lb = 0;
+    int in_b = 0;
+    if (i < L.na) {
+      a = L.a[i];
+      lb = lower_bound_i32(L.b, L.nb, a);
+      in_b = (lb < L.nb && L.b[lb] == a);
+    }
+    const int common_before = block_scan_flags(in_b, warp_tot, &carry);
+    if (i < L.na) {
+      const int64_t pos = i + lb - common_before;
+      gx[pos] = a;
+      uint32_t* d = dw + (pos / bn) * 8;
+      const int c = static_cast<int>(pos % bn);
+      atomicOr(&d[c >> 5], 1u << (c & 31));
+      if (in_b) atomicOr(&d[4 + (c >> 5)], 1u << (c & 31));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  // keys only the second list holds: rank = j + #{a < b} - #{common keys before b}
+  for (int64_t base = 0; base < L.nb; base += blockDim.x) {
+    const int64_t j = base + threadIdx.x;
+    int32_t b = 0;
+    int64_t lb = 0;
+    int in_a = 0;
+    if (j < L.nb) {
+      b = L.b[j];
+      lb = lower_bound_i32(L.a, L.na, b);
+      in_a = (lb < L.na && L.a[lb] == b);
+    }
+    const int common_before = block_scan_flags(in_a, warp_tot, &carry);
+    if (j < L.nb && !in_a) {
+      const int64_t pos = j + lb - common_before;
+      gx[pos] = b;
+      uint32_t* d = dw + (pos / bn) * 8;
+      const int c = static_cast<int>(pos % bn);
+      atomicOr(&d[4 + (c >> 5)], 1u << (c & 31));
+    }
+  }
+  // padding of the last tile: any in-range key; its columns stay masked
+  for (int64_t pos = u + threadIdx.x; pos < static_cast<int64_t>(ne) * bn; pos += blockDim.x)
+    gx[pos] = 0;
+  __threadfence_block();
+  __syncthreads();
+  for (int32_t c = threadIdx.x; c < ne; c += blockDim.x) {
+    const volatile uint32_t* d = dw + c * 8;
+    bool full = static_cast<int64_t>(c + 1) * bn <= u;
+    for (int w = 0; w < bn / 32; ++w) {
+      full = full && d[w] == 0xFFFFFFFFu;
+      if (L.b_rows) full = full && d[4 + w] == 0xFFFFFFFFu;
+    }
+    entries[e0 + c] = make_int2(static_cast<int32_t>((e0 + c) * bn),
+                                full ? -1 : static_cast<int32_t>(e0 + c));
+  }
+}
+
+}  // namespace
+
+tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
+                              cudaStream_t stream) {
+  const int32_t B = mask->B, H = mask->H, N = mask->N, M = mask->slice_m;
+  const int32_t nqt = (N + kBM - 1) / kBM, nqb = (N + M - 1) / M;
+  const int64_t n_items = static_cast<int64_t>(B) * H * nqt;
+  const int64_t n_lists = static_cast<int64_t>(B) * H * nqb;
+  P->n_items = n_items;
+  P->gathered = 1;
+  P->slice_m = M;
+  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 3 * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_tot, sizeof(unsigned long long) * 8)) return s;
+  if (!P->host_tot) TSR_CUDA(cudaMallocHost(&P->host_tot, sizeof(unsigned long long) * 9));
+  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
+  unsigned long long* tot = static_cast<unsigned long long*>(P->b_tot.p);
+  TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
+  TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
+  const int threads = 256;
+  keylist_validate_kernel<<<static_cast<unsigned>((n_lists * 32 + threads - 1) / threads), threads, 0,
+                            stream>>>(mask->indptr, mask->indices, n_lists, N, P->err);
+  TSR_CUDA(cudaGetLastError());
+  unsigned long long* host_tot = P->host_tot;
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+  if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
+    return fail(TSR_ERR_INVALID_ARG,
+                "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward");
+  keylist_count_kernel<<<static_cast<unsigned>((n_items * 32 + threads - 1) / threads), threads, 0,
+                         stream>>>(mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
+  TSR_CUDA(cudaGetLastError());
+  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost,
+                           stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+
+  P->n_logical_on = static_cast<int64_t>(host_tot[4]);
+  P->n_logical_total = n_lists * static_cast<int64_t>(N);
+  const double density = static_cast<double>(host_tot[4]) / static_cast<double>(n_lists) / N;
+  Regime rg = regime_lookup(TSR_MASK_KEYLIST, M, 1, N, density, P->d);
+  if (opts) {
+    if (opts->bn) rg.bn = opts->bn, rg.id = -1;
+    if (opts->stages) rg.stages = opts->stages, rg.id = -1;
+    if (opts->ctas_per_sm) rg.ctas = opts->ctas_per_sm, rg.id = -1;
+  }
+  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas, true))
+    return fail(TSR_ERR_UNSUPPORTED, "no gathered kernel variant for d=" + std::to_string(P->d) +
+                                         " bn=" + std::to_string(rg.bn) + " stages=" +
+                                         std::to_string(rg.stages) + " ctas=" +
+                                         std::to_string(rg.ctas));
+  P->bn = rg.bn;
+  P->stages = rg.stages;
+  P->ctas = rg.ctas;
+  P->regime_id = rg.id;
+  const int which = (rg.bn == 64) ? 0 : 1;
+  P->n_entries = static_cast<int64_t>(host_tot[which]);
+  P->n_desc = P->n_entries;
+  P->n_gidx = P->n_entries * rg.bn;
+  P->max_item_len = static_cast<int64_t>(host_tot[2 + which]);
+  if (P->n_gidx >= (int64_t{1} << 31))
+    return fail(TSR_ERR_UNSUPPORTED, "gathered plan has more than 2^31 key slots");
+
+  if (tsr_status s = devbuf_reserve(P->b_items, sizeof(tsr_plan_item) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_descs, 32 * static_cast<size_t>(P->n_desc))) return s;
+  if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  P->items = P->b_items.p;
+  P->entries = P->b_entries.p;
+  P->descs = P->b_descs.p;
+  P->gidx = static_cast<int32_t*>(P->b_gidx.p);
+  int32_t* ebegin = static_cast<int32_t*>(P->b_ebegin.p);
+  const int32_t* cnt_e = cnt + which * n_items;
+  const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
+  if (tsr_status s = plan_schedule_into(cnt_e, cnt_e, n_items, nqt, H, lpt,
+                                        static_cast<int32_t>(P->max_item_len), ebegin,
+                                        static_cast<int32_t*>(P->b_dbegin.p),
+                                        static_cast<int32_t*>(P->b_hist.p), P->items, stream))
+    return s;
+  if (n_items > 0) {
+    keylist_emit_kernel<<<static_cast<unsigned>(n_items), 256, 0, stream>>>(
+        mask->indptr, mask->indices, nqt, nqb, M, N, rg.bn, cnt_e, cnt + 2 * n_items, ebegin,
+        static_cast<int2*>(P->entries), static_cast<uint32_t*>(P->descs), P->gidx);
+    TSR_CUDA(cudaGetLastError());
+  }
+  return TSR_OK;
+}
+
+}  // namespace tsr

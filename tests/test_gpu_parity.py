@@ -266,3 +266,80 @@ def test_plan_update_across_masks():
         compare(O_ref, L_ref, out.float().cpu().numpy(), lse.cpu().double().numpy(), "update")
         check_coverage(spec, plan)
     tsr.tsr_plan_device_status(plan)
+
+
+# ------------------------------------------------------- KEYLIST (gathered)
+KEYLIST_CASES = [
+    # (N, H, d, slice_m, lo, hi, opts)
+    (1000, 2, 128, 64, 0, 400, None),
+    (777, 2, 128, 64, 1, 777, {"bn": 128, "stages": 3, "ctas_per_sm": 1}),
+    (1024, 1, 64, 128, 0, 300, None),
+    (1100, 2, 64, 64, 5, 200, {"bn": 128, "stages": 4, "ctas_per_sm": 1}),
+    (640, 1, 128, 128, 640, 640, None),          # every key listed: full gathered tiles
+]
+
+
+@pytest.mark.parametrize("case", KEYLIST_CASES, ids=[str(i) for i in range(len(KEYLIST_CASES))])
+def test_keylist_masks(case):
+    N, H, d, M, lo, hi, opts = case
+    spec = W.random_keylist(N + M, 1, H, N, slice_m=M, lo=lo, hi=hi)
+    (q, k, v), plan, O, L = run(spec, d, seed=N + 1, opts=opts)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, f"keylist {case}")
+    st = check_coverage(spec, plan)
+    assert plan.stats()["gathered"] == 1
+    if lo == hi == N:
+        assert st["full"] == st["tiles"]
+
+
+def test_keylist_clustered_runs():
+    """FG-Attn-shaped lists: clustered runs (Geometric lengths) covering 15% of keys."""
+    spec = W.keylist_mask(seed=4, H=2, N=4096)
+    (q, k, v), plan, O, L = run(spec, 128, seed=4)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "keylist clustered")
+    check_coverage(spec, plan)
+
+
+def test_keylist_invalid_lists_rejected():
+    spec = W.random_keylist(3, 1, 1, 512, slice_m=64, lo=4, hi=20)
+    bad = spec.indices.copy()
+    bad[2] = bad[1]                                  # a repeated key
+    spec.indices = bad
+    mask = tsr.make_mask(spec.kind, 1, 1, 512, 64, **W.mask_tensors(spec))
+    with pytest.raises(tsr.TsrError) as e:
+        tsr.tsr_plan(mask)
+    assert e.value.status == 1
+    spec.indices = np.where(np.arange(len(bad)) == 0, 600, spec.indices).astype(np.int32)  # out of range
+    mask = tsr.make_mask(spec.kind, 1, 1, 512, 64, **W.mask_tensors(spec))
+    with pytest.raises(tsr.TsrError):
+        tsr.tsr_plan(mask)
+
+
+@pytest.mark.slow
+def test_keylist_720p_coverage_two_heads():
+    spec = W.keylist_mask(seed=4, H=2)               # 75,600 tokens, 11,340 keys per block
+    (q, k, v), plan, O, L = run(spec, 128, seed=40)
+    check_coverage(spec, plan)
+    rows = _sample_rows(spec, 32, 40)
+    O_ref, L_ref, _ = oracle.attention_rows(spec, q, k, v, rows)
+    compare(O_ref, L_ref, O.reshape(-1, 128)[rows], L.reshape(-1)[rows], "keylist 720p H2")
+
+
+@pytest.mark.slow
+def test_keylist_720p_full_size():
+    spec = W.keylist_mask(seed=4)                     # 24 heads x 75,600 tokens
+    _sampled_parity(spec, 128, seed=4, rows_per_head=12)
+
+
+def test_host_entry_point_keylist():
+    spec = W.random_keylist(8, 1, 2, 900, slice_m=64, lo=0, hi=300)
+    q, k, v = W.qkv(1, 2, 900, 128, 8)
+    _, _, O, L = run(spec, 128, seed=0, qkv=(q, k, v))
+    out = torch.empty_like(q).pin_memory()
+    lse = torch.empty((1, 2, 900), dtype=torch.float32).pin_memory()
+    tsr.tsr_attention_host(spec.kind, 1, 2, 900, 128, q.pin_memory(), k.pin_memory(),
+                           v.pin_memory(), out, lse, slice_m=64, indptr=spec.indptr,
+                           indices=spec.indices)
+    assert np.array_equal(out.float().numpy(), O)
+    assert np.array_equal(lse.double().numpy(), L)
