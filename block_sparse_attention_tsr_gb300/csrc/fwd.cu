@@ -709,6 +709,26 @@ bool variant_exists(int d, int bn, int stages, int ctas, bool gathered) {
   return false;
 }
 
+// Complete a partly specified regime: fields given as 0 are free; the first
+// compiled variant that matches every given field is taken.
+bool variant_pick(int d, bool gathered, int bn, int stages, int ctas, int* out_bn, int* out_st,
+                  int* out_ct) {
+#define TSR_PICK(D_, BN_, S_, C_)                                                         \
+  if (D_ == d && (!bn || bn == BN_) && (!stages || stages == S_) && (!ctas || ctas == C_)) { \
+    *out_bn = BN_;                                                                        \
+    *out_st = S_;                                                                         \
+    *out_ct = C_;                                                                         \
+    return true;                                                                          \
+  }
+  if (gathered) {
+    TSR_VARIANTS_GATHERED(TSR_PICK)
+  } else {
+    TSR_VARIANTS_CONTIGUOUS(TSR_PICK)
+  }
+#undef TSR_PICK
+  return false;
+}
+
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
   const tsr_plan_impl* P = a.plan;
   if (P->n_items == 0) return TSR_OK;

@@ -112,6 +112,12 @@ struct FwdArgs {
 };
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream);
 bool variant_exists(int d, int bn, int stages, int ctas, bool gathered);
+bool variant_pick(int d, bool gathered, int bn, int stages, int ctas, int* out_bn, int* out_st,
+                  int* out_ct);
+// The regime for a plan: the table's choice, with the caller's overrides (opts
+// fields that are nonzero) taking precedence; completed to a compiled variant.
+tsr_status resolve_regime(Regime table, const tsr_plan_opts* opts, int d, bool gathered,
+                          Regime* out);
 
 // permutation (permute.cu)
 tsr_status launch_permute(const void* src, void* dst, int32_t B, int32_t H, int32_t F, int32_t S,

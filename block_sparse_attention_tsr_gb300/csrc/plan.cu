@@ -343,6 +343,36 @@ void devbuf_free(DevBuf& b) {
   b.cap = 0;
 }
 
+tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gathered,
+                          Regime* out) {
+  if (opts && (opts->bn || opts->stages || opts->ctas_per_sm)) {
+    if (opts->bn && opts->bn != 64 && opts->bn != 128)
+      return fail(TSR_ERR_INVALID_ARG, "bn must be 64 or 128");
+    int bn = 0, st = 0, ct = 0;
+    // the caller's fields, then the table's for the rest if that combination exists
+    const int want_bn = opts->bn, want_st = opts->stages, want_ct = opts->ctas_per_sm;
+    if (!variant_pick(d, gathered, want_bn ? want_bn : rg.bn, want_st ? want_st : rg.stages,
+                      want_ct ? want_ct : rg.ctas, &bn, &st, &ct) &&
+        !variant_pick(d, gathered, want_bn, want_st, want_ct, &bn, &st, &ct))
+      return fail(TSR_ERR_UNSUPPORTED,
+                  "no kernel variant for d=" + std::to_string(d) + " bn=" + std::to_string(want_bn) +
+                      " stages=" + std::to_string(want_st) + " ctas=" + std::to_string(want_ct) +
+                      (gathered ? " (gathered)" : ""));
+    *out = Regime{bn, st, ct, -1};
+    return TSR_OK;
+  }
+  if (!variant_exists(d, rg.bn, rg.stages, rg.ctas, gathered)) {
+    int bn = 0, st = 0, ct = 0;
+    if (!variant_pick(d, gathered, rg.bn, 0, 0, &bn, &st, &ct) &&
+        !variant_pick(d, gathered, 0, 0, 0, &bn, &st, &ct))
+      return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(d));
+    *out = Regime{bn, st, ct, rg.id};
+    return TSR_OK;
+  }
+  *out = rg;
+  return TSR_OK;
+}
+
 tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items,
                               int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
                               int32_t* ebegin, int32_t* dbegin, int32_t* hist, void* items,
@@ -431,18 +461,10 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     P->n_logical_total = static_cast<int64_t>(B) * H * N * static_cast<int64_t>(N);
     density = on / (static_cast<double>(H) * N * static_cast<double>(N));
   }
-  Regime rg = regime_lookup(m.kind, m.bq, m.bk, N, density, P->d);
-  if (opts) {
-    if (opts->bn) rg.bn = opts->bn, rg.id = -1;
-    if (opts->stages) rg.stages = opts->stages, rg.id = -1;
-    if (opts->ctas_per_sm) rg.ctas = opts->ctas_per_sm, rg.id = -1;
-  }
-  if (rg.bn != 64 && rg.bn != 128) return fail(TSR_ERR_INVALID_ARG, "bn must be 64 or 128");
-  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas, false))
-    return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) +
-                                         " bn=" + std::to_string(rg.bn) + " stages=" +
-                                         std::to_string(rg.stages) + " ctas=" +
-                                         std::to_string(rg.ctas));
+  Regime rg;
+  if (tsr_status s = resolve_regime(regime_lookup(m.kind, m.bq, m.bk, N, density, P->d), opts,
+                                    P->d, false, &rg))
+    return s;
   P->bn = rg.bn;
   P->stages = rg.stages;
   P->ctas = rg.ctas;

@@ -250,17 +250,10 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   P->n_logical_on = static_cast<int64_t>(host_tot[4]);
   P->n_logical_total = n_lists * static_cast<int64_t>(N);
   const double density = static_cast<double>(host_tot[4]) / static_cast<double>(n_lists) / N;
-  Regime rg = regime_lookup(TSR_MASK_KEYLIST, M, 1, N, density, P->d);
-  if (opts) {
-    if (opts->bn) rg.bn = opts->bn, rg.id = -1;
-    if (opts->stages) rg.stages = opts->stages, rg.id = -1;
-    if (opts->ctas_per_sm) rg.ctas = opts->ctas_per_sm, rg.id = -1;
-  }
-  if (!variant_exists(P->d, rg.bn, rg.stages, rg.ctas, true))
-    return fail(TSR_ERR_UNSUPPORTED, "no gathered kernel variant for d=" + std::to_string(P->d) +
-                                         " bn=" + std::to_string(rg.bn) + " stages=" +
-                                         std::to_string(rg.stages) + " ctas=" +
-                                         std::to_string(rg.ctas));
+  Regime rg;
+  if (tsr_status s = resolve_regime(regime_lookup(TSR_MASK_KEYLIST, M, 1, N, density, P->d), opts,
+                                    P->d, true, &rg))
+    return s;
   P->bn = rg.bn;
   P->stages = rg.stages;
   P->ctas = rg.ctas;
