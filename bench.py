@@ -47,6 +47,19 @@ def allowed_pairs_uniform(spec) -> int:
                          rk.astype(np.int64)))
 
 
+def launches_per_step(spec, stats) -> int:
+    """Kernels of this library launched per step (re-plan + forward)."""
+    import workloads as W
+    if spec.kind == W.MASK_KEYLIST:
+        return 4 + 1                       # validate, count, schedule, emit + attention
+    n = 4 + 1                              # count, logical count, schedule, emit + attention
+    if spec.kind == W.MASK_SVG:
+        n -= 1                             # no logical-grid count
+        if stats["n_temporal_heads"]:
+            n += 3                         # temporal-major copies of Q, K, V
+    return n
+
+
 def read_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -158,11 +171,44 @@ def cpu_baseline(spec, q, k, v, target_s: float = 12.0) -> dict:
                       f"({pairs} allowed pairs, {t:.1f} s)", "seconds": t}
 
 
-def make_workload(heads: int = 24):
+WORKLOADS = {
+    # name: (description, generator)
+    "video480p": (WORKLOAD, lambda W, h: W.video_block_mask(seed=2, H=h)),
+    "svg480p": ("svg480p_spatial_temporal_F21_S1560_H24_d128",
+                lambda W, h: W.svg_mask(1, h, n_frames=21, frame_size=1560)),
+    "keylist720p": ("fg720p_keylist_M64_15pct_N75600_H24_d128",
+                    lambda W, h: W.keylist_mask(seed=4, H=h)),
+}
+
+
+def make_workload(heads: int = 24, name: str = "video480p"):
     import workloads as W
-    spec = W.video_block_mask(seed=2, H=heads)
-    q, k, v = W.qkv(spec.B, spec.H, spec.N, D, seed=2)
+    if name.startswith("sweep"):
+        spec = W.sweep_mask(int(name[5:] or 0), H=heads)
+    else:
+        spec = WORKLOADS[name][1](W, heads)
+    seed = {"video480p": 2, "svg480p": 3, "keylist720p": 4}.get(name, 10)
+    q, k, v = W.qkv(spec.B, spec.H, spec.N, D, seed=seed)
     return spec, q, k, v
+
+
+def allowed_pairs(spec) -> int:
+    """|E| for any mask form (counted from the logical mask, no attention)."""
+    import workloads as W
+    if spec.kind == W.MASK_UNIFORM:
+        return allowed_pairs_uniform(spec)
+    if spec.kind == W.MASK_SVG:
+        S, F, N = spec.frame_size, spec.n_frames, spec.N
+        per = [S * S * (2 * F - 1) if int(k) == W.HEAD_SPATIAL else N * F for k in spec.head_kind]
+        return int(sum(per)) * spec.B
+    if spec.kind == W.MASK_KEYLIST:
+        M, N = spec.slice_m, spec.N
+        lens = np.diff(spec.indptr).reshape(spec.B * spec.H, -1)
+        rows = np.minimum(M, N - np.arange(lens.shape[1]) * M)
+        return int((lens * rows[None, :]).sum())
+    rq = np.diff(spec.q_bounds)
+    rk = np.diff(spec.k_bounds)
+    return int(np.einsum("bhij,i,j->", spec.blocks.astype(np.int64), rq, rk))
 
 
 def run_reference(args, rank: int, world: int) -> None:
@@ -200,6 +246,8 @@ def main():
     ap.add_argument("--bn", type=int, default=0, help="force the K/V tile width (0 = table)")
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--ctas", type=int, default=0)
+    ap.add_argument("--workload", default="video480p",
+                    help="video480p (the benchmark), svg480p, keylist720p, sweepM")
     ap.add_argument("--heads", type=int, default=24,
                     help="heads of the workload (24 = the benchmark; fewer for profiling)")
     args = ap.parse_args()
@@ -226,8 +274,8 @@ def main():
     tsr.build()
     tsr.lib()
 
-    spec, q, k, v = make_workload(args.heads)
-    pairs = allowed_pairs_uniform(spec)
+    spec, q, k, v = make_workload(args.heads, args.workload)
+    pairs = allowed_pairs(spec)
     flops = 4.0 * D * pairs
     dev = torch.device("cuda", local)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -297,11 +345,16 @@ def main():
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
         oh = torch.empty_like(qh).pin_memory()
         lh = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32).pin_memory()
-        blocks = np.ascontiguousarray(spec.blocks)
+        marr = {k2: v2 for k2, v2 in dict(bq=spec.bq, bk=spec.bk, blocks=spec.blocks,
+                                            q_bounds=spec.q_bounds, k_bounds=spec.k_bounds,
+                                            head_kind=spec.head_kind, n_frames=spec.n_frames,
+                                            frame_size=spec.frame_size, slice_m=spec.slice_m,
+                                            indptr=spec.indptr, indices=spec.indices).items()
+                if v2 is not None}
+        mask_bytes = sum(np.asarray(v2).nbytes for v2 in marr.values() if isinstance(v2, np.ndarray))
 
         def host_call():
-            tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, D, qh, kh, vh, oh, lh,
-                                   bq=spec.bq, bk=spec.bk, blocks=blocks)
+            tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, D, qh, kh, vh, oh, lh, **marr)
 
         for _ in range(2):
             host_call()
@@ -311,7 +364,7 @@ def main():
             host_call()
         e2e_s = (time.perf_counter() - t0) / n_e2e
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": 3 * qh.numel() * 2 + blocks.nbytes,
+               "h2d_bytes_per_step": 3 * qh.numel() * 2 + mask_bytes,
                "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
                "ms_per_step": 1e3 * e2e_s}
 
@@ -320,14 +373,16 @@ def main():
         cpu = cpu_baseline(spec, q, k, v)
         cpu.pop("seconds", None)
 
+    wname = WORKLOADS[args.workload][0] if args.workload in WORKLOADS else args.workload
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD if args.heads == 24 else f"{WORKLOAD}_heads{args.heads}",
+            "config": {"workload": wname if args.heads == 24 else f"{wname}_heads{args.heads}",
                        "B": spec.B, "H": spec.H, "N": spec.N, "d": D,
-                       "logical_block": [spec.bq, spec.bk], "allowed_pairs": pairs,
+                       "mask_kind": int(spec.kind), "logical_block": [spec.bq, spec.bk],
+                       "allowed_pairs": pairs,
                        "density": pairs / (spec.B * spec.H * spec.N * spec.N),
                        "step": "tsr_plan_update (re-plan of the mask) + tsr_bsa_forward",
                        "l2": "inputs (603 MB Q/K/V) exceed the 129 MB L2; no flush",
@@ -344,7 +399,7 @@ def main():
                                         f"{'sustained' if long_region else 'burst'}",
                          "kernel": "bsa_fwd_kernel", "kernel_source_hash": khash},
             "clocks": clk.summary(),
-            "gpu_launches": args.steps * 5,
+            "gpu_launches": args.steps * launches_per_step(spec, stats),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
