@@ -189,11 +189,13 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     // Gathered tiles (FG-Attn abstract: only the listed keys of a query block are
     // loaded, packed into dense tiles in shared memory).  The warp copies the
     // listed K or V rows with 16-byte cp.async straight into the 128-byte
-    // swizzled layout the MMA reads; one copy group per tile.  A group is
-    // published (proxy fence, then the tile's full barrier) once the next group
-    // has been issued, so one tile's copies are always in flight.
-    uint32_t pend_bar = 0;
-    bool pending = false;
+    // swizzled layout the MMA reads; one copy group per tile.  Up to four groups
+    // stay in flight; a group is published (proxy fence, then the tile's full
+    // barrier) when a fifth is issued, and all are published before the
+    // producer blocks on anything (a blocked producer must not hold tiles the
+    // MMA issuer is waiting for).
+    uint32_t pq0 = 0, pq1 = 0, pq2 = 0, pq3 = 0;   // pending groups, oldest first
+    int npend = 0;
     auto gather_rows = [&](const __nv_bfloat16* head_base, int32_t kv, uint32_t dst) {
       constexpr int UNITS = D / 8;        // 16-byte units per row
       constexpr int RPI = 32 / UNITS;     // rows per warp instruction
@@ -210,24 +212,44 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       }
       cp_async_commit();
     };
+    auto publish = [&](uint32_t bar) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
     auto retire_push = [&](uint32_t bar) {
-      if (pending) {
-        cp_async_wait_1();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pend_bar);
+      if (npend == 4) {
+        cp_async_wait_3();
+        publish(pq0);
+        pq0 = pq1;
+        pq1 = pq2;
+        pq2 = pq3;
+        --npend;
       }
-      pend_bar = bar;
-      pending = true;
+      if (npend == 0) pq0 = bar;
+      else if (npend == 1) pq1 = bar;
+      else if (npend == 2) pq2 = bar;
+      else pq3 = bar;
+      ++npend;
     };
     auto drain = [&]() {
-      if (pending) {
+      if (npend) {
         cp_async_wait_all();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pend_bar);
-        pending = false;
+        if (lane == 0) {
+          mbar_arrive(pq0);
+          if (npend > 1) mbar_arrive(pq1);
+          if (npend > 2) mbar_arrive(pq2);
+          if (npend > 3) mbar_arrive(pq3);
+        }
+        npend = 0;
       }
+    };
+    // wait for a free stage; publish pending copies first if the wait may block
+    auto wait_free = [&](uint32_t bar, uint32_t parity) -> bool {
+      if (GATHER && npend && !mbar_test_wait(bar, parity)) drain();
+      return mbar_wait(bar, parity, abort_flag, p.err);
     };
     while (ok) {
       int32_t it = 0;
@@ -250,7 +272,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       const CUtensorMap* mk = layout ? &p.tk_p : &p.tk;
       const CUtensorMap* mv = layout ? &p.tv_p : &p.tv;
       const size_t head_off = static_cast<size_t>(bh) * p.N * D;
-      if (!mbar_wait(smem_u32(&ctrl.q_empty), (q_cnt & 1) ^ 1, abort_flag, p.err)) break;
+      if (!wait_free(smem_u32(&ctrl.q_empty), (q_cnt & 1) ^ 1)) break;
       if (lane == 0) {
         const uint32_t bar = smem_u32(&ctrl.q_full);
         mbar_arrive_expect_tx(bar, C::Q_BYTES);
@@ -267,7 +289,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         if (i < n) {
           const uint32_t kvi = kv_cnt + i;
           const int s = kvi % STAGES;
-          if (!mbar_wait(smem_u32(&ctrl.k_empty[s]), ((kvi / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+          if (!wait_free(smem_u32(&ctrl.k_empty[s]), ((kvi / STAGES) & 1) ^ 1)) {
             ok = false;
             break;
           }
@@ -287,7 +309,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         if (i >= 1) {
           const uint32_t kvi = kv_cnt + i - 1;
           const int s = kvi % STAGES;
-          if (!mbar_wait(smem_u32(&ctrl.v_empty[s]), ((kvi / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+          if (!wait_free(smem_u32(&ctrl.v_empty[s]), ((kvi / STAGES) & 1) ^ 1)) {
             ok = false;
             break;
           }

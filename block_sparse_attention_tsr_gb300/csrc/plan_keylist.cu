@@ -212,6 +212,150 @@ __global__ void __launch_bounds__(256) keylist_emit_kernel(
   }
 }
 
+// Bitmap form (N up to kBitmapMaxN): one block per query tile builds the two
+// lists' key bitmaps in shared memory; union ranks are popcount prefixes, so no
+// searching is needed.
+constexpr int32_t kBitmapMaxN = 196608;
+
+__device__ __forceinline__ void set_bits(uint32_t* bm, const int32_t* keys, int64_t n) {
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int32_t k = keys[i];
+    atomicOr(&bm[k >> 5], 1u << (k & 31));
+  }
+}
+
+// Exclusive scan over nw words of popcount(a | b) with one block of 256
+// threads; pre[w] receives the union rank of word w's first key.  Returns the
+// union size.
+__device__ int32_t union_prefix(const uint32_t* a, const uint32_t* b, int32_t* pre, int32_t nw,
+                                int* wsum) {
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int per = (nw + T - 1) / T;
+  const int lo = min(nw, tid * per), hi = min(nw, lo + per);
+  int s = 0;
+  for (int w = lo; w < hi; ++w) s += __popc(a[w] | b[w]);
+  // block exclusive scan of s
+  const int lane = tid & 31, warp = tid >> 5;
+  int x = s;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int i = 0; i < (T >> 5); ++i) {
+    if (i < warp) before += wsum[i];
+    total += wsum[i];
+  }
+  int run = before + x - s;
+  for (int w = lo; w < hi; ++w) {
+    pre[w] = run;
+    run += __popc(a[w] | b[w]);
+  }
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
+    const int64_t* indptr, const int32_t* indices, int64_t n_items, int32_t nqt, int32_t nqb,
+    int32_t slice_m, int32_t N, int32_t* cnt, unsigned long long* tot) {
+  extern __shared__ uint32_t sm[];
+  __shared__ int wsum[8];
+  const int32_t nw = (N + 31) >> 5;
+  uint32_t* bma = sm;
+  uint32_t* bmb = sm + nw;
+  const int64_t item = blockIdx.x;
+  const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
+  for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
+  __syncthreads();
+  set_bits(bma, L.a, L.na);
+  set_bits(bmb, L.b, L.nb);
+  __syncthreads();
+  int s = 0;
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) s += __popc(bma[w] | bmb[w]);
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t u = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) u += wsum[i];
+    const int32_t e64 = static_cast<int32_t>((u + 63) / 64), e128 = static_cast<int32_t>((u + 127) / 128);
+    cnt[item] = e64;
+    cnt[n_items + item] = e128;
+    cnt[2 * n_items + item] = static_cast<int32_t>(u);
+    atomicAdd(&tot[0], static_cast<unsigned long long>(e64));
+    atomicAdd(&tot[1], static_cast<unsigned long long>(e128));
+    atomicMax(&tot[2], static_cast<unsigned long long>(e64));
+    atomicMax(&tot[3], static_cast<unsigned long long>(e128));
+    atomicAdd(&tot[4], static_cast<unsigned long long>(L.na + L.nb));
+  }
+}
+
+__global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
+    const int64_t* indptr, const int32_t* indices, int32_t nqt, int32_t nqb, int32_t slice_m,
+    int32_t N, int32_t bn, const int32_t* cnt_e, const int32_t* ebegin, int2* entries,
+    uint32_t* descs, int32_t* gidx) {
+  extern __shared__ uint32_t sm[];
+  __shared__ int wsum[8];
+  const int32_t nw = (N + 31) >> 5;
+  uint32_t* bma = sm;
+  uint32_t* bmb = sm + nw;
+  int32_t* pre = reinterpret_cast<int32_t*>(sm + 2 * nw);
+  const int64_t item = blockIdx.x;
+  const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
+  const int64_t e0 = ebegin[item];
+  const int32_t ne = cnt_e[item];
+  for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
+  __syncthreads();
+  set_bits(bma, L.a, L.na);
+  set_bits(bmb, L.b, L.nb);
+  __syncthreads();
+  const int32_t u = union_prefix(bma, bmb, pre, nw, wsum);
+  int32_t* gx = gidx + e0 * bn;
+  uint32_t* dw = descs + e0 * 8;
+  const int wpt = bn >> 5;                       // mask words per row segment in use
+  // each group of wpt mask words (bn keys of the union) is written by one thread:
+  // walk union ranks [c*bn, c*bn + bn) through the bitmaps
+  for (int32_t c = threadIdx.x; c < ne; c += blockDim.x) {
+    uint32_t ma[4] = {0u, 0u, 0u, 0u}, mb[4] = {0u, 0u, 0u, 0u};
+    const int32_t r0 = c * bn, r1 = min(u, r0 + bn);
+    // first word whose prefix reaches r0
+    int lo = 0, hi = nw - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    int32_t rank = pre[lo];
+    for (int w = lo; w < nw && rank < r1; ++w) {
+      uint32_t bits = bma[w] | bmb[w];
+      while (bits && rank < r1) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        if (rank >= r0) {
+          const int col = rank - r0;
+          const int32_t key = (w << 5) + bit;
+          gx[rank] = key;
+          if ((bma[w] >> bit) & 1u) ma[col >> 5] |= 1u << (col & 31);
+          if ((bmb[w] >> bit) & 1u) mb[col >> 5] |= 1u << (col & 31);
+        }
+        ++rank;
+      }
+    }
+    for (int32_t q = r1; q < r0 + bn; ++q) gx[q] = 0;   // padding, masked
+    bool full = (r1 - r0 == bn);
+    for (int w = 0; w < wpt; ++w) {
+      full = full && ma[w] == 0xFFFFFFFFu;
+      if (L.b_rows) full = full && mb[w] == 0xFFFFFFFFu;
+    }
+    uint4* d = reinterpret_cast<uint4*>(dw + c * 8);
+    d[0] = make_uint4(ma[0], ma[1], ma[2], ma[3]);
+    d[1] = make_uint4(mb[0], mb[1], mb[2], mb[3]);
+    entries[e0 + c] = make_int2(static_cast<int32_t>((e0 + c) * bn),
+                                full ? -1 : static_cast<int32_t>(e0 + c));
+  }
+}
+
 }  // namespace
 
 tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
@@ -240,9 +384,27 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
     return fail(TSR_ERR_INVALID_ARG,
                 "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward");
-  keylist_count_kernel<<<static_cast<unsigned>((n_items * 32 + threads - 1) / threads), threads, 0,
-                         stream>>>(mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
-  TSR_CUDA(cudaGetLastError());
+  const bool bitmap = N <= kBitmapMaxN;
+  const size_t nw = static_cast<size_t>((N + 31) / 32);
+  if (bitmap) {
+    static bool attr_done[64] = {false};
+    if (P->device < 0 || P->device >= 64 || !attr_done[P->device]) {
+      TSR_CUDA(cudaFuncSetAttribute(keylist_count_bitmap_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * 4 * kBitmapMaxN / 32));
+      TSR_CUDA(cudaFuncSetAttribute(keylist_emit_bitmap_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * 4 * kBitmapMaxN / 32));
+      if (P->device >= 0 && P->device < 64) attr_done[P->device] = true;
+    }
+    if (n_items > 0) {
+      keylist_count_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 2 * 4 * nw, stream>>>(
+          mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
+      TSR_CUDA(cudaGetLastError());
+    }
+  } else {
+    keylist_count_kernel<<<static_cast<unsigned>((n_items * 32 + threads - 1) / threads), threads, 0,
+                           stream>>>(mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
+    TSR_CUDA(cudaGetLastError());
+  }
   TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost,
                            stream));
   TSR_CUDA(cudaStreamSynchronize(stream));
@@ -285,7 +447,12 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
                                         static_cast<int32_t*>(P->b_dbegin.p),
                                         static_cast<int32_t*>(P->b_hist.p), P->items, stream))
     return s;
-  if (n_items > 0) {
+  if (n_items > 0 && bitmap) {
+    keylist_emit_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 3 * 4 * nw, stream>>>(
+        mask->indptr, mask->indices, nqt, nqb, M, N, rg.bn, cnt_e, ebegin,
+        static_cast<int2*>(P->entries), static_cast<uint32_t*>(P->descs), P->gidx);
+    TSR_CUDA(cudaGetLastError());
+  } else if (n_items > 0) {
     keylist_emit_kernel<<<static_cast<unsigned>(n_items), 256, 0, stream>>>(
         mask->indptr, mask->indices, nqt, nqb, M, N, rg.bn, cnt_e, cnt + 2 * n_items, ebegin,
         static_cast<int2*>(P->entries), static_cast<uint32_t*>(P->descs), P->gidx);
