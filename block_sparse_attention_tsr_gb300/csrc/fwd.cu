@@ -189,12 +189,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     // Gathered tiles (FG-Attn abstract: only the listed keys of a query block are
     // loaded, packed into dense tiles in shared memory).  The warp copies the
     // listed K or V rows with 16-byte cp.async straight into the 128-byte
-    // swizzled layout the MMA reads; one copy group per tile.  Up to four groups
-    // stay in flight; a group is published (proxy fence, then the tile's full
-    // barrier) when a fifth is issued, and all are published before the
-    // producer blocks on anything (a blocked producer must not hold tiles the
-    // MMA issuer is waiting for).
-    uint32_t pq0 = 0, pq1 = 0, pq2 = 0, pq3 = 0;   // pending groups, oldest first
+    // swizzled layout the MMA reads; one copy group per tile.  Two groups stay
+    // in flight: issuing a third waits for the oldest and publishes it (proxy
+    // fence, then the tile's full barrier).  Before the producer blocks on
+    // anything it publishes every pending group, oldest first (a blocked
+    // producer must not hold tiles the MMA issuer is waiting for).
+    uint32_t pq0 = 0, pq1 = 0, pq2 = 0;   // pending groups, oldest first
     int npend = 0;
     auto gather_rows = [&](const __nv_bfloat16* head_base, int32_t kv, uint32_t dst) {
       constexpr int UNITS = D / 8;        // 16-byte units per row
@@ -218,31 +218,28 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(bar);
     };
     auto retire_push = [&](uint32_t bar) {
-      if (npend == 4) {
-        cp_async_wait_3();
+      if (npend == 0) pq0 = bar;
+      else if (npend == 1) pq1 = bar;
+      else pq2 = bar;
+      ++npend;
+      if (npend == 3) {
+        cp_async_wait_2();
         publish(pq0);
         pq0 = pq1;
         pq1 = pq2;
-        pq2 = pq3;
-        --npend;
+        npend = 2;
       }
-      if (npend == 0) pq0 = bar;
-      else if (npend == 1) pq1 = bar;
-      else if (npend == 2) pq2 = bar;
-      else pq3 = bar;
-      ++npend;
     };
     auto drain = [&]() {
-      if (npend) {
+      if (npend == 2) {
+        cp_async_wait_1();
+        publish(pq0);
+        pq0 = pq1;
+        npend = 1;
+      }
+      if (npend == 1) {
         cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(pq0);
-          if (npend > 1) mbar_arrive(pq1);
-          if (npend > 2) mbar_arrive(pq2);
-          if (npend > 3) mbar_arrive(pq3);
-        }
+        publish(pq0);
         npend = 0;
       }
     };

@@ -111,8 +111,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __device__ __forceinline__ void cp_async_wait_1() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_3() {
-  asm volatile("cp.async.wait_group 3;" ::: "memory");
+__device__ __forceinline__ void cp_async_wait_2() {
+  asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
