@@ -150,8 +150,9 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     mbar_init(smem_u32(&ctrl.q_full), 1);
     mbar_init(smem_u32(&ctrl.q_empty), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&ctrl.k_full[s]), 1);
-      mbar_init(smem_u32(&ctrl.v_full[s]), 1);
+      // gathered tiles: one completion arrival per producer lane
+      mbar_init(smem_u32(&ctrl.k_full[s]), GATHER ? 32 : 1);
+      mbar_init(smem_u32(&ctrl.v_full[s]), GATHER ? 32 : 1);
       mbar_init(smem_u32(&ctrl.k_empty[s]), 1);
       mbar_init(smem_u32(&ctrl.v_empty[s]), 1);
     }
@@ -189,14 +190,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     // Gathered tiles (FG-Attn abstract: only the listed keys of a query block are
     // loaded, packed into dense tiles in shared memory).  The warp copies the
     // listed K or V rows with 16-byte cp.async straight into the 128-byte
-    // swizzled layout the MMA reads; one copy group per tile.  Two groups stay
-    // in flight: issuing a third waits for the oldest and publishes it (proxy
-    // fence, then the tile's full barrier).  Before the producer blocks on
-    // anything it publishes every pending group, oldest first (a blocked
-    // producer must not hold tiles the MMA issuer is waiting for).
-    uint32_t pq0 = 0, pq1 = 0, pq2 = 0;   // pending groups, oldest first
-    int npend = 0;
-    auto gather_rows = [&](const __nv_bfloat16* head_base, int32_t kv, uint32_t dst) {
+    // swizzled layout the MMA reads.  Each lane then asks for an arrival on the
+    // tile's full barrier when its copies have landed (the barrier expects 32),
+    // so the producer never waits for its own copies; the MMA issuer puts a
+    // proxy fence between that barrier and the MMAs that read the tile.
+    auto gather_rows = [&](const __nv_bfloat16* head_base, int32_t kv, uint32_t dst,
+                           uint32_t bar) {
       constexpr int UNITS = D / 8;        // 16-byte units per row
       constexpr int RPI = 32 / UNITS;     // rows per warp instruction
       int32_t my_idx[BN / 32];
@@ -210,42 +209,9 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         const void* src = reinterpret_cast<const uint8_t*>(head_base + static_cast<size_t>(key) * D) + j * 16;
         cp_async_16(dst + c * BN * 128 + row * 128 + ((u ^ (row & 7)) << 4), src);
       }
-      cp_async_commit();
+      cp_async_arrive_noinc(bar);
     };
-    auto publish = [&](uint32_t bar) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
-    };
-    auto retire_push = [&](uint32_t bar) {
-      if (npend == 0) pq0 = bar;
-      else if (npend == 1) pq1 = bar;
-      else pq2 = bar;
-      ++npend;
-      if (npend == 3) {
-        cp_async_wait_2();
-        publish(pq0);
-        pq0 = pq1;
-        pq1 = pq2;
-        npend = 2;
-      }
-    };
-    auto drain = [&]() {
-      if (npend == 2) {
-        cp_async_wait_1();
-        publish(pq0);
-        pq0 = pq1;
-        npend = 1;
-      }
-      if (npend == 1) {
-        cp_async_wait_all();
-        publish(pq0);
-        npend = 0;
-      }
-    };
-    // wait for a free stage; publish pending copies first if the wait may block
     auto wait_free = [&](uint32_t bar, uint32_t parity) -> bool {
-      if (GATHER && npend && !mbar_test_wait(bar, parity)) drain();
       return mbar_wait(bar, parity, abort_flag, p.err);
     };
     while (ok) {
@@ -293,8 +259,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           const uint32_t kb = smem_u32(&ctrl.k_full[s]);
           const uint32_t sk = sK0 + s * C::KV_BYTES;
           if constexpr (GATHER) {
-            gather_rows(p.kg + head_off, __ldg(&p.entries[begin + i]).x, sk);
-            retire_push(kb);
+            gather_rows(p.kg + head_off, __ldg(&p.entries[begin + i]).x, sk, kb);
           } else if (lane == 0) {
             const int32_t kv = __ldg(&p.entries[begin + i]).x;
             mbar_arrive_expect_tx(kb, C::KV_BYTES);
@@ -313,8 +278,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           const uint32_t vb = smem_u32(&ctrl.v_full[s]);
           const uint32_t sv = sV0 + s * C::KV_BYTES;
           if constexpr (GATHER) {
-            gather_rows(p.vg + head_off, __ldg(&p.entries[begin + i - 1]).x, sv);
-            retire_push(vb);
+            gather_rows(p.vg + head_off, __ldg(&p.entries[begin + i - 1]).x, sv, vb);
           } else if (lane == 0) {
             const int32_t kv = __ldg(&p.entries[begin + i - 1]).x;
             mbar_arrive_expect_tx(vb, C::KV_BYTES);
@@ -325,9 +289,6 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         }
       }
       kv_cnt += n;
-      // the item's last gathered copies are published before the producer can
-      // block on the work-item queue
-      if constexpr (GATHER) drain();
     }
     if constexpr (GATHER) cp_async_wait_all();
     // On an abort, let the copies already issued land before the CTA exits
@@ -363,6 +324,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           const int s = kvi % STAGES;
           if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err)) return false;
           if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err)) return false;
+          if constexpr (GATHER) fence_proxy_async_smem();   // cp.async writes -> tensor core reads
           if (j == 0) {
             if (!mbar_wait(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1, abort_flag, p.err)) return false;
             ++o_cnt;
@@ -386,6 +348,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             ok = false;
             break;
           }
+          if constexpr (GATHER) fence_proxy_async_smem();   // cp.async writes -> tensor core reads
           tc_fence_after();
           const uint32_t sk = sK0 + s * C::KV_BYTES;
 #pragma unroll

@@ -114,6 +114,11 @@ __device__ __forceinline__ void cp_async_wait_1() {
 __device__ __forceinline__ void cp_async_wait_2() {
   asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
+// Arrive (once, without changing the expected count) on an mbarrier when every
+// cp.async this thread issued before it has completed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
