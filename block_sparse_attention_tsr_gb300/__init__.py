@@ -25,11 +25,11 @@ __all__ = [
     "tsr_bsa_forward",
     "tsr_plan_device_status", "tsr_temporal_permute", "tsr_attention_host", "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
-    "PLAN_SYNC_CHECK", "PLAN_NO_LPT",
+    "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL",
 ]
 
 UNIFORM, SEGMENTS, SVG, KEYLIST = 0, 1, 2, 3
-PLAN_SYNC_CHECK, PLAN_NO_LPT = 1, 2
+PLAN_SYNC_CHECK, PLAN_NO_LPT, PLAN_TEST_STALL = 1, 2, 4
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory",
            5: "device wait timed out", 6: "internal error"}
 

@@ -54,6 +54,8 @@ struct FwdParams {
   const __nv_bfloat16* vg;
   const int32_t* gidx;
   int32_t slice_m;
+  int32_t test_stall;           // test only: the MMA issuer waits on a barrier nobody signals
+  uint64_t timeout_ns;          // bound of every wait
 };
 
 // Rescale the running output only when the running maximum grew by more than
@@ -68,7 +70,7 @@ struct alignas(8) Ctrl {
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_full, o_empty;
   uint64_t item_full[2], item_empty[2];
-  uint64_t final_bar;
+  uint64_t final_bar, never;
   int32_t item_slot[2];
   uint32_t tmem_base;
   int32_t abort_flag;
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     mbar_init(smem_u32(&ctrl.o_full), 1);
     mbar_init(smem_u32(&ctrl.o_empty), 4);
     mbar_init(smem_u32(&ctrl.final_bar), 1);
+    mbar_init(smem_u32(&ctrl.never), 1);
     ctrl.abort_flag = 0;
     fence_mbar_init();
   }
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       cp_async_arrive_noinc(bar);
     };
     auto wait_free = [&](uint32_t bar, uint32_t parity) -> bool {
-      return mbar_wait(bar, parity, abort_flag, p.err);
+      return mbar_wait(bar, parity, abort_flag, p.err, p.timeout_ns);
     };
     while (ok) {
       int32_t it = 0;
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
       const bool done = it >= p.n_items;
       const int slot = item_seq & 1;
-      if (!mbar_wait(smem_u32(&ctrl.item_empty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+      if (!mbar_wait(smem_u32(&ctrl.item_empty[slot]), ((item_seq >> 1) & 1) ^ 1, abort_flag, p.err, p.timeout_ns)) break;
       if (lane == 0) {
         ctrl.item_slot[slot] = done ? -1 : it;
         mbar_arrive(smem_u32(&ctrl.item_full[slot]));
@@ -305,9 +308,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     if (lane == 0) {
       uint32_t item_seq = 0, kv_cnt = 0, t_cnt = 0, q_cnt = 0, o_cnt = 0;
       bool ok = true;
+      // Failure-path test: wait on a barrier that is never signalled, so the
+      // bounded wait expires, the CTA aborts and the error word reports it.
+      if (p.test_stall) ok = mbar_wait(smem_u32(&ctrl.never), 0, abort_flag, p.err, p.timeout_ns);
       while (ok) {
         const int slot = item_seq & 1;
-        if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err, p.timeout_ns)) break;
         const int32_t it = ctrl.item_slot[slot];
         mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
         ++item_seq;
@@ -315,18 +321,18 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         const int4 i0 = __ldg(&p.items[2 * it]);
         const int32_t n = i0.w - i0.z;
         if (n <= 0) continue;
-        if (!mbar_wait(smem_u32(&ctrl.q_full), q_cnt & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(smem_u32(&ctrl.q_full), q_cnt & 1, abort_flag, p.err, p.timeout_ns)) break;
         ++q_cnt;
         tc_fence_after();
         // O += P V for tile j of this item
         auto issue_pv = [&](int32_t j) -> bool {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
-          if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err)) return false;
-          if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err)) return false;
+          if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+          if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) return false;
           if constexpr (GATHER) fence_proxy_async_smem();   // cp.async writes -> tensor core reads
           if (j == 0) {
-            if (!mbar_wait(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1, abort_flag, p.err)) return false;
+            if (!mbar_wait(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1, abort_flag, p.err, p.timeout_ns)) return false;
             ++o_cnt;
           }
           tc_fence_after();
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         for (int32_t j = 0; j < n && ok; ++j) {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
-          if (!mbar_wait(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1, abort_flag, p.err)) {
+          if (!mbar_wait(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     bool ok = true;
     while (ok) {
       const int slot = item_seq & 1;
-      if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err, p.timeout_ns)) break;
       const int32_t it = ctrl.item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             dn1 = __ldg(&p.descs[2 * desc_next + 1]);
           }
         }
-        if (!mbar_wait(smem_u32(&ctrl.s_full[sb]), (t >> 1) & 1, abort_flag, p.err)) {
+        if (!mbar_wait(smem_u32(&ctrl.s_full[sb]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         // Rows that had no finite maximum before hold O = 0 and need nothing.
         const bool fix_o = fix && j > 0;
         if (__any_sync(0xFFFFFFFFu, fix_o)) {
-          if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err)) {
+          if (!mbar_wait(smem_u32(&ctrl.pv_done), (t - 1) & 1, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -582,7 +588,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       if (n > 0) {
         // o_full completes once per non-empty item, after its last PV; the next
         // item's first PV waits for o_empty, so the phases cannot run ahead.
-        if (!mbar_wait(smem_u32(&ctrl.o_full), o_seq & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(smem_u32(&ctrl.o_full), o_seq & 1, abort_flag, p.err, p.timeout_ns)) break;
         ++o_seq;
         tc_fence_after();
 #pragma unroll
@@ -746,6 +752,8 @@ tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
   prm.vg = static_cast<const __nv_bfloat16*>(a.v);
   prm.gidx = P->gidx;
   prm.slice_m = P->slice_m;
+  prm.test_stall = (P->flags & TSR_PLAN_TEST_STALL) ? 1 : 0;
+  prm.timeout_ns = prm.test_stall ? 100000000ull : kWaitTimeoutNs;
   TSR_CUDA(cudaMemsetAsync(P->counter, 0, sizeof(int32_t), stream));
   const int n = static_cast<int>(P->n_items), dev = P->device;
   const int key = vkey(P->d, P->bn, P->stages, P->ctas, P->gathered ? 1 : 0);

@@ -69,13 +69,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // is aborting (flag already set by another thread) or the wait timed out (then
 // this thread sets the flag and the error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err) {
+                                          uint32_t* err, uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       atomicOr(err, DEV_ERR_TIMEOUT);
       return false;

@@ -132,6 +132,11 @@ typedef struct {
 #define TSR_PLAN_SYNC_CHECK 1  /* tsr_bsa_forward synchronises and reads the device
                                   error word (slower; for debugging)               */
 #define TSR_PLAN_NO_LPT     2  /* keep work items in (b, h, q-tile) order          */
+#define TSR_PLAN_TEST_STALL 4  /* TEST ONLY: the attention kernel waits on a barrier
+                                  that is never signalled, so its bounded-wait path
+                                  runs: after 0.1 s it gives up, frees its resources
+                                  and tsr_plan_device_status() returns
+                                  TSR_ERR_TIMEOUT; the context stays usable      */
 
 typedef struct tsr_plan_s *tsr_plan_t;   /* opaque, library-owned */
 

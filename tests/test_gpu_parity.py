@@ -343,3 +343,22 @@ def test_host_entry_point_keylist():
                            indices=spec.indices)
     assert np.array_equal(out.float().numpy(), O)
     assert np.array_equal(lse.double().numpy(), L)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a GPU fault: with the test-only stall flag the
+    MMA issuer waits on a barrier nothing signals; the kernel gives up after its
+    bound, reports TSR_ERR_TIMEOUT through the error word, and the next normal
+    call on the same context is correct."""
+    spec = W.tiny_block_mask(seed=12)
+    q, k, v = W.qkv(1, 2, 1024, 64, 12)
+    mask = tsr.make_mask(spec.kind, 1, 2, 1024, 64, **W.mask_tensors(spec))
+    plan = tsr.tsr_plan(mask, {"flags": tsr.PLAN_TEST_STALL})
+    tsr.tsr_bsa_forward(q.cuda(), k.cuda(), v.cuda(), plan)
+    with pytest.raises(tsr.TsrError) as e:
+        tsr.tsr_plan_device_status(plan)
+    assert e.value.status == 5
+    tsr.tsr_plan_device_status(plan)                 # the error word was cleared
+    (q, k, v), plan2, O, L = run(spec, 64, seed=0, qkv=(q, k, v))
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, "after timeout")
