@@ -62,6 +62,8 @@ struct FwdParams {
 // this many powers of two: P = 2^(x - m_ref) then stays below 2^8, far inside
 // bf16 and fp32 range, and O / l is unchanged because O and l share the factor.
 constexpr float kRescaleThreshold = 8.0f;
+// How many tiles ahead of the K stream the producer prefetches K and V into L2.
+constexpr int kPrefetchAhead = 4;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct alignas(8) Ctrl {
@@ -247,6 +249,17 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           tma_load_3d(sQ + c * C::BM * 128, mq, bar, c * 64, q_tile * C::BM, bh);
       }
       ++q_cnt;
+      if (!GATHER && lane == 0) {
+        const int32_t np = min(end - begin, kPrefetchAhead);
+        for (int32_t i = 0; i < np; ++i) {
+          const int32_t kvp = __ldg(&p.entries[begin + i]).x;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_l2_3d(mk, c * 64, kvp, bh);
+            tma_prefetch_l2_3d(mv, c * 64, kvp, bh);
+          }
+        }
+      }
       // K runs one tile ahead of V: K of tile i is needed by QK(i), which the
       // MMA issuer runs before PV(i-1); a K stage is released by its QK, a V
       // stage by its PV, so the K stream never waits behind a PV.
@@ -268,6 +281,16 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             mbar_arrive_expect_tx(kb, C::KV_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tma_load_3d(sk + c * BN * 128, mk, kb, c * 64, kv, bh);
+            // L2 prefetch of the K and V tiles kPrefetchAhead tiles later, so the
+            // loads the ring can issue only late (its stages are few) hit in L2
+            if (i + kPrefetchAhead < n) {
+              const int32_t kvp = __ldg(&p.entries[begin + i + kPrefetchAhead]).x;
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c) {
+                tma_prefetch_l2_3d(mk, c * 64, kvp, bh);
+                tma_prefetch_l2_3d(mv, c * 64, kvp, bh);
+              }
+            }
           }
           ++k_iss;
         }

@@ -89,8 +89,9 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
                               cudaStream_t stream);
 tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items,
                               int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
-                              int32_t* ebegin, int32_t* dbegin, int32_t* hist, void* items,
-                              cudaStream_t stream);
+                              int32_t group_heads, int32_t* ebegin, int32_t* dbegin,
+                              int32_t* hist, void* items, cudaStream_t stream);
+int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads);
 tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
                            uint32_t* err, int64_t n_grid, cudaStream_t stream);
 tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int32_t* cnt_e,

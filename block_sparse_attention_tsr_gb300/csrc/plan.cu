@@ -215,40 +215,44 @@ __device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int64_t n,
   __syncthreads();
 }
 
-// One block: tile offsets, descriptor offsets and the work items in
-// longest-first order (counting sort on the tile count).
+// One block: tile offsets, descriptor offsets and the work items.  With lpt the
+// items are ordered by head group (group_heads consecutive (b, h) per group,
+// sized so a group's K and V stay in L2), and longest first inside a group
+// (counting sort over n_groups x (max_len + 1) buckets).
 __global__ void __launch_bounds__(1024) plan_schedule_kernel(
     const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items, int32_t nqt, int32_t H,
-    const int8_t* head_kind, int32_t is_svg, int32_t max_len, int32_t lpt, int32_t* ebegin,
-    int32_t* dbegin, int32_t* hist, int4* items) {
+    const int8_t* head_kind, int32_t is_svg, int32_t max_len, int32_t lpt, int32_t group_heads,
+    int64_t n_buckets, int32_t* ebegin, int32_t* dbegin, int32_t* hist, int4* items) {
   __shared__ int64_t sh[1024];
   block_exclusive_scan(cnt_e, ebegin, n_items, sh);
   block_exclusive_scan(cnt_b, dbegin, n_items, sh);
   const int T = blockDim.x, tid = threadIdx.x;
+  const int64_t per_group = static_cast<int64_t>(group_heads) * nqt;
   if (lpt) {
-    for (int i = tid; i <= max_len; i += T) hist[i] = 0;
+    for (int64_t i = tid; i < n_buckets; i += T) hist[i] = 0;
     __syncthreads();
-    for (int64_t i = tid; i < n_items; i += T) atomicAdd(&hist[cnt_e[i]], 1);
+    for (int64_t i = tid; i < n_items; i += T)
+      atomicAdd(&hist[(i / per_group) * (max_len + 1) + (max_len - cnt_e[i])], 1);
     __syncthreads();
-    // positions in descending length order: pos[L] = sum of hist[L'] for L' > L
-    if (tid == 0) {
-      int32_t run = 0;
-      for (int L = max_len; L >= 0; --L) {
-        const int32_t c = hist[L];
-        hist[L] = run;
-        run += c;
-      }
-    }
-    __syncthreads();
+    block_exclusive_scan(hist, hist, n_buckets, sh);   // in place: bucket start positions
   }
   for (int64_t i = tid; i < n_items; i += T) {
     const int32_t len = cnt_e[i];
-    const int64_t pos = lpt ? atomicAdd(&hist[len], 1) : i;
+    const int64_t pos =
+        lpt ? atomicAdd(&hist[(i / per_group) * (max_len + 1) + (max_len - len)], 1) : i;
     const int32_t bh = static_cast<int32_t>(i / nqt), qt = static_cast<int32_t>(i % nqt);
     const int32_t layout = (is_svg && head_kind[bh % H] == TSR_HEAD_TEMPORAL) ? 1 : 0;
     items[2 * pos] = make_int4(bh, qt, ebegin[i], ebegin[i] + len);
     items[2 * pos + 1] = make_int4(layout, 0, 0, 0);
   }
+}
+
+// Heads per scheduling group: as many (b, h) as keep their K and V (2 x N x d
+// bf16 each) within ~96 MB of the 126 MB L2.
+int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
+  const double per_head = 2.0 * N * d * 2.0;
+  const int64_t g = static_cast<int64_t>(96.0e6 / per_head);
+  return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(g, n_heads)));
 }
 
 __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32_t* ebegin,
@@ -311,9 +315,11 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
   const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
   const int threads = 256;
   const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  const int32_t all_heads = static_cast<int32_t>(n_items / nqt);
   plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, m.H, m.head_kind,
-                                               m.kind == TSR_MASK_SVG ? 1 : 0, max_len, 1, ebegin,
-                                               dbegin, hist, static_cast<int4*>(items));
+                                               m.kind == TSR_MASK_SVG ? 1 : 0, max_len, 1,
+                                               all_heads, max_len + 1, ebegin, dbegin, hist,
+                                               static_cast<int4*>(items));
   TSR_CUDA(cudaGetLastError());
   plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
       m, nqt, bn, ebegin, dbegin, static_cast<int2*>(entries), static_cast<tsr_tile_desc*>(descs));
@@ -375,11 +381,12 @@ tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gath
 
 tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items,
                               int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
-                              int32_t* ebegin, int32_t* dbegin, int32_t* hist, void* items,
-                              cudaStream_t stream) {
+                              int32_t group_heads, int32_t* ebegin, int32_t* dbegin,
+                              int32_t* hist, void* items, cudaStream_t stream) {
+  const int64_t n_groups = (n_items / nqt + group_heads - 1) / group_heads;
   plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, H, nullptr, 0, max_len,
-                                               lpt, ebegin, dbegin, hist,
-                                               static_cast<int4*>(items));
+                                               lpt, group_heads, n_groups * (max_len + 1), ebegin,
+                                               dbegin, hist, static_cast<int4*>(items));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;
 }
@@ -481,7 +488,10 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   if (tsr_status s = devbuf_reserve(P->b_descs, sizeof(tsr_tile_desc) * P->n_desc)) return s;
   if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
-  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  const int32_t group_heads = heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
+  const int64_t n_buckets = n_groups * (P->max_item_len + 1);
+  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_buckets + 1))) return s;
   P->items = P->b_items.p;
   P->entries = P->b_entries.p;
   P->descs = P->b_descs.p;
@@ -493,7 +503,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
   plan_schedule_kernel<<<1, 1024, 0, stream>>>(
       cnt_e, cnt_b, n_items, nqt, H, P->head_kind_dev, m.kind == TSR_MASK_SVG ? 1 : 0,
-      static_cast<int32_t>(P->max_item_len), lpt, ebegin, dbegin, hist,
+      static_cast<int32_t>(P->max_item_len), lpt, group_heads, n_buckets, ebegin, dbegin, hist,
       static_cast<int4*>(P->items));
   TSR_CUDA(cudaGetLastError());
   plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(

@@ -434,7 +434,10 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
   if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
-  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (P->max_item_len + 2))) return s;
+  const int32_t group_heads = heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
+  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_groups * (P->max_item_len + 1) + 1)))
+    return s;
   P->items = P->b_items.p;
   P->entries = P->b_entries.p;
   P->descs = P->b_descs.p;
@@ -443,7 +446,7 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   const int32_t* cnt_e = cnt + which * n_items;
   const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
   if (tsr_status s = plan_schedule_into(cnt_e, cnt_e, n_items, nqt, H, lpt,
-                                        static_cast<int32_t>(P->max_item_len), ebegin,
+                                        static_cast<int32_t>(P->max_item_len), group_heads, ebegin,
                                         static_cast<int32_t*>(P->b_dbegin.p),
                                         static_cast<int32_t*>(P->b_hist.p), P->items, stream))
     return s;
