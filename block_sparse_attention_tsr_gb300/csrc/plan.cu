@@ -247,14 +247,6 @@ __global__ void __launch_bounds__(1024) plan_schedule_kernel(
   }
 }
 
-// Heads per scheduling group: as many (b, h) as keep their K and V (2 x N x d
-// bf16 each) within ~96 MB of the 126 MB L2.
-int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
-  const double per_head = 2.0 * N * d * 2.0;
-  const int64_t g = static_cast<int64_t>(96.0e6 / per_head);
-  return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(g, n_heads)));
-}
-
 __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32_t* ebegin,
                                  const int32_t* dbegin, int2* entries, tsr_tile_desc* descs) {
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -347,6 +339,14 @@ void devbuf_free(DevBuf& b) {
   cudaFree(b.p);
   b.p = nullptr;
   b.cap = 0;
+}
+
+// Heads per scheduling group: as many (b, h) as keep their K and V (2 x N x d
+// bf16 each) within ~96 MB of the 126 MB L2.
+int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
+  const double per_head = 2.0 * N * d * 2.0;
+  const int64_t g = static_cast<int64_t>(96.0e6 / per_head);
+  return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(g, n_heads)));
 }
 
 tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gathered,
