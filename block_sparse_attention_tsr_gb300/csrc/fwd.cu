@@ -328,42 +328,34 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs the issue loop (so descriptors and counters stay
-    // warp-uniform); lane 0 alone issues the MMAs and their commits.
-    const bool leader = (lane == 0);
-    auto wait_u = [&](uint32_t bar, uint32_t parity) -> bool {
-      const bool r = mbar_wait(bar, parity, abort_flag, p.err, p.timeout_ns);
-      return __shfl_sync(0xFFFFFFFFu, r ? 1 : 0, 0) != 0;
-    };
-    {
+    if (lane == 0) {
       uint32_t item_seq = 0, kv_cnt = 0, t_cnt = 0, q_cnt = 0, o_cnt = 0;
       bool ok = true;
       // Failure-path test: wait on a barrier that is never signalled, so the
       // bounded wait expires, the CTA aborts and the error word reports it.
-      if (p.test_stall) ok = wait_u(smem_u32(&ctrl.never), 0);
+      if (p.test_stall) ok = mbar_wait(smem_u32(&ctrl.never), 0, abort_flag, p.err, p.timeout_ns);
       while (ok) {
         const int slot = item_seq & 1;
-        if (!wait_u(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1)) break;
+        if (!mbar_wait(smem_u32(&ctrl.item_full[slot]), (item_seq >> 1) & 1, abort_flag, p.err, p.timeout_ns)) break;
         const int32_t it = ctrl.item_slot[slot];
-        __syncwarp();
-        if (leader) mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
+        mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
         ++item_seq;
         if (it < 0) break;
         const int4 i0 = __ldg(&p.items[2 * it]);
         const int32_t n = i0.w - i0.z;
         if (n <= 0) continue;
-        if (!wait_u(smem_u32(&ctrl.q_full), q_cnt & 1)) break;
+        if (!mbar_wait(smem_u32(&ctrl.q_full), q_cnt & 1, abort_flag, p.err, p.timeout_ns)) break;
         ++q_cnt;
         tc_fence_after();
         // O += P V for tile j of this item
         auto issue_pv = [&](int32_t j) -> bool {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
-          if (!wait_u(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1)) return false;
-          if (!wait_u(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1)) return false;
+          if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+          if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) return false;
           if constexpr (GATHER) fence_proxy_async_smem();   // cp.async writes -> tensor core reads
           if (j == 0) {
-            if (!wait_u(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1)) return false;
+            if (!mbar_wait(smem_u32(&ctrl.o_empty), (o_cnt & 1) ^ 1, abort_flag, p.err, p.timeout_ns)) return false;
             ++o_cnt;
           }
           tc_fence_after();
@@ -371,21 +363,17 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t bdesc = sdesc_sw128(sv + kk * 16 * 128, BN * 128, 1024);
-            if (leader)
-              mma_bf16_ts(tmem + C::O_COL, tmem + (t & 1) * BN + kk * 8, bdesc, C::IDESC_PV,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + C::O_COL, tmem + (t & 1) * BN + kk * 8, bdesc, C::IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
           }
-          if (leader) {
-            mma_commit(smem_u32(&ctrl.v_empty[s]));
-            mma_commit(smem_u32(&ctrl.pv_done));
-          }
-          __syncwarp();
+          mma_commit(smem_u32(&ctrl.v_empty[s]));
+          mma_commit(smem_u32(&ctrl.pv_done));
           return true;
         };
         for (int32_t j = 0; j < n && ok; ++j) {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
-          if (!wait_u(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1)) {
+          if (!mbar_wait(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -396,27 +384,21 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t adesc = sdesc_sw128(sQ + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024);
             const uint64_t bdesc = sdesc_sw128(sk + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
-            if (leader)
-              mma_bf16_ss(tmem + (t & 1) * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + (t & 1) * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
           }
-          if (leader) {
-            mma_commit(smem_u32(&ctrl.s_full[t & 1]));
-            mma_commit(smem_u32(&ctrl.k_empty[s]));
-            if (j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
-          }
-          __syncwarp();
+          mma_commit(smem_u32(&ctrl.s_full[t & 1]));
+          mma_commit(smem_u32(&ctrl.k_empty[s]));
+          if (j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
           if (j > 0 && !issue_pv(j - 1)) ok = false;
         }
         if (ok && !issue_pv(n - 1)) ok = false;
         // the item's output accumulator is complete once its last PV finishes
-        if (ok && leader) mma_commit(smem_u32(&ctrl.o_full));
-        __syncwarp();
+        if (ok) mma_commit(smem_u32(&ctrl.o_full));
         t_cnt += n;
         kv_cnt += n;
       }
       // every MMA issued has finished before TMEM is released
-      if (leader) mma_commit(smem_u32(&ctrl.final_bar));
-      __syncwarp();
+      mma_commit(smem_u32(&ctrl.final_bar));
       volatile int32_t dummy = 0;
       mbar_wait(smem_u32(&ctrl.final_bar), 0, &dummy, p.err);
     }
