@@ -163,8 +163,13 @@ def cpu_baseline(spec, q, k, v, target_s: float = 12.0) -> dict:
         _, _, cnt = oracle.attention_rows(spec, q, k, v, rows, nthreads)
         return time.perf_counter() - t0, int(cnt.sum())
 
-    t, _ = timed(64)
-    n = int(min(spec.B * spec.H * spec.N, max(64, 64 * target_s / max(t, 1e-3))))
+    # calibrate on a sample large enough that thread start-up does not dominate
+    n = 512
+    t, _ = timed(n)
+    while t < 0.5 and n < spec.B * spec.H * spec.N // 4:
+        n *= 4
+        t, _ = timed(n)
+    n = int(min(spec.B * spec.H * spec.N, max(n, n * target_s / max(t, 1e-3))))
     t, pairs = timed(n)
     return {"value": 4.0 * D * pairs / t / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{n} random whole query rows of the {WORKLOAD} workload "
