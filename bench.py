@@ -72,7 +72,7 @@ def read_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fwd.cu", "ptx.cuh"):
+    for f in ("fwd_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

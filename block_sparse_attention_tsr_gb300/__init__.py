@@ -221,6 +221,9 @@ class Plan:
 def _opts(opts) -> Optional[_Opts]:
     if opts is None:
         return None
+    unknown = set(opts) - {"bn", "stages", "ctas_per_sm", "flags"}
+    if unknown:
+        raise ValueError(f"unknown plan option(s): {sorted(unknown)}")
     o = _Opts()
     o.bn = int(opts.get("bn", 0))
     o.stages = int(opts.get("stages", 0))

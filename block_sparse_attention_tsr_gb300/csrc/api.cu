@@ -227,7 +227,6 @@ void free_plan(tsr_plan_s* P) {
   cudaFree(P->counter);
   cudaFree(P->err);
   cudaFree(P->head_kind_dev);
-  cudaFree(P->scratch);
   if (P->host_tot) cudaFreeHost(P->host_tot);
   delete P;
 }
@@ -263,15 +262,6 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
     if (tsr_status s = plan_build_keylist(mask, P->has_opts ? &P->opts : nullptr, P, st)) return s;
   } else if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) {
     return s;
-  }
-  if (P->n_temporal > 0 && !P->scratch) {
-    P->scratch_bytes = static_cast<size_t>(P->B) * P->H * P->N * P->d * 2;
-    const cudaError_t e = cudaMalloc(&P->scratch, 3 * P->scratch_bytes);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      P->scratch = nullptr;
-      return fail(TSR_ERR_OOM, "temporal-major scratch allocation failed");
-    }
   }
   return TSR_OK;
 }
@@ -411,26 +401,9 @@ tsr_status tsr_bsa_forward(const void* q, const void* k, const void* v, tsr_plan
   a.q = q;
   a.k = k;
   a.v = v;
-  a.qs = a.ks = a.vs = nullptr;
   a.out = out;
   a.lse = lse;
   a.plan = plan;
-  if (plan->n_temporal > 0) {
-    uint8_t* s = static_cast<uint8_t*>(plan->scratch);
-    a.qs = s;
-    a.ks = s + plan->scratch_bytes;
-    a.vs = s + 2 * plan->scratch_bytes;
-    const int32_t rb = plan->d * 2;
-    const int8_t* hk = plan->head_layout.data();
-    if (tsr_status e = launch_permute(q, s, plan->B, plan->H, plan->F, plan->S, rb, hk, 0, st))
-      return e;
-    if (tsr_status e = launch_permute(k, s + plan->scratch_bytes, plan->B, plan->H, plan->F,
-                                      plan->S, rb, hk, 0, st))
-      return e;
-    if (tsr_status e = launch_permute(v, s + 2 * plan->scratch_bytes, plan->B, plan->H, plan->F,
-                                      plan->S, rb, hk, 0, st))
-      return e;
-  }
   if (tsr_status e = launch_forward(a, st)) return e;
   if (plan->flags & TSR_PLAN_SYNC_CHECK) return tsr_plan_device_status(plan, stream);
   return TSR_OK;

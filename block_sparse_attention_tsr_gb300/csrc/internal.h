@@ -68,8 +68,6 @@ struct tsr_plan_impl {
   int32_t* counter = nullptr;
   uint32_t* err = nullptr;
   int8_t* head_kind_dev = nullptr;
-  void* scratch = nullptr;   // temporal-major Q, K, V copies: 3 x [B][H][N][d] bf16
-  size_t scratch_bytes = 0;
   // storage reused when the plan is rebuilt for a new mask (tsr_plan_update)
   DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist, b_gidx;
   unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
@@ -104,9 +102,6 @@ struct FwdArgs {
   const void* q;
   const void* k;
   const void* v;
-  const void* qs;   // temporal-major scratch copies (or null)
-  const void* ks;
-  const void* vs;
   void* out;
   float* lse;
   const tsr_plan_impl* plan;

@@ -214,7 +214,6 @@ extern "C" tsr_status tsr_attention_noalloc(const tsr_mask* mask, const void* q,
   a.q = q;
   a.k = k;
   a.v = v;
-  a.qs = a.ks = a.vs = nullptr;
   a.out = out;
   a.lse = lse;
   a.plan = &P;

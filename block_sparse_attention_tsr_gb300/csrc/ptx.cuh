@@ -114,6 +114,12 @@ __device__ __forceinline__ void cp_async_wait_1() {
 __device__ __forceinline__ void cp_async_wait_2() {
   asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
+// Make the current phase of an mbarrier also wait for every cp.async this thread
+// issued before it: the pending count goes up by one now and comes back down when
+// those copies have completed, so the phase still needs its ordinary arrivals.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 // Arrive (once, without changing the expected count) on an mbarrier when every
 // cp.async this thread issued before it has completed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
