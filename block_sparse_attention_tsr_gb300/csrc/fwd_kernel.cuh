@@ -75,8 +75,6 @@ struct FwdParams {
 // this many powers of two: P = 2^(x - m_ref) then stays below 2^8, far inside
 // bf16 and fp32 range, and O / l is unchanged because O and l share the factor.
 constexpr float kRescaleThreshold = 8.0f;
-// How many tiles ahead of the K stream the producer prefetches K and V into L2.
-constexpr int kPrefetchAhead = 4;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct alignas(8) Ctrl {
@@ -91,14 +89,27 @@ struct alignas(8) Ctrl {
   int32_t abort_flag;
 };
 
-template <int D, int BN, int STAGES>
+template <int D, int BN, int STAGES, int CTAS>
 struct Cfg {
   static constexpr int BM = kBM;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int SMEM = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;
-  static constexpr int TMEM_COLS = (2 * BN + D <= 256) ? 256 : 512;
+  // TMEM per CTA (512 columns per SM shared by CTAS CTAs) holds two BN-column S
+  // buffers (P is written over S as bf16), O (D columns) and, where the rest
+  // leaves room, the query tile (D / 2 columns of bf16 pairs).  With Q in TMEM
+  // the S = Q K^T MMAs read A from TMEM and shared memory feeds the tensor core
+  // only K and V (measured: +6 to +9 % on one-CTA variants).  Two-CTA variants
+  // at d = 128 have no room for it; giving up the second S buffer to make room
+  // was measured 25 % slower, because QK of tile j+1 then waits for the softmax
+  // of tile j.
+  static constexpr int BUDGET = 512 / CTAS;
+  static constexpr bool Q_TMEM = 2 * BN + D + D / 2 <= BUDGET;
   static constexpr int O_COL = 2 * BN;
+  static constexpr int Q_COL = O_COL + D;
+  static constexpr int COLS = O_COL + D + (Q_TMEM ? D / 2 : 0);
+  static constexpr int TMEM_COLS = COLS <= 128 ? 128 : COLS <= 256 ? 256 : 512;
+  static_assert(TMEM_COLS * CTAS <= 512, "TMEM");
   static constexpr uint32_t IDESC_QK = idesc_bf16(128, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
   static_assert(STAGES >= 2 && STAGES <= 8, "stages");
@@ -184,7 +195,7 @@ __device__ __forceinline__ void gather_tile(const __nv_bfloat16* head_base,
 
 template <int D, int BN, int STAGES, int CTAS, int MODE>
 __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = Cfg<D, BN, STAGES>;
+  using C = Cfg<D, BN, STAGES, CTAS>;
   constexpr bool GATHER = MODE == kModeList;   // K / V rows named by a key list
   constexpr bool PERM = MODE == kModePerm;     // items may be temporal-major
   extern __shared__ uint8_t smem_raw[];
@@ -286,17 +297,6 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         tma_tile(&p.tq, sQ, smem_u32(&ctrl.q_full), q_tile * C::BM, C::BM, C::Q_BYTES, bh);
       }
       ++q_cnt;
-      if (!GATHER && !perm && lane == 0) {
-        const int32_t np = min(end - begin, kPrefetchAhead);
-        for (int32_t i = 0; i < np; ++i) {
-          const int32_t kvp = __ldg(&p.entries[begin + i]).x;
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_prefetch_l2_3d(&p.tk, c * 64, kvp, bh);
-            tma_prefetch_l2_3d(&p.tv, c * 64, kvp, bh);
-          }
-        }
-      }
       // one K or V tile of entry e into stage buffer dst
       auto load_kv = [&](const CUtensorMap* map, const __nv_bfloat16* base, int32_t e, uint32_t dst,
                          uint32_t bar) {
@@ -324,16 +324,6 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             break;
           }
           load_kv(&p.tk, p.kg, begin + i, sK0 + s * C::KV_BYTES, smem_u32(&ctrl.k_full[s]));
-          // L2 prefetch of the K and V tiles kPrefetchAhead tiles later, so the
-          // loads the ring can issue only late (its stages are few) hit in L2
-          if (!GATHER && !perm && lane == 0 && i + kPrefetchAhead < n) {
-            const int32_t kvp = __ldg(&p.entries[begin + i + kPrefetchAhead]).x;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_l2_3d(&p.tk, c * 64, kvp, bh);
-              tma_prefetch_l2_3d(&p.tv, c * 64, kvp, bh);
-            }
-          }
           ++k_iss;
         }
         if (i >= 1) {
@@ -384,11 +374,24 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         ++q_cnt;
         if (gathered) fence_proxy_async_smem();
         tc_fence_after();
+        if constexpr (C::Q_TMEM) {
+          // Q (shared, swizzled K-major) -> TMEM, 16 columns of K per copy: lane r
+          // holds row r, as the A operand of S = Q K^T expects.  The previous
+          // item's QK MMAs have completed (its softmax consumed their S before
+          // its last PV was issued), and the copies run ahead of this item's MMAs
+          // in issue order.  The shared-memory tile is free once they land.
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tmem_cp_128x256b(tmem + C::Q_COL + kk * 8,
+                             sdesc_sw128(sQ + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024));
+          mma_commit(smem_u32(&ctrl.q_empty));
+        }
         // O += P V for tile j of this item
         auto issue_pv = [&](int32_t j) -> bool {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
-          if (!mbar_wait(smem_u32(&ctrl.p_full[t & 1]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) return false;
+          const uint32_t sb = t & 1;
+          if (!mbar_wait(smem_u32(&ctrl.p_full[sb]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) return false;
           if (!mbar_wait(smem_u32(&ctrl.v_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) return false;
           if (gathered) fence_proxy_async_smem();
           if (j == 0) {
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t bdesc = sdesc_sw128(sv + kk * 16 * 128, BN * 128, 1024);
-            mma_bf16_ts(tmem + C::O_COL, tmem + (t & 1) * BN + kk * 8, bdesc, C::IDESC_PV,
+            mma_bf16_ts(tmem + C::O_COL, tmem + sb * BN + kk * 8, bdesc, C::IDESC_PV,
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&ctrl.v_empty[s]));
@@ -410,6 +413,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         for (int32_t j = 0; j < n && ok; ++j) {
           const uint32_t t = t_cnt + j, kvi = kv_cnt + j;
           const int s = kvi % STAGES;
+          const uint32_t sb = t & 1;
           if (!mbar_wait(smem_u32(&ctrl.k_full[s]), (kvi / STAGES) & 1, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
@@ -419,13 +423,19 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
           const uint32_t sk = sK0 + s * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t adesc = sdesc_sw128(sQ + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024);
             const uint64_t bdesc = sdesc_sw128(sk + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tmem + (t & 1) * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            if constexpr (C::Q_TMEM) {
+              mma_bf16_ts(tmem + sb * BN, tmem + C::Q_COL + kk * 8, bdesc, C::IDESC_QK,
+                          kk > 0 ? 1u : 0u);
+            } else {
+              const uint64_t adesc = sdesc_sw128(sQ + (kk >> 2) * C::BM * 128 + (kk & 3) * 32, 16, 1024);
+              mma_bf16_ss(tmem + sb * BN, adesc, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+            }
           }
-          mma_commit(smem_u32(&ctrl.s_full[t & 1]));
+          mma_commit(smem_u32(&ctrl.s_full[sb]));
           mma_commit(smem_u32(&ctrl.k_empty[s]));
-          if (j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
+          if (!C::Q_TMEM && j == n - 1) mma_commit(smem_u32(&ctrl.q_empty));
+          // QK of tile j runs ahead of PV of tile j-1 (the other S buffer)
           if (j > 0 && !issue_pv(j - 1)) ok = false;
         }
         if (ok && !issue_pv(n - 1)) ok = false;
@@ -692,7 +702,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
 
 template <int D, int BN, int STAGES, int CTAS, int MODE>
 tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStream_t stream) {
-  using C = Cfg<D, BN, STAGES>;
+  using C = Cfg<D, BN, STAGES, CTAS>;
   auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS, MODE>;
   static bool attr_set[64] = {false};
   if (device < 0 || device >= 64 || !attr_set[device]) {
