@@ -257,20 +257,52 @@ __device__ int32_t union_prefix(const uint32_t* a, const uint32_t* b, int32_t* p
   return total;
 }
 
+// Count (bitmap form), validating the tile's lists on the way: indptr must run
+// upward from 0 and each list must be ascending, unique and inside [0, N).  A
+// bad list sets DEV_ERR_BAD_INPUT and is not used as an index; the host checks
+// the error word before anything reads the counts.  Every list belongs to
+// exactly one query tile, so every list is checked once.
+__device__ __forceinline__ bool list_ok(const int64_t* indptr, int64_t row) {
+  return indptr[row + 1] >= indptr[row] && (row != 0 || indptr[0] == 0);
+}
+
+__device__ __forceinline__ bool set_bits_checked(uint32_t* bm, const int32_t* keys, int64_t n,
+                                                 int32_t N) {
+  bool bad = false;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int32_t k = keys[i];
+    if (k < 0 || k >= N || (i + 1 < n && keys[i + 1] <= k)) {
+      bad = true;
+      continue;
+    }
+    atomicOr(&bm[k >> 5], 1u << (k & 31));
+  }
+  return bad;
+}
+
 __global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
     const int64_t* indptr, const int32_t* indices, int64_t n_items, int32_t nqt, int32_t nqb,
-    int32_t slice_m, int32_t N, int32_t* cnt, unsigned long long* tot) {
+    int32_t slice_m, int32_t N, int32_t* cnt, unsigned long long* tot, uint32_t* err) {
   extern __shared__ uint32_t sm[];
   __shared__ int wsum[8];
   const int32_t nw = (N + 31) >> 5;
   uint32_t* bma = sm;
   uint32_t* bmb = sm + nw;
   const int64_t item = blockIdx.x;
+  const int64_t bh = item / nqt, qt = item % nqt;
+  const int64_t qa = (slice_m == 64) ? 2 * qt : qt;
+  const int64_t ra = bh * nqb + qa;
+  const bool two = slice_m == 64 && qa + 1 < nqb;
+  if (!list_ok(indptr, ra) || (two && !list_ok(indptr, ra + 1))) {
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_BAD_INPUT);
+    return;
+  }
   const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
   for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
   __syncthreads();
-  set_bits(bma, L.a, L.na);
-  set_bits(bmb, L.b, L.nb);
+  bool bad = set_bits_checked(bma, L.a, L.na, N);
+  bad = set_bits_checked(bmb, L.b, L.nb, N) || bad;
+  if (bad) atomicOr(err, DEV_ERR_BAD_INPUT);
   __syncthreads();
   int s = 0;
   for (int w = threadIdx.x; w < nw; w += blockDim.x) s += __popc(bma[w] | bmb[w]);
@@ -292,6 +324,14 @@ __global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
   }
 }
 
+// Shared memory of the bitmap emit kernel, in 32-bit words: the two lists'
+// key bitmaps, the union rank of each bitmap word, and the two membership masks
+// in union-rank order (4 words of slack: the last tile's mask words may reach
+// past the union).
+__host__ __device__ constexpr size_t emit_bitmap_words(int32_t N) {
+  return 5 * static_cast<size_t>((N + 31) / 32) + 8;
+}
+
 __global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
     const int64_t* indptr, const int32_t* indices, int32_t nqt, int32_t nqb, int32_t slice_m,
     int32_t N, int32_t bn, const int32_t* cnt_e, const int32_t* ebegin, int2* entries,
@@ -302,11 +342,14 @@ __global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
   uint32_t* bma = sm;
   uint32_t* bmb = sm + nw;
   int32_t* pre = reinterpret_cast<int32_t*>(sm + 2 * nw);
+  uint32_t* rka = sm + 3 * nw;                  // membership of list a, union-rank order
+  uint32_t* rkb = sm + 4 * nw + 4;              // membership of list b
   const int64_t item = blockIdx.x;
   const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
   const int64_t e0 = ebegin[item];
   const int32_t ne = cnt_e[item];
   for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
+  for (int w = threadIdx.x; w < 2 * nw + 8; w += blockDim.x) rka[w] = 0u;
   __syncthreads();
   set_bits(bma, L.a, L.na);
   set_bits(bmb, L.b, L.nb);
@@ -314,37 +357,41 @@ __global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
   const int32_t u = union_prefix(bma, bmb, pre, nw, wsum);
   int32_t* gx = gidx + e0 * bn;
   uint32_t* dw = descs + e0 * 8;
-  const int wpt = bn >> 5;                       // mask words per row segment in use
-  // each group of wpt mask words (bn keys of the union) is written by one thread:
-  // walk union ranks [c*bn, c*bn + bn) through the bitmaps
+  // Each thread takes whole bitmap words: their union keys go to consecutive
+  // ranks starting at pre[w] (so a warp's stores are contiguous), and their
+  // membership bits, shifted to rank order, touch at most two mask words.
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+    const uint32_t A = bma[w], Bm = bmb[w];
+    uint32_t bits = A | Bm;
+    if (!bits) continue;
+    const int32_t rank = pre[w];
+    const int sh = rank & 31;
+    uint64_t pa = 0, pb = 0;
+    int k = 0;
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      gx[rank + k] = (w << 5) + bit;
+      pa |= static_cast<uint64_t>((A >> bit) & 1u) << (sh + k);
+      pb |= static_cast<uint64_t>((Bm >> bit) & 1u) << (sh + k);
+      ++k;
+    }
+    const int g = rank >> 5;
+    if (static_cast<uint32_t>(pa)) atomicOr(&rka[g], static_cast<uint32_t>(pa));
+    if (pa >> 32) atomicOr(&rka[g + 1], static_cast<uint32_t>(pa >> 32));
+    if (static_cast<uint32_t>(pb)) atomicOr(&rkb[g], static_cast<uint32_t>(pb));
+    if (pb >> 32) atomicOr(&rkb[g + 1], static_cast<uint32_t>(pb >> 32));
+  }
+  // padding of the last tile: any in-range key; its columns stay masked
+  for (int64_t q = u + threadIdx.x; q < static_cast<int64_t>(ne) * bn; q += blockDim.x) gx[q] = 0;
+  __syncthreads();
+  const int wpt = bn >> 5;                       // mask words per tile
   for (int32_t c = threadIdx.x; c < ne; c += blockDim.x) {
     uint32_t ma[4] = {0u, 0u, 0u, 0u}, mb[4] = {0u, 0u, 0u, 0u};
-    const int32_t r0 = c * bn, r1 = min(u, r0 + bn);
-    // first word whose prefix reaches r0
-    int lo = 0, hi = nw - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
-    }
-    int32_t rank = pre[lo];
-    for (int w = lo; w < nw && rank < r1; ++w) {
-      uint32_t bits = bma[w] | bmb[w];
-      while (bits && rank < r1) {
-        const int bit = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        if (rank >= r0) {
-          const int col = rank - r0;
-          const int32_t key = (w << 5) + bit;
-          gx[rank] = key;
-          if ((bma[w] >> bit) & 1u) ma[col >> 5] |= 1u << (col & 31);
-          if ((bmb[w] >> bit) & 1u) mb[col >> 5] |= 1u << (col & 31);
-        }
-        ++rank;
-      }
-    }
-    for (int32_t q = r1; q < r0 + bn; ++q) gx[q] = 0;   // padding, masked
-    bool full = (r1 - r0 == bn);
+    bool full = static_cast<int64_t>(c + 1) * bn <= u;
     for (int w = 0; w < wpt; ++w) {
+      ma[w] = rka[c * wpt + w];
+      mb[w] = rkb[c * wpt + w];
       full = full && ma[w] == 0xFFFFFFFFu;
       if (L.b_rows) full = full && mb[w] == 0xFFFFFFFFu;
     }
@@ -375,39 +422,46 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
   const int threads = 256;
-  keylist_validate_kernel<<<static_cast<unsigned>((n_lists * 32 + threads - 1) / threads), threads, 0,
-                            stream>>>(mask->indptr, mask->indices, n_lists, N, P->err);
-  TSR_CUDA(cudaGetLastError());
-  unsigned long long* host_tot = P->host_tot;
-  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
-  TSR_CUDA(cudaStreamSynchronize(stream));
-  if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
-    return fail(TSR_ERR_INVALID_ARG,
-                "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward");
   const bool bitmap = N <= kBitmapMaxN;
   const size_t nw = static_cast<size_t>((N + 31) / 32);
+  unsigned long long* host_tot = P->host_tot;
+  const char* bad_lists =
+      "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward";
   if (bitmap) {
+    // validation runs inside the count kernel
     static bool attr_done[64] = {false};
     if (P->device < 0 || P->device >= 64 || !attr_done[P->device]) {
       TSR_CUDA(cudaFuncSetAttribute(keylist_count_bitmap_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * 4 * kBitmapMaxN / 32));
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(2 * 4 * ((kBitmapMaxN + 31) / 32))));
       TSR_CUDA(cudaFuncSetAttribute(keylist_emit_bitmap_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 3 * 4 * kBitmapMaxN / 32));
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(4 * emit_bitmap_words(kBitmapMaxN))));
       if (P->device >= 0 && P->device < 64) attr_done[P->device] = true;
     }
     if (n_items > 0) {
       keylist_count_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 2 * 4 * nw, stream>>>(
-          mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
+          mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot, P->err);
       TSR_CUDA(cudaGetLastError());
     }
   } else {
+    keylist_validate_kernel<<<static_cast<unsigned>((n_lists * 32 + threads - 1) / threads), threads,
+                              0, stream>>>(mask->indptr, mask->indices, n_lists, N, P->err);
+    TSR_CUDA(cudaGetLastError());
+    TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+    TSR_CUDA(cudaStreamSynchronize(stream));
+    if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
+      return fail(TSR_ERR_INVALID_ARG, bad_lists);
     keylist_count_kernel<<<static_cast<unsigned>((n_items * 32 + threads - 1) / threads), threads, 0,
                            stream>>>(mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot);
     TSR_CUDA(cudaGetLastError());
   }
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
   TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost,
                            stream));
   TSR_CUDA(cudaStreamSynchronize(stream));
+  if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
+    return fail(TSR_ERR_INVALID_ARG, bad_lists);
 
   P->n_logical_on = static_cast<int64_t>(host_tot[4]);
   P->n_logical_total = n_lists * static_cast<int64_t>(N);
@@ -451,7 +505,8 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
                                         static_cast<int32_t*>(P->b_hist.p), P->items, stream))
     return s;
   if (n_items > 0 && bitmap) {
-    keylist_emit_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 3 * 4 * nw, stream>>>(
+    keylist_emit_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 4 * emit_bitmap_words(N),
+                                 stream>>>(
         mask->indptr, mask->indices, nqt, nqb, M, N, rg.bn, cnt_e, ebegin,
         static_cast<int2*>(P->entries), static_cast<uint32_t*>(P->descs), P->gidx);
     TSR_CUDA(cudaGetLastError());

@@ -333,6 +333,26 @@ def test_keylist_invalid_lists_rejected():
     mask = tsr.make_mask(spec.kind, 1, 1, 512, 64, **W.mask_tensors(spec))
     with pytest.raises(tsr.TsrError):
         tsr.tsr_plan(mask)
+    # a negative key in the second list of a query tile, a decreasing indptr,
+    # and an indptr that does not start at 0
+    good = W.random_keylist(3, 1, 1, 512, slice_m=64, lo=4, hi=20)
+    neg = good.indices.copy()
+    neg[good.indptr[1]] = -1
+    bad_ptr = good.indptr.copy()
+    bad_ptr[3] = bad_ptr[2] - 1
+    off_ptr = good.indptr.copy()
+    off_ptr[0] = 1                                   # every offset stays inside the array
+    for ind, ptr in ((neg, good.indptr), (good.indices, bad_ptr), (good.indices, off_ptr)):
+        t = W.mask_tensors(good)
+        t["indices"] = torch.as_tensor(np.asarray(ind, np.int32)).cuda()
+        t["indptr"] = torch.as_tensor(np.asarray(ptr, np.int64)).cuda()
+        with pytest.raises(tsr.TsrError) as e:
+            tsr.tsr_plan(tsr.make_mask(good.kind, 1, 1, 512, 64, **t))
+        assert e.value.status == 1
+    # the valid lists still plan and run after the refusals
+    (q, k, v), plan, O, L = run(good, 64, seed=4)
+    O_ref, L_ref = oracle.attention(good, q, k, v)
+    compare(O_ref, L_ref, O, L, "keylist after refusals")
 
 
 @pytest.mark.slow
