@@ -297,16 +297,31 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         tma_tile(&p.tq, sQ, smem_u32(&ctrl.q_full), q_tile * C::BM, C::BM, C::Q_BYTES, bh);
       }
       ++q_cnt;
-      // one K or V tile of entry e into stage buffer dst
-      auto load_kv = [&](const CUtensorMap* map, const __nv_bfloat16* base, int32_t e, uint32_t dst,
-                         uint32_t bar) {
-        const int32_t kv = __ldg(&p.entries[e]).x;
-        if (GATHER || perm) {
+      // Where tile e's rows come from: its first key row (TMA, temporal-major),
+      // or its slice of gidx (key lists; gathered tile e owns gidx[e * BN, +BN)).
+      // Key-list sources are fetched one tile ahead, so the gidx load latency
+      // overlaps the stage wait (measured +21 %); the others are fetched after
+      // the stage wait, separately for K and V (fetching them earlier, or
+      // reusing K's for V, measured 2 % slower on SVG).
+      auto tile_src = [&](int32_t e, int32_t (&rows)[BN / 32]) -> int32_t {
+        if constexpr (GATHER) {
+#pragma unroll
+          for (int m = 0; m < BN / 32; ++m) rows[m] = __ldg(p.gidx + e * BN + 32 * m + lane);
+          return e * BN;
+        } else {
+          return __ldg(&p.entries[e]).x;
+        }
+      };
+      // one K or V tile into stage buffer dst
+      auto load_kv = [&](const CUtensorMap* map, const __nv_bfloat16* base, int32_t kv,
+                         const int32_t (&src_rows)[BN / 32], uint32_t dst, uint32_t bar) {
+        if (GATHER) {
+          gather_tile<D, BN, true>(base + head_off, src_rows, dst, bar, lane);
+        } else if (perm) {
           int32_t rows[BN / 32];
 #pragma unroll
-          for (int m = 0; m < BN / 32; ++m)
-            rows[m] = GATHER ? __ldg(p.gidx + kv + 32 * m + lane) : perm_row(kv + 32 * m + lane);
-          gather_tile<D, BN, GATHER>(base + head_off, rows, dst, bar, lane);
+          for (int m = 0; m < BN / 32; ++m) rows[m] = perm_row(kv + 32 * m + lane);
+          gather_tile<D, BN, false>(base + head_off, rows, dst, bar, lane);
         } else {
           tma_tile(map, dst, bar, kv, BN, C::KV_BYTES, bh);
         }
@@ -315,7 +330,11 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       // MMA issuer runs before PV(i-1); a K stage is released by its QK, a V
       // stage by its PV, so the K stream never waits behind a PV.
       const int32_t n = end - begin;
+      int32_t kv_k = 0, rows_k[BN / 32] = {}, kv_v = 0, rows_v[BN / 32] = {};
+      if (GATHER && n > 0) kv_k = tile_src(begin, rows_k);
       for (int32_t i = 0; i <= n && ok; ++i) {
+        int32_t kv_n = 0, rows_n[BN / 32] = {};
+        if (GATHER && i + 1 < n) kv_n = tile_src(begin + i + 1, rows_n);
         if (i < n) {
           const uint32_t kvi = kv_cnt + i;
           const int s = kvi % STAGES;
@@ -323,7 +342,8 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             ok = false;
             break;
           }
-          load_kv(&p.tk, p.kg, begin + i, sK0 + s * C::KV_BYTES, smem_u32(&ctrl.k_full[s]));
+          if (!GATHER) kv_k = tile_src(begin + i, rows_k);
+          load_kv(&p.tk, p.kg, kv_k, rows_k, sK0 + s * C::KV_BYTES, smem_u32(&ctrl.k_full[s]));
           ++k_iss;
         }
         if (i >= 1) {
@@ -333,8 +353,17 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             ok = false;
             break;
           }
-          load_kv(&p.tv, p.vg, begin + i - 1, sV0 + s * C::KV_BYTES, smem_u32(&ctrl.v_full[s]));
+          if (!GATHER) kv_v = tile_src(begin + i - 1, rows_v);
+          load_kv(&p.tv, p.vg, kv_v, rows_v, sV0 + s * C::KV_BYTES, smem_u32(&ctrl.v_full[s]));
           ++v_iss;
+        }
+        kv_v = kv_k;
+#pragma unroll
+        for (int m = 0; m < BN / 32; ++m) rows_v[m] = rows_k[m];
+        if constexpr (GATHER) {
+          kv_k = kv_n;
+#pragma unroll
+          for (int m = 0; m < BN / 32; ++m) rows_k[m] = rows_n[m];
         }
       }
       kv_cnt += n;
