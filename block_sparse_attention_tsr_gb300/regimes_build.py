@@ -35,6 +35,21 @@ DENSITY_EDGES = (0.0, 0.15, 0.30, 0.45, 0.60, 1.01)
 N_BUCKETS = ((0, 8191, 4096), (8192, 1 << 24, 32760))   # (n_min, n_max, N used to profile)
 VARIANTS = {128: ((128, 3, 1), (128, 2, 1), (64, 4, 1), (64, 2, 2)),
             64: ((128, 4, 1), (64, 4, 1), (64, 3, 2))}
+# key-list (M x 1 slice) masks: classes by slice height and listed-key fraction;
+# the gathered kernel variants
+KEYLIST_M = (64, 128)
+KEYLIST_EDGES = (0.0, 0.10, 0.20, 0.35, 0.60, 1.01)
+VARIANTS_GATHERED = {128: ((128, 3, 1), (64, 2, 2)), 64: ((128, 4, 1), (64, 3, 2))}
+
+
+def keylist_spec(N, M, frac, heads, seed):
+    """A key-list mask of one head's lists (clustered runs), repeated for every
+    head: the generator is slow at high densities, and identical heads time the
+    same as distinct ones of the same class."""
+    one = W.keylist_mask(seed=seed, B=1, H=1, N=N, slice_m=M, frac=frac)
+    indptr = np.concatenate([[0]] + [one.indptr[1:] + h * one.indptr[-1] for h in range(heads)])
+    return W.MaskSpec(W.MASK_KEYLIST, 1, heads, N, slice_m=M, indptr=indptr.astype(np.int64),
+                      indices=np.tile(one.indices, heads))
 
 
 def time_variant(mask, q, k, v, out, lse, variant, reps):
@@ -94,13 +109,43 @@ def main():
                     rows.append((W.MASK_UNIFORM, bq, bk, n_min, n_max, lo, hi, d) + best)
                     print(f"d={d} N={N} {bq}x{bk} dens[{lo:.2f},{hi:.2f}) -> {best}  " +
                           " ".join(f"{vv}:{t:.3f}ms" for vv, t in med.items()), flush=True)
-            # masks of the other kinds: one default row per head dimension
+            # key-list masks (listed keys drawn in clustered runs, mean length 8)
+            for M in KEYLIST_M:
+                for lo, hi in zip(KEYLIST_EDGES[:-1], KEYLIST_EDGES[1:]):
+                    times = {vv: [] for vv in VARIANTS_GATHERED[d]}
+                    for m in range(args.masks):
+                        spec = keylist_spec(N, M, 0.5 * (lo + min(hi, 1.0)), args.heads,
+                                            seed=31 * M + 7 * m + int(100 * lo))
+                        mask = tsr.make_mask(spec.kind, 1, args.heads, N, d, **W.mask_tensors(spec))
+                        for vv in VARIANTS_GATHERED[d]:
+                            times[vv].append(time_variant(mask, q, k, v, out, lse, vv, args.reps))
+                    med = {vv: float(np.median(t)) for vv, t in times.items()}
+                    best = min(med, key=med.get)
+                    rows.append((W.MASK_KEYLIST, M, 1, n_min, n_max, lo, hi, d) + best)
+                    print(f"d={d} N={N} keylist M={M} frac[{lo:.2f},{hi:.2f}) -> {best}  " +
+                          " ".join(f"{vv}:{t:.3f}ms" for vv, t in med.items()), flush=True)
+            # head-routed (SVG) masks: one row per length bucket
+            F = 21 if N >= 8192 else 16         # >= 16 frames: at most 8 segments per tile
+            S = N // F
+            spec = W.svg_mask(1, args.heads, n_frames=F, frame_size=S)
+            qs, ks, vs = (x.cuda() for x in W.qkv(1, args.heads, F * S, d, seed=6))
+            outs = torch.empty_like(qs)
+            lses = torch.empty((1, args.heads, F * S), device="cuda")
+            mask = tsr.make_mask(spec.kind, 1, args.heads, F * S, d, **W.mask_tensors(spec))
+            med = {vv: time_variant(mask, qs, ks, vs, outs, lses, vv, args.reps)
+                   for vv in VARIANTS[d]}
+            best = min(med, key=med.get)
+            rows.append((W.MASK_SVG, "*", "*", n_min, n_max, "*", "*", d) + best)
+            print(f"d={d} N={F * S} svg -> {best}  " +
+                  " ".join(f"{vv}:{t:.3f}ms" for vv, t in med.items()), flush=True)
+    # anything else: one default row per head dimension
     rows.append(("*", "*", "*", "*", "*", "*", "*", 128, 64, 2, 2))
     rows.append(("*", "*", "*", "*", "*", "*", "*", 64, 64, 3, 2))
     with open(args.out, "w") as f:
         f.write("# Regime table for GB300 (sm_103a), written by regimes_build.py\n")
-        f.write(f"# {time.strftime('%Y-%m-%d')}: {args.masks} seeded banded-plus-random masks per "
-                f"class, {args.heads} heads, median of plan + forward time\n")
+        f.write(f"# {time.strftime('%Y-%m-%d')}: {args.masks} seeded masks per class (banded-plus-"
+                f"random blocks; clustered key lists, one head's repeated; SVG routing), "
+                f"{args.heads} heads, median of plan + forward time\n")
         f.write("# kind bq bk n_min n_max dens_min dens_max d bn stages ctas\n")
         for r in rows:
             f.write(" ".join(f"{x:.2f}" if isinstance(x, float) else str(x) for x in r) + "\n")
