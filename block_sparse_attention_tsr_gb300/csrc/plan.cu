@@ -114,6 +114,48 @@ __device__ int classify(const MaskDev& m, int bh, int h, const RowSegs& rs, int 
   return 2;
 }
 
+// Key tiles of width w that can hold an allowed key for query rows [q0, q1),
+// as up to two ascending, disjoint tile-index ranges [t0, t1).  SVG spatial
+// heads: frame 0 and the rows' own frames; SVG temporal heads (temporal-major
+// order): the rows' own F-token segments.  Every other tile is empty for these
+// rows, so count and emit skip it.  Other mask kinds: all tiles.
+struct KeyWindow {
+  int n;
+  int t0[2], t1[2];
+  __device__ int size() const { return (t1[0] - t0[0]) + (n > 1 ? t1[1] - t0[1] : 0); }
+  __device__ int tile(int i) const { return i < t1[0] - t0[0] ? t0[0] + i : t0[1] + i - (t1[0] - t0[0]); }
+};
+
+__device__ KeyWindow key_window(const MaskDev& m, int h, int q0, int q1, int w) {
+  int lo0 = 0, hi0 = m.N, lo1 = 0, hi1 = 0;   // token ranges
+  if (m.kind == TSR_MASK_SVG) {
+    if (m.head_kind[h] == TSR_HEAD_TEMPORAL) {
+      lo0 = (q0 / m.F) * m.F;
+      hi0 = min(m.N, ((q1 + m.F - 1) / m.F) * m.F);
+    } else {
+      hi0 = m.S;
+      lo1 = (q0 / m.S) * m.S;
+      hi1 = min(m.N, ((q1 - 1) / m.S + 1) * m.S);
+    }
+  }
+  KeyWindow kw;
+  kw.n = 1;
+  kw.t0[0] = lo0 / w;
+  kw.t1[0] = (hi0 + w - 1) / w;
+  kw.t0[1] = kw.t1[1] = 0;
+  if (hi1 > lo1) {
+    const int b0 = lo1 / w, b1 = (hi1 + w - 1) / w;
+    if (b0 <= kw.t1[0]) {
+      kw.t1[0] = max(kw.t1[0], b1);
+    } else {
+      kw.n = 2;
+      kw.t0[1] = b0;
+      kw.t1[1] = b1;
+    }
+  }
+  return kw;
+}
+
 __device__ void grid_dims(const MaskDev& m, int64_t* nqs, int64_t* nks) {
   if (m.kind == TSR_MASK_UNIFORM) {
     *nqs = (m.N + m.bq - 1) / m.bq;
@@ -140,10 +182,12 @@ __global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned
   rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
   int64_t nqs, nks;
   grid_dims(m, &nqs, &nks);
-  const int nkt128 = (m.N + 127) / 128;
+  const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), 128);
+  const int n_kt = kw.size();
   int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
   bool bad = false;
-  for (int kt = lane; kt < nkt128; kt += 32) {
+  for (int i = lane; i < n_kt; i += 32) {
+    const int kt = kw.tile(i);
     const int ca = classify(m, bh, h, rs, kt * 128, 64, nqs, nks, nullptr);
     const int cb = classify(m, bh, h, rs, kt * 128 + 64, 64, nqs, nks, nullptr);
     if (ca < 0 || cb < 0) {
@@ -258,12 +302,13 @@ __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32
   rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
   int64_t nqs, nks;
   grid_dims(m, &nqs, &nks);
-  const int nkt = (m.N + bn - 1) / bn;
+  const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), bn);
+  const int n_kt = kw.size();
   int32_t e_pos = ebegin[warp], d_pos = dbegin[warp];
-  for (int base = 0; base < nkt; base += 32) {
-    const int kt = base + lane;
+  for (int base = 0; base < n_kt; base += 32) {
+    const int kt = (base + lane < n_kt) ? kw.tile(base + lane) : 0;
     tsr_tile_desc d;
-    const int c = (kt < nkt) ? classify(m, bh, h, rs, kt * bn, bn, nqs, nks, &d) : 0;
+    const int c = (base + lane < n_kt) ? classify(m, bh, h, rs, kt * bn, bn, nqs, nks, &d) : 0;
     const unsigned nonempty = __ballot_sync(0xFFFFFFFFu, c > 0);
     const unsigned bnd = __ballot_sync(0xFFFFFFFFu, c == 2);
     const unsigned below = (1u << lane) - 1u;
