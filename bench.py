@@ -240,6 +240,77 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args) -> None:
+    """Mask sweep through the regime table: members 0 .. K-1 of the seeded sweep
+    (block shape from five, density U(0.05, 0.60)); each mask is planned and run
+    with the table's regime and with every compiled variant forced, and the
+    table's regret against the best variant is reported.  One JSON line."""
+    import torch
+    import block_sparse_attention_tsr_gb300 as tsr
+    import workloads as W
+    from block_sparse_attention_tsr_gb300.regimes_build import VARIANTS
+
+    tsr.build()
+    tsr.lib()
+    dev = torch.device("cuda", 0)
+    N, H = 32760, args.heads
+    q, k, v = (x.to(dev) for x in W.qkv(1, H, N, D, seed=10))
+    out = torch.empty_like(q)
+    lse = torch.empty((1, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(mask, opts, reps=3):
+        plan = tsr.tsr_plan(mask, opts, stream)
+        for _ in range(2):
+            plan.update(mask, stream)
+            tsr.tsr_bsa_forward(q, k, v, plan, out, lse, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            plan.update(mask, stream)
+            tsr.tsr_bsa_forward(q, k, v, plan, out, lse, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        tsr.tsr_plan_device_status(plan)
+        st = plan.stats()
+        plan.destroy()
+        return a.elapsed_time(b) / reps, (st["bn"], st["stages"], st["ctas_per_sm"])
+
+    rows = []
+    t0 = time.time()
+    for m in range(args.sweep_masks):
+        spec = W.sweep_mask(m, H=H, N=N)
+        mask = tsr.make_mask(spec.kind, 1, H, N, D, **W.mask_tensors(spec, dev))
+        flops = 4.0 * D * allowed_pairs(spec)
+        t_lut, picked = timed(mask, None)
+        t_var = {vv: timed(mask, {"bn": vv[0], "stages": vv[1], "ctas_per_sm": vv[2]})[0]
+                 for vv in VARIANTS[D]}
+        best = min(t_var, key=t_var.get)
+        rows.append({"m": m, "shape": f"{spec.bq}x{spec.bk}", "rho": spec.meta["rho"],
+                     "flops": flops, "ms_lut": t_lut, "ms_best": t_var[best], "lut": picked,
+                     "best": best})
+    regret = np.array([r["ms_lut"] / r["ms_best"] - 1.0 for r in rows])
+    tot_flops = sum(r["flops"] for r in rows)
+    tot_ms = sum(r["ms_lut"] for r in rows)
+    shapes = {}
+    for r in rows:
+        shapes.setdefault(r["shape"], []).append(r["flops"] / r["ms_lut"] / 1e9)
+    line = {"metric": METRIC, "value": tot_flops / tot_ms / 1e9, "unit": UNIT, "n_gpus": 1,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"sweep_{args.sweep_masks}_masks_N{N}_H{H}_d{D}",
+                       "step": "tsr_plan_update + tsr_bsa_forward per mask, regime from the table",
+                       "l2": "inputs exceed L2; no flush"},
+            "lut_regret": {"mean": float(regret.mean()), "median": float(np.median(regret)),
+                           "p90": float(np.quantile(regret, 0.9)), "max": float(regret.max()),
+                           "picked_best_within_2pct": float(np.mean(regret <= 0.02))},
+            "tflops_by_shape": {k: float(np.mean(v)) for k, v in sorted(shapes.items())},
+            "seconds": time.time() - t0}
+    if args.sweep_detail:
+        line["masks"] = rows
+    print(json.dumps(line, default=str), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -252,9 +323,13 @@ def main():
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--workload", default="video480p",
-                    help="video480p (the benchmark), svg480p, keylist720p, sweepM")
+                    help="video480p (the benchmark), svg480p, keylist720p, sweepM (one member), "
+                         "sweep (regime-table regret over --sweep-masks members)")
     ap.add_argument("--heads", type=int, default=24,
                     help="heads of the workload (24 = the benchmark; fewer for profiling)")
+    ap.add_argument("--sweep-masks", type=int, default=32,
+                    help="with --workload sweep: how many sweep members (256 = all)")
+    ap.add_argument("--sweep-detail", action="store_true", help="per-mask rows in the sweep line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -265,6 +340,10 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload == "sweep":
+        if rank == 0:
+            run_sweep(args)
         return
 
     import torch
