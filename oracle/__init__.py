@@ -48,6 +48,7 @@ class _Mask(ctypes.Structure):
         ("head_kind", ctypes.c_void_p),
         ("slice_m", ctypes.c_int32),
         ("indptr", ctypes.c_void_p), ("indices", ctypes.c_void_p),
+        ("temporal_radius", ctypes.c_int32),
     ]
 
 
@@ -131,6 +132,7 @@ class _Bound:
         ix = arr(spec.indices if spec.indices is None or len(spec.indices) else np.zeros(1),
                  np.int32)
         m.indptr, m.indices = _ptr(ip), _ptr(ix)
+        m.temporal_radius = int(getattr(spec, "temporal_radius", 0))
         self.m = m
 
     @property

@@ -36,7 +36,7 @@ def dense_mask(spec, b: int, h: int) -> np.ndarray:
             f = t // S
             return (f[:, None] == f[None, :]) | (f[None, :] == 0)
         s = t % S
-        return s[:, None] == s[None, :]
+        return np.abs(s[:, None] - s[None, :]) <= int(getattr(spec, "temporal_radius", 0))
     if spec.kind == KEYLIST:
         M = spec.slice_m
         nqb = -(-N // M)

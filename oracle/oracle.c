@@ -31,7 +31,8 @@
  *             row / column is truncated at N, not padded.
  *   SEGMENTS: allowed(i, j) = L[b][h][seg_q(i)][seg_k(j)] for ascending bounds.
  *   SVG     : spatial head  -> frame(i) == frame(j) or frame(j) == 0
- *             temporal head -> i mod S == j mod S   (same spatial index)
+ *             temporal head -> |i mod S - j mod S| <= r (spatial index within
+ *                              radius r of the query's; r = 0: the same index)
  *             with frame(t) = t / S, tokens in frame-major order (t = f*S + s).
  *             The oracle never permutes tokens.
  *   KEYLIST : allowed(i, j) = j is in the sorted key list of query block i / M.
@@ -66,6 +67,8 @@ typedef struct {
   int32_t slice_m;
   const int64_t *indptr;
   const int32_t *indices;
+  /* SVG temporal heads: spatial radius r >= 0 */
+  int32_t temporal_radius;
 } oracle_mask;
 
 static int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -116,8 +119,11 @@ static int64_t allowed_keys(const oracle_mask *m, int32_t b, int32_t h, int32_t 
       const int32_t fi = i / S;
       for (int32_t j = 0; j < N; ++j)
         if (j / S == fi || j / S == 0) keys[n++] = j;
-    } else {                               /* temporal: same spatial index */
-      for (int32_t j = i % S; j < N; j += S) keys[n++] = j;
+    } else {                               /* temporal: spatial index within r */
+      const int32_t si = i % S, r = m->temporal_radius;
+      const int32_t lo = si - r < 0 ? 0 : si - r, hi = si + r > S - 1 ? S - 1 : si + r;
+      for (int32_t f = 0; f * S < N; ++f)
+        for (int32_t sj = lo; sj <= hi; ++sj) keys[n++] = f * S + sj;
     }
     break;
   }
@@ -187,6 +193,7 @@ static int check_mask(const oracle_mask *m) {
   case OR_UNIFORM: return (m->bq > 0 && m->bk > 0 && m->blocks) ? 0 : -1;
   case OR_SEGMENTS: return (m->n_qseg > 0 && m->n_kseg > 0 && m->q_bounds && m->k_bounds && m->blocks) ? 0 : -1;
   case OR_SVG: return (m->frame_size > 0 && m->n_frames > 0 && m->head_kind &&
+                       m->temporal_radius >= 0 &&
                        (int64_t)m->frame_size * m->n_frames == m->N) ? 0 : -1;
   case OR_KEYLIST: return (m->slice_m > 0 && m->indptr && m->indices) ? 0 : -1;
   default: return -1;

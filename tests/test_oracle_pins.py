@@ -42,10 +42,12 @@ def _masks_small(N=200, H=2):
     out.append(W.svg_mask(1, H, n_frames=5, frame_size=N // 5, kinds=np.array([0, 1][:H], np.int8)))
     out.append(W.random_keylist(5, 1, H, N, slice_m=64, lo=0, hi=N // 2))
     out.append(W.random_keylist(6, 1, H, N, slice_m=128, lo=1, hi=N))
+    out.append(W.svg_mask(1, H, n_frames=5, frame_size=N // 5, kinds=np.array([1, 0][:H], np.int8),
+                          temporal_radius=3))
     return out
 
 
-@pytest.mark.parametrize("idx", range(8))
+@pytest.mark.parametrize("idx", range(9))
 @pytest.mark.parametrize("d", [64, 128])
 def test_brute_force_agrees(idx, d):
     spec = _masks_small()[idx]
@@ -129,6 +131,53 @@ def test_svg_counted_densities(F, S):
     assert per[1] == F * S * F
     if (F, S) == (21, 1560):
         assert per[0] == 99_777_600 and per[1] == 687_960
+
+
+@pytest.mark.parametrize("F,S,r", [(21, 1560, 1), (5, 40, 3), (16, 17, 16), (4, 10, 25)])
+def test_svg_temporal_radius_counted(F, S, r):
+    """Temporal head with radius r: a row with spatial index s sees F keys for
+    each index in [max(0, s - r), min(S - 1, s + r)], so summed over the S
+    indices |E| = F^2 (S (2r + 1) - r (r + 1)) while r < S, and N^2 beyond."""
+    spec = W.svg_mask(1, 1, n_frames=F, frame_size=S, kinds=np.array([1], np.int8),
+                      temporal_radius=r)
+    per = oracle.count_allowed(spec)
+    want = F * F * (S * (2 * r + 1) - r * (r + 1)) if r < S else (F * S) ** 2
+    assert per[0] == want
+    for i in (0, S - 1, S // 2, F * S - 1):
+        s_i = i % S
+        assert len(oracle.row_keys(spec, 0, 0, i)) == F * (min(S - 1, s_i + r) - max(0, s_i - r) + 1)
+
+
+def test_temporal_radius_covering_frame_is_dense():
+    """r >= S - 1 allows every key: dense attention (library fp64 routine)."""
+    F, S, d = 4, 24, 64
+    N = F * S
+    q, k, v = _qkv(1, 1, N, d, seed=23)
+    spec = W.svg_mask(1, 1, n_frames=F, frame_size=S, kinds=np.array([1], np.int8),
+                      temporal_radius=S - 1)
+    O, L = oracle.attention(spec, q, k, v)
+    qd, kd, vd = (x.double() for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd)
+    assert np.abs(O - ref.numpy()).max() <= 1e-12
+
+
+def test_temporal_radius_is_a_band_in_temporal_major_order():
+    """In temporal-major order t' = s F + f, the radius-r temporal pattern is
+    the band |i - j| <= r of F x F blocks."""
+    F, S, d, r = 6, 40, 64, 2
+    N = F * S
+    q, k, v = _qkv(1, 1, N, d, seed=73)
+    spec = W.svg_mask(1, 1, n_frames=F, frame_size=S, kinds=np.array([1], np.int8),
+                      temporal_radius=r)
+    O, L = oracle.attention(spec, q, k, v)
+    perm = np.array([(tp % F) * S + tp // F for tp in range(N)])
+    qp, kp, vp = (x[:, :, perm].contiguous() for x in (q, k, v))
+    idx = np.arange(S)
+    blk = (np.abs(idx[:, None] - idx[None, :]) <= r).astype(np.uint8)[None, None]
+    spec_p = W.MaskSpec(W.MASK_UNIFORM, 1, 1, N, bq=F, bk=F, blocks=blk)
+    Op, Lp = oracle.attention(spec_p, qp, kp, vp)
+    assert np.abs(Op - O[:, :, perm]).max() <= 1e-12
+    assert np.abs(Lp - L[:, :, perm]).max() <= 1e-12
 
 
 def test_one_key_closed_form():

@@ -59,6 +59,7 @@ class MaskSpec:
     slice_m: int = 0
     indptr: Optional[np.ndarray] = None
     indices: Optional[np.ndarray] = None
+    temporal_radius: int = 0
     meta: dict = field(default_factory=dict)
 
 
@@ -204,17 +205,18 @@ def segment_mask(seed: int, B: int, H: int, N: int, lo: int = 16, hi: int = 200,
 # --------------------------------------------------------------------------
 
 def svg_mask(B: int = 1, H: int = 24, n_frames: int = 21, frame_size: int = 1560,
-             kinds: Optional[np.ndarray] = None) -> MaskSpec:
+             kinds: Optional[np.ndarray] = None, temporal_radius: int = 0) -> MaskSpec:
     """Half the heads spatial, half temporal (first half spatial), unless
-    ``kinds`` gives the routing explicitly."""
+    ``kinds`` gives the routing explicitly.  ``temporal_radius`` r widens a
+    temporal head to the spatial indices within r of the query's."""
     if kinds is None:
         kinds = np.array([HEAD_SPATIAL] * (H // 2) + [HEAD_TEMPORAL] * (H - H // 2),
                          dtype=np.int8)
     kinds = np.asarray(kinds, dtype=np.int8)
     assert kinds.shape == (H,)
     return MaskSpec(MASK_SVG, B, H, n_frames * frame_size, head_kind=kinds,
-                    n_frames=n_frames, frame_size=frame_size,
-                    meta={"workload": f"svg_F{n_frames}_S{frame_size}_H{H}"})
+                    n_frames=n_frames, frame_size=frame_size, temporal_radius=temporal_radius,
+                    meta={"workload": f"svg_F{n_frames}_S{frame_size}_H{H}_r{temporal_radius}"})
 
 
 # --------------------------------------------------------------------------
@@ -309,7 +311,7 @@ def mask_tensors(spec: MaskSpec, device="cuda") -> dict:
         return None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=dt)).to(device)
 
     kw = dict(bq=spec.bq, bk=spec.bk, n_frames=spec.n_frames, frame_size=spec.frame_size,
-              slice_m=spec.slice_m)
+              slice_m=spec.slice_m, temporal_radius=spec.temporal_radius)
     kw["blocks"] = t(spec.blocks, np.uint8)
     kw["q_bounds"] = t(spec.q_bounds, np.int32)
     kw["k_bounds"] = t(spec.k_bounds, np.int32)
