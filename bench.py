@@ -203,8 +203,9 @@ def allowed_pairs(spec) -> int:
     if spec.kind == W.MASK_UNIFORM:
         return allowed_pairs_uniform(spec)
     if spec.kind == W.MASK_SVG:
-        S, F, N = spec.frame_size, spec.n_frames, spec.N
-        per = [S * S * (2 * F - 1) if int(k) == W.HEAD_SPATIAL else N * F for k in spec.head_kind]
+        S, F, N, r = spec.frame_size, spec.n_frames, spec.N, spec.temporal_radius
+        temporal = F * F * (S * (2 * r + 1) - r * (r + 1)) if r < S else N * N
+        per = [S * S * (2 * F - 1) if int(k) == W.HEAD_SPATIAL else temporal for k in spec.head_kind]
         return int(sum(per)) * spec.B
     if spec.kind == W.MASK_KEYLIST:
         M, N = spec.slice_m, spec.N

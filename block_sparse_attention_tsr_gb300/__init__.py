@@ -54,6 +54,7 @@ class _Mask(ctypes.Structure):
         ("head_kind", ctypes.c_void_p),
         ("slice_m", ctypes.c_int32),
         ("indptr", ctypes.c_void_p), ("indices", ctypes.c_void_p),
+        ("temporal_radius", ctypes.c_int32),
     ]
 
 
@@ -158,7 +159,8 @@ class Mask:
 
     def __init__(self, kind: int, B: int, H: int, N: int, d: int, *, bq: int = 0, bk: int = 0,
                  blocks=None, q_bounds=None, k_bounds=None, head_kind=None, n_frames: int = 0,
-                 frame_size: int = 0, slice_m: int = 0, indptr=None, indices=None):
+                 frame_size: int = 0, slice_m: int = 0, indptr=None, indices=None,
+                 temporal_radius: int = 0):
         self.tensors = dict(blocks=blocks, q_bounds=q_bounds, k_bounds=k_bounds,
                             head_kind=head_kind, indptr=indptr, indices=indices)
         s = _Mask()
@@ -172,6 +174,7 @@ class Mask:
         s.n_frames, s.frame_size = n_frames, frame_size
         s.slice_m = slice_m
         s.indptr, s.indices = _dptr(indptr), _dptr(indices)
+        s.temporal_radius = int(temporal_radius)
         self.struct = s
         self.kind, self.B, self.H, self.N, self.d = kind, B, H, N, d
 

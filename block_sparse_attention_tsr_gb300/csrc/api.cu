@@ -198,6 +198,7 @@ tsr_status check_mask(const tsr_mask* m) {
       if (m->n_frames <= 0 || m->frame_size <= 0 ||
           static_cast<int64_t>(m->n_frames) * m->frame_size != m->N || !m->head_kind)
         return fail(TSR_ERR_INVALID_ARG, "SVG needs N = n_frames * frame_size and head_kind");
+      if (m->temporal_radius < 0) return fail(TSR_ERR_INVALID_ARG, "temporal_radius must be >= 0");
       return TSR_OK;
     case TSR_MASK_KEYLIST:
       if (m->slice_m != 64 && m->slice_m != 128)

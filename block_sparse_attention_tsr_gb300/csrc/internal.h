@@ -32,6 +32,7 @@ struct MaskDev {
   const int32_t* k_bounds;
   const uint8_t* blocks;
   int32_t F, S;
+  int32_t R;                 // SVG temporal radius
   const int8_t* head_kind;   // device copy, [H]
   int32_t slice_m;
   const int64_t* indptr;

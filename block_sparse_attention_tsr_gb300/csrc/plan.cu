@@ -72,7 +72,7 @@ __device__ int tile_segments(const MaskDev& m, int h, int axis, int t0, int t1, 
 __device__ __forceinline__ bool seg_allowed(const MaskDev& m, int bh, int h, int qid, int kid,
                                             int64_t nqs, int64_t nks) {
   if (m.kind == TSR_MASK_SVG) {
-    if (m.head_kind[h] == TSR_HEAD_TEMPORAL) return qid == kid;  // same spatial index
+    if (m.head_kind[h] == TSR_HEAD_TEMPORAL) return abs(qid - kid) <= m.R;  // index within R
     return qid == kid || kid == 0;                                // same frame, or frame 0
   }
   return m.blocks[(static_cast<int64_t>(bh) * nqs + qid) * nks + kid] != 0;
@@ -117,8 +117,9 @@ __device__ int classify(const MaskDev& m, int bh, int h, const RowSegs& rs, int 
 // Key tiles of width w that can hold an allowed key for query rows [q0, q1),
 // as up to two ascending, disjoint tile-index ranges [t0, t1).  SVG spatial
 // heads: frame 0 and the rows' own frames; SVG temporal heads (temporal-major
-// order): the rows' own F-token segments.  Every other tile is empty for these
-// rows, so count and emit skip it.  Other mask kinds: all tiles.
+// order): the F-token segments within the radius of the rows' own.  Every
+// other tile is empty for these rows, so count and emit skip it.  Other mask
+// kinds: all tiles.
 struct KeyWindow {
   int n;
   int t0[2], t1[2];
@@ -130,8 +131,9 @@ __device__ KeyWindow key_window(const MaskDev& m, int h, int q0, int q1, int w) 
   int lo0 = 0, hi0 = m.N, lo1 = 0, hi1 = 0;   // token ranges
   if (m.kind == TSR_MASK_SVG) {
     if (m.head_kind[h] == TSR_HEAD_TEMPORAL) {
-      lo0 = (q0 / m.F) * m.F;
-      hi0 = min(m.N, ((q1 + m.F - 1) / m.F) * m.F);
+      const int64_t s0 = q0 / m.F - m.R, s1 = (q1 - 1) / m.F + 1 + static_cast<int64_t>(m.R);
+      lo0 = static_cast<int>((s0 > 0 ? s0 : 0) * m.F);
+      hi0 = static_cast<int>(s1 * m.F < m.N ? s1 * m.F : m.N);
     } else {
       hi0 = m.S;
       lo1 = (q0 / m.S) * m.S;
@@ -459,6 +461,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   m.blocks = mask->blocks;
   m.F = mask->n_frames;
   m.S = mask->frame_size;
+  m.R = mask->temporal_radius;
   m.head_kind = P->head_kind_dev;
 
   if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items)) return s;
@@ -504,11 +507,13 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     P->n_logical_total = n_grid;
     density = static_cast<double>(host_tot[6]) / static_cast<double>(n_grid);
   } else if (m.kind == TSR_MASK_SVG) {
-    // allowed elements per head: spatial S^2 (2F - 1), temporal N F
-    const double S = m.S, F = m.F;
+    // allowed elements per head: spatial S^2 (2F - 1); temporal with radius r
+    // F^2 (S (2r + 1) - r (r + 1)) while r < S, else N^2
+    const double S = m.S, F = m.F, r = m.R;
+    const double temporal = (m.R < m.S) ? F * F * (S * (2 * r + 1) - r * (r + 1))
+                                        : static_cast<double>(N) * N;
     double on = 0;
-    for (int32_t h = 0; h < H; ++h)
-      on += (P->head_layout[h] ? static_cast<double>(N) * F : S * S * (2 * F - 1));
+    for (int32_t h = 0; h < H; ++h) on += (P->head_layout[h] ? temporal : S * S * (2 * F - 1));
     P->n_logical_on = static_cast<int64_t>(on) * B;
     P->n_logical_total = static_cast<int64_t>(B) * H * N * static_cast<int64_t>(N);
     density = on / (static_cast<double>(H) * N * static_cast<double>(N));

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define TSR_ABI_VERSION 1
+#define TSR_ABI_VERSION 2
 
 typedef enum {
   TSR_OK = 0,
@@ -89,11 +89,15 @@ typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
  * SVG     : head_kind = int8 [H] (tsr_head_kind), N = n_frames * frame_size,
  *           tokens frame-major (t = f * frame_size + s).
  *             spatial  head: allowed(i, j) = frame(i) == frame(j) || frame(j) == 0
- *             temporal head: allowed(i, j) = i mod frame_size == j mod frame_size
- *           Temporal heads run in temporal-major order (t' = s * n_frames + f);
- *           the library permutes Q/K/V into plan-owned scratch and writes O and
- *           lse back in the caller's order.  frame_size >= 16 and n_frames >= 16
- *           (so that no 128-token tile holds more than 8 segments).
+ *             temporal head: allowed(i, j) = |i mod frame_size - j mod frame_size|
+ *                                            <= temporal_radius
+ *           (temporal_radius = 0: the same spatial index in every frame).
+ *           Temporal heads run in temporal-major order (t' = s * n_frames + f):
+ *           the attention kernel reads their Q/K/V rows through the inverse
+ *           permutation and writes O and lse back in the caller's order; nothing
+ *           is copied.  frame_size >= 16 and n_frames >= 16 (a 128-token tile may
+ *           hold at most 8 segments; smaller values give TSR_ERR_UNSUPPORTED),
+ *           temporal_radius >= 0.
  * KEYLIST : slice_m in {64, 128}.  indptr = int64 [B*H*ceil(N/slice_m) + 1] (CSR
  *           over (b, h, query block), indptr[0] = 0), indices = int32 keys, each
  *           list ascending, unique, in [0, N).  allowed(i, j) = j in the list of
@@ -118,6 +122,8 @@ typedef struct {
   int32_t slice_m;
   const int64_t *indptr;
   const int32_t *indices;
+  /* SVG temporal heads: spatial radius (ABI version 2) */
+  int32_t temporal_radius;
 } tsr_mask;
 
 /* Plan options (pass NULL for defaults). */

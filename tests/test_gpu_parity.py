@@ -144,6 +144,24 @@ def test_svg_ragged_temporal_gather(opts, F, S):
     assert plan.stats()["n_temporal_heads"] == 2
 
 
+@pytest.mark.parametrize("r,opts", [(1, None), (4, {"bn": 128, "stages": 3}),
+                                     (2, {"bn": 64, "stages": 3, "ctas_per_sm": 2}), (40, None)])
+def test_svg_temporal_radius(r, opts):
+    """Temporal heads with a spatial radius: a band of (2r + 1) F-token
+    segments in temporal-major order; r = 40 >= S - 1 makes those heads dense.
+    N = 16 x 41 = 656 leaves ragged tiles."""
+    d = 64 if opts and opts.get("ctas_per_sm") == 2 else 128
+    spec = W.svg_mask(1, 3, n_frames=16, frame_size=41, kinds=np.array([1, 0, 1], np.int8),
+                      temporal_radius=r)
+    (q, k, v), plan, O, L = run(spec, d, seed=31 + r, opts=opts)
+    O_ref, L_ref = oracle.attention(spec, q, k, v)
+    compare(O_ref, L_ref, O, L, f"svg radius {r}")
+    st = check_coverage(spec, plan)
+    F, S = 16, 41
+    temporal = F * F * (S * (2 * r + 1) - r * (r + 1)) if r < S else (F * S) ** 2
+    assert st["allowed"] == 2 * temporal + S * S * (2 * F - 1)
+
+
 def test_q_zero_closed_form_on_gpu():
     """Q = 0: lse_i = ln |A_i| exactly in fp64; the GPU must reproduce the count
     of allowed keys, so a tile computed twice or skipped shows up here."""
