@@ -11,12 +11,16 @@ Contents:
                    the passages it follows and the readings it takes);
   * ``brute.py``   an independent dense NumPy brute force for tiny inputs;
   * ``coverage.c`` expansion of an exported tile plan into element sets, to be
-                   compared bit-exactly with the oracle's allowed set.
+                   compared bit-exactly with the oracle's allowed set;
+  * ``route.py``   SVG head routing by sampled queries (error of each pattern
+                   against dense attention), built on ``oracle.c``.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, dense library attention for the all-ones mask, per-block dense
 attention for block-diagonal masks, Q = 0 / one-key / constant-V closed forms,
-counted densities, permutation invariance).  The pages print no values for any
+counted densities, permutation invariance); ``route.py`` by
+``tests/test_oracle_route.py`` (K = 0 means, brute force, dense radius,
+structured heads).  The pages print no values for any
 input, so nothing is pinned to a worked example of the pages themselves.
 """
 from __future__ import annotations

@@ -223,6 +223,34 @@ def svg_mask(B: int = 1, H: int = 24, n_frames: int = 21, frame_size: int = 1560
 # KEYLIST (M x 1 key-slice) masks
 # --------------------------------------------------------------------------
 
+def svg_routing_heads(B: int, kinds, n_frames: int, frame_size: int, d: int, seed: int,
+                      contrast: float = 6.0, noise: float = 0.5):
+    """bf16 Q, K, V [B, H, N, d] (H = len(kinds)) whose heads are built to be
+    spatial (kinds[h] = 0: Q and K carry a one-hot code of the token's frame in
+    the first n_frames dimensions) or temporal (kinds[h] = 1: a one-hot code of
+    the spatial index modulo d - n_frames in the next dimensions), scaled by
+    ``contrast``, plus N(0, noise^2) in every dimension; V ~ N(0, 1).  Inputs for
+    routing tests only: which pattern a head follows is set here by design."""
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    kinds = np.asarray(kinds, dtype=np.int8)
+    H, N = len(kinds), n_frames * frame_size
+    assert d > n_frames + 1
+    t = np.arange(N)
+    code = np.zeros((H, N, d), np.float32)
+    for h in range(H):
+        if kinds[h] == 0:
+            code[h, t, t // frame_size] = contrast
+        else:
+            code[h, t, n_frames + (t % frame_size) % (d - n_frames)] = contrast
+    code = torch.from_numpy(code)[None].expand(B, H, N, d)
+    q = code + noise * torch.randn((B, H, N, d), generator=g)
+    k = code + noise * torch.randn((B, H, N, d), generator=g)
+    v = torch.randn((B, H, N, d), generator=g)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
 def clustered_keys(N: int, target: int, r: np.random.Generator,
                    mean_run: float = 8.0) -> np.ndarray:
     """Sorted unique key indices: runs with uniform starts and Geometric
