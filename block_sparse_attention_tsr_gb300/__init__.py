@@ -23,7 +23,8 @@ from . import _build
 __all__ = [
     "TsrError", "build", "lib", "make_mask", "Mask", "Plan", "tsr_plan", "tsr_plan_update",
     "tsr_bsa_forward",
-    "tsr_plan_device_status", "tsr_temporal_permute", "tsr_attention_host", "tsr_regime_load",
+    "tsr_plan_device_status", "tsr_temporal_permute", "tsr_svg_route", "tsr_attention_host",
+    "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
     "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL",
 ]
@@ -82,7 +83,7 @@ class _Regime(ctypes.Structure):
 _LIB = None
 EXPORTS = ("tsr_abi_version", "tsr_status_string", "tsr_last_error", "tsr_plan", "tsr_plan_update",
            "tsr_bsa_forward", "tsr_plan_device_status", "tsr_plan_destroy", "tsr_plan_get_stats",
-           "tsr_plan_export", "tsr_temporal_permute", "tsr_attention_host",
+           "tsr_plan_export", "tsr_temporal_permute", "tsr_svg_route", "tsr_attention_host",
            "tsr_release_host_buffers", "tsr_regime_load", "tsr_regime_lookup")
 
 
@@ -117,6 +118,7 @@ def lib():
         "tsr_plan_get_stats": ([P, P], ctypes.c_int),
         "tsr_plan_export": ([P, P, P], ctypes.c_int),
         "tsr_temporal_permute": ([P, P, I32, I32, I32, I32, I32, P, I32, P], ctypes.c_int),
+        "tsr_svg_route": ([P, P, P, I32, I32, I32, I32, I32, I32, P, I32, P, P, P], ctypes.c_int),
         "tsr_attention_host": ([P, P, P, P, P, P, P], ctypes.c_int),
         "tsr_release_host_buffers": ([], None),
         "tsr_regime_load": ([ctypes.c_char_p], ctypes.c_int),
@@ -282,6 +284,27 @@ def tsr_temporal_permute(src: torch.Tensor, dst: torch.Tensor, n_frames: int, fr
     _check(lib().tsr_temporal_permute(_dptr(src), _dptr(dst), B, H, n_frames, frame_size,
                                       row_bytes, hk, 1 if inverse else 0, _stream_ptr(stream)))
     return dst
+
+
+def tsr_svg_route(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_frames: int,
+                  frame_size: int, samples, temporal_radius: int = 0, stats=None,
+                  head_kind=None, stream=None):
+    """Route each head to the spatial or temporal SVG pattern from sampled query
+    rows (see include/tsr.h).  Returns (stats fp32 [B, H, 3], head_kind int8 [H]),
+    both on q's device; ``samples`` is a host sequence of row indices."""
+    B, H, N, d = q.shape
+    if N != n_frames * frame_size or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must be [B, H, n_frames * frame_size, d] alike")
+    if stats is None:
+        stats = torch.empty((B, H, 3), dtype=torch.float32, device=q.device)
+    if head_kind is None:
+        head_kind = torch.empty((H,), dtype=torch.int8, device=q.device)
+    smp = [int(x) for x in samples]
+    arr = (ctypes.c_int32 * max(1, len(smp)))(*smp)
+    _check(lib().tsr_svg_route(_dptr(q), _dptr(k), _dptr(v), B, H, n_frames, frame_size, d,
+                               temporal_radius, ctypes.cast(arr, ctypes.c_void_p), len(smp),
+                               _dptr(stats), _dptr(head_kind), _stream_ptr(stream)))
+    return stats, head_kind
 
 
 def tsr_attention_host(kind: int, B: int, H: int, N: int, d: int, q, k, v, out, lse,

@@ -495,6 +495,30 @@ tsr_status tsr_temporal_permute(const void* src, void* dst, int32_t B, int32_t H
                         static_cast<cudaStream_t>(stream));
 }
 
+tsr_status tsr_svg_route(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                         int32_t n_frames, int32_t frame_size, int32_t d, int32_t temporal_radius,
+                         const int32_t* samples, int32_t n_samples, float* stats,
+                         int8_t* head_kind, void* stream) {
+  set_error("");
+  if (!q || !k || !v || !samples || !stats || !head_kind)
+    return fail(TSR_ERR_INVALID_ARG, "NULL pointer");
+  if (B <= 0 || H <= 0 || n_frames <= 0 || frame_size <= 0 || n_samples <= 0 ||
+      temporal_radius < 0)
+    return fail(TSR_ERR_INVALID_ARG, "B, H, n_frames, frame_size, n_samples must be > 0, "
+                                     "temporal_radius >= 0");
+  if (d != 64 && d != 128) return fail(TSR_ERR_INVALID_ARG, "d must be 64 or 128");
+  const int64_t N = static_cast<int64_t>(n_frames) * frame_size;
+  if (N > (1 << 24)) return fail(TSR_ERR_UNSUPPORTED, "N above 2^24");
+  if (static_cast<int64_t>(B) * H > (1 << 20)) return fail(TSR_ERR_UNSUPPORTED, "B*H above 2^20");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(stats))
+    return fail(TSR_ERR_INVALID_ARG, "q, k, v and stats must be 16-byte aligned");
+  for (int32_t s = 0; s < n_samples; ++s)
+    if (samples[s] < 0 || samples[s] >= N)
+      return fail(TSR_ERR_INVALID_ARG, "sampled row " + std::to_string(s) + " outside [0, N)");
+  return launch_route(q, k, v, B, H, n_frames, frame_size, d, temporal_radius, samples, n_samples,
+                      stats, head_kind, static_cast<cudaStream_t>(stream));
+}
+
 tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, const void* q,
                               const void* k, const void* v, void* out, float* lse) {
   set_error("");

@@ -116,6 +116,11 @@ bool variant_pick(int d, bool gathered, int bn, int stages, int ctas, int* out_b
 tsr_status resolve_regime(Regime table, const tsr_plan_opts* opts, int d, bool gathered,
                           Regime* out);
 
+// SVG head routing (route.cu)
+tsr_status launch_route(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                        int32_t F, int32_t S, int32_t d, int32_t R, const int32_t* samples,
+                        int32_t n_samples, float* stats, int8_t* head_kind, cudaStream_t stream);
+
 // permutation (permute.cu)
 tsr_status launch_permute(const void* src, void* dst, int32_t B, int32_t H, int32_t F, int32_t S,
                           int32_t row_bytes, const int8_t* head_kind_host, int32_t inverse,

@@ -298,6 +298,36 @@ tsr_status tsr_temporal_permute(const void *src, void *dst, int32_t B, int32_t H
                                 const int8_t *head_kind, int32_t inverse, void *stream);
 
 /*
+ * tsr_svg_route -- route each head to the spatial or the temporal SVG pattern
+ * from sampled queries (Sparse VideoGen digest, "Sparse VideoGen": heads are
+ * assigned to a spatial or a temporal sparse pattern on the fly; the pages give
+ * no criterion, this is the reading taken).
+ *
+ * For every (b, h) and every sampled query row i = samples[s] (tokens
+ * frame-major, t = f * frame_size + s), the head's attention output is
+ * computed under dense attention, the spatial pattern and the temporal pattern
+ * (with temporal_radius), and
+ *   stats[b][h][0] = sum_s |O_spatial(i)  - O_dense(i)|^2
+ *   stats[b][h][1] = sum_s |O_temporal(i) - O_dense(i)|^2
+ *   stats[b][h][2] = sum_s |O_dense(i)|^2
+ * head_kind[h] = TSR_HEAD_TEMPORAL iff sum_b stats[b][h][1] < sum_b stats[b][h][0],
+ * else TSR_HEAD_SPATIAL: usable as the head_kind of an SVG tsr_mask.
+ *
+ * q, k, v: device bf16 [B][H][n_frames * frame_size][d], d in {64, 128},
+ * 16-byte aligned.  samples: HOST int32 [n_samples], 1 <= n_samples <= 1024,
+ * each in [0, N) (the caller draws them; the same rows for every head).
+ * stats: device fp32 [B][H][3], 16-byte aligned; head_kind: device int8 [H].
+ * Both are written on `stream`.  fp32 arithmetic on CUDA cores; the sums are
+ * accumulated with atomics, so their last bits vary from run to run.
+ * Errors: TSR_ERR_INVALID_ARG for bad shapes, pointers or sample rows,
+ * TSR_ERR_UNSUPPORTED for more than 1024 samples or N above 2^24.
+ */
+tsr_status tsr_svg_route(const void *q, const void *k, const void *v, int32_t B, int32_t H,
+                         int32_t n_frames, int32_t frame_size, int32_t d, int32_t temporal_radius,
+                         const int32_t *samples, int32_t n_samples, float *stats,
+                         int8_t *head_kind, void *stream);
+
+/*
  * tsr_attention_host -- one whole call from HOST memory: copies the mask arrays
  * and Q, K, V to the device, plans, runs the forward and copies O and lse back,
  * then synchronises.  Every pointer in `mask` and q, k, v, out, lse are HOST

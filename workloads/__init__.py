@@ -224,27 +224,27 @@ def svg_mask(B: int = 1, H: int = 24, n_frames: int = 21, frame_size: int = 1560
 # --------------------------------------------------------------------------
 
 def svg_routing_heads(B: int, kinds, n_frames: int, frame_size: int, d: int, seed: int,
-                      contrast: float = 6.0, noise: float = 0.5):
+                      contrast: float = 12.0, noise: float = 0.5):
     """bf16 Q, K, V [B, H, N, d] (H = len(kinds)) whose heads are built to be
-    spatial (kinds[h] = 0: Q and K carry a one-hot code of the token's frame in
-    the first n_frames dimensions) or temporal (kinds[h] = 1: a one-hot code of
-    the spatial index modulo d - n_frames in the next dimensions), scaled by
-    ``contrast``, plus N(0, noise^2) in every dimension; V ~ N(0, 1).  Inputs for
-    routing tests only: which pattern a head follows is set here by design."""
+    spatial (kinds[h] = 0: Q and K carry a code of the token's frame) or
+    temporal (kinds[h] = 1: a code of the token's spatial index).  Codes are
+    seeded random unit vectors scaled by ``contrast``, so tokens sharing the
+    code score about contrast^2 / sqrt(d) above the rest; N(0, noise^2) is added
+    to every dimension of Q and K; V ~ N(0, 1).  Inputs for routing tests only:
+    which pattern a head follows is set here by design."""
     import torch
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
     kinds = np.asarray(kinds, dtype=np.int8)
     H, N = len(kinds), n_frames * frame_size
-    assert d > n_frames + 1
-    t = np.arange(N)
-    code = np.zeros((H, N, d), np.float32)
+    t = torch.arange(N)
+    codes = []
     for h in range(H):
-        if kinds[h] == 0:
-            code[h, t, t // frame_size] = contrast
-        else:
-            code[h, t, n_frames + (t % frame_size) % (d - n_frames)] = contrast
-    code = torch.from_numpy(code)[None].expand(B, H, N, d)
+        n_codes = n_frames if kinds[h] == 0 else frame_size
+        e = torch.randn((n_codes, d), generator=g)
+        e = contrast * e / e.norm(dim=1, keepdim=True)
+        codes.append(e[t // frame_size] if kinds[h] == 0 else e[t % frame_size])
+    code = torch.stack(codes)[None].expand(B, H, N, d)
     q = code + noise * torch.randn((B, H, N, d), generator=g)
     k = code + noise * torch.randn((B, H, N, d), generator=g)
     v = torch.randn((B, H, N, d), generator=g)
