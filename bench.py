@@ -453,6 +453,21 @@ def main():
                "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
                "ms_per_step": 1e3 * e2e_s}
 
+    route = None
+    if spec.kind == W.MASK_SVG:
+        # the step before the path: routing the heads from 64 sampled query rows
+        smp = np.sort(np.random.Generator(np.random.PCG64(64)).choice(spec.N, size=64,
+                                                                      replace=False))
+        for _ in range(2):
+            tsr.tsr_svg_route(qd, kd, vd, spec.n_frames, spec.frame_size, smp, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(5):
+            tsr.tsr_svg_route(qd, kd, vd, spec.n_frames, spec.frame_size, smp, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        route = {"samples": 64, "ms": a.elapsed_time(b) / 5, "timed": "separately, not in the step"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(spec, q, k, v)
@@ -475,6 +490,7 @@ def main():
                        "tiles": stats["n_entries"], "boundary_tiles": stats["n_boundary"],
                        "fill": pairs / computed if computed else None,
                        "forward_ms": fwd_avg, "plan_ms": ms_step - fwd_avg,
+                       **({"svg_route": route} if route else {}),
                        "forward_tflops": achieved,
                        "forward_frac_of_peak": achieved / peak},
             "pct_of_peak": 100.0 * value / peak,
