@@ -4,6 +4,7 @@
 // lookup table filled by offline profiling).
 #include <cstdio>
 #include <cstdlib>
+#include <array>
 #include <cstring>
 #include <fstream>
 #include <mutex>
@@ -267,20 +268,32 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
   return TSR_OK;
 }
 
-// Device buffers of tsr_attention_host, kept per thread and grown on demand.
+// Device buffers, streams, events and per-head-group plans of
+// tsr_attention_host, kept per thread and grown on demand.
 struct HostCache {
   void* buf[8] = {nullptr};
   size_t cap[8] = {0};
-  cudaStream_t stream = nullptr;
+  cudaStream_t stream = nullptr;               // attention
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_plan = nullptr;
+  std::vector<cudaEvent_t> ev;                 // 3 per head group: inputs, plan, attention
+  std::vector<tsr_plan_t> plans;               // one per head group
+  std::vector<std::array<int64_t, 9>> plan_key;
   int device = -1;
   void release() {
+    for (tsr_plan_t pl : plans) tsr_plan_destroy(pl);
+    plans.clear();
+    plan_key.clear();
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
     for (int i = 0; i < 8; ++i) {
       cudaFree(buf[i]);
       buf[i] = nullptr;
       cap[i] = 0;
     }
-    if (stream) cudaStreamDestroy(stream);
-    stream = nullptr;
+    for (cudaStream_t* s : {&stream, &s_in, &s_out, &s_plan}) {
+      if (*s) cudaStreamDestroy(*s);
+      *s = nullptr;
+    }
     device = -1;
   }
   ~HostCache() { release(); }
@@ -531,74 +544,168 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     hc.release();
     hc.device = dev;
   }
-  if (!hc.stream) TSR_CUDA(cudaStreamCreateWithFlags(&hc.stream, cudaStreamNonBlocking));
-  cudaStream_t st = hc.stream;
-  const size_t tb = static_cast<size_t>(mask->B) * mask->H * mask->N * mask->d * 2;
-  const size_t lb = static_cast<size_t>(mask->B) * mask->H * mask->N * 4;
+  for (cudaStream_t* st : {&hc.stream, &hc.s_in, &hc.s_out, &hc.s_plan})
+    if (!*st) TSR_CUDA(cudaStreamCreateWithFlags(st, cudaStreamNonBlocking));
+  const int64_t BH = static_cast<int64_t>(mask->B) * mask->H;
+  const size_t row_b = static_cast<size_t>(mask->N) * mask->d * 2;   // one head of Q, K, V or O
+  const size_t tb = BH * row_b;
+  const size_t lb = static_cast<size_t>(BH) * mask->N * 4;
+  // Heads are processed in groups of about 160 MB of Q, K and V: the inputs of
+  // group g + 1 are copied in while group g is attended and group g - 1 is
+  // copied out (three streams; the copy engines and the SMs overlap).
+  const int64_t n_groups = std::max<int64_t>(
+      1, std::min<int64_t>(BH, static_cast<int64_t>((3 * tb + (160u << 20) - 1) / (160u << 20))));
+  const int64_t per = (BH + n_groups - 1) / n_groups;
+  const int64_t G = (BH + per - 1) / per;
   void *dq, *dk, *dv, *dout, *dlse;
   if (tsr_status s = hc.get(0, tb, &dq)) return s;
   if (tsr_status s = hc.get(1, tb, &dk)) return s;
   if (tsr_status s = hc.get(2, tb, &dv)) return s;
   if (tsr_status s = hc.get(3, tb, &dout)) return s;
   if (tsr_status s = hc.get(4, lb, &dlse)) return s;
-  tsr_mask dm = *mask;
+  while (static_cast<int64_t>(hc.ev.size()) < 3 * G) {
+    cudaEvent_t e;
+    TSR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    hc.ev.push_back(e);
+  }
+  // 1. the mask to the device, and one mask view per head group
+  cudaStream_t sp = hc.s_plan;
+  std::vector<tsr_mask> views(G, *mask);
+  const int64_t nqb = (mask->kind == TSR_MASK_KEYLIST) ? (mask->N + mask->slice_m - 1) / mask->slice_m : 0;
   if (mask->kind == TSR_MASK_UNIFORM || mask->kind == TSR_MASK_SEGMENTS) {
-    size_t nb;
-    if (mask->kind == TSR_MASK_UNIFORM)
-      nb = static_cast<size_t>(mask->B) * mask->H * ((mask->N + mask->bq - 1) / mask->bq) *
-           ((mask->N + mask->bk - 1) / mask->bk);
-    else
-      nb = static_cast<size_t>(mask->B) * mask->H * mask->n_qseg * mask->n_kseg;
+    const int64_t per_head = (mask->kind == TSR_MASK_UNIFORM)
+                                 ? static_cast<int64_t>((mask->N + mask->bq - 1) / mask->bq) *
+                                       ((mask->N + mask->bk - 1) / mask->bk)
+                                 : static_cast<int64_t>(mask->n_qseg) * mask->n_kseg;
     void* db;
-    if (tsr_status s = hc.get(5, nb, &db)) return s;
-    TSR_CUDA(cudaMemcpyAsync(db, mask->blocks, nb, cudaMemcpyHostToDevice, st));
-    dm.blocks = static_cast<const uint8_t*>(db);
+    if (tsr_status s = hc.get(5, BH * per_head, &db)) return s;
+    TSR_CUDA(cudaMemcpyAsync(db, mask->blocks, BH * per_head, cudaMemcpyHostToDevice, sp));
+    const int32_t* qb = nullptr;
+    const int32_t* kb = nullptr;
     if (mask->kind == TSR_MASK_SEGMENTS) {
       void* dbnd;
       const size_t nq = mask->n_qseg + 1, nk = mask->n_kseg + 1;
       if (tsr_status s = hc.get(6, 4 * (nq + nk), &dbnd)) return s;
-      int32_t* p = static_cast<int32_t*>(dbnd);
-      TSR_CUDA(cudaMemcpyAsync(p, mask->q_bounds, 4 * nq, cudaMemcpyHostToDevice, st));
-      TSR_CUDA(cudaMemcpyAsync(p + nq, mask->k_bounds, 4 * nk, cudaMemcpyHostToDevice, st));
-      dm.q_bounds = p;
-      dm.k_bounds = p + nq;
+      int32_t* pb = static_cast<int32_t*>(dbnd);
+      TSR_CUDA(cudaMemcpyAsync(pb, mask->q_bounds, 4 * nq, cudaMemcpyHostToDevice, sp));
+      TSR_CUDA(cudaMemcpyAsync(pb + nq, mask->k_bounds, 4 * nk, cudaMemcpyHostToDevice, sp));
+      qb = pb;
+      kb = pb + nq;
+    }
+    for (int64_t g = 0; g < G; ++g) {
+      views[g].blocks = static_cast<const uint8_t*>(db) + g * per * per_head;
+      views[g].q_bounds = qb;
+      views[g].k_bounds = kb;
     }
   } else if (mask->kind == TSR_MASK_KEYLIST) {
-    const int64_t n_lists = static_cast<int64_t>(mask->B) * mask->H *
-                            ((mask->N + mask->slice_m - 1) / mask->slice_m);
-    const int64_t n_idx = mask->indptr[n_lists];   // HOST array here
-    if (n_idx < 0) return fail(TSR_ERR_INVALID_ARG, "indptr must not decrease");
+    const int64_t n_lists = BH * nqb;
+    const int64_t n_idx = mask->indptr[n_lists];   // HOST arrays here
+    if (n_idx < 0 || mask->indptr[0] != 0)
+      return fail(TSR_ERR_INVALID_ARG, "indptr must run upward from 0");
+    // each group's slice of indptr, rebased to start at 0
+    std::vector<int64_t> rebased;
+    rebased.reserve(n_lists + G);
+    std::vector<int64_t> start(G), base(G);
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t l0 = g * per * nqb, l1 = std::min(BH, (g + 1) * per) * nqb;
+      start[g] = static_cast<int64_t>(rebased.size());
+      base[g] = mask->indptr[l0];
+      for (int64_t l = l0; l <= l1; ++l) rebased.push_back(mask->indptr[l] - base[g]);
+    }
     void *dp, *di;
-    if (tsr_status s = hc.get(5, sizeof(int64_t) * (n_lists + 1), &dp)) return s;
+    if (tsr_status s = hc.get(5, sizeof(int64_t) * rebased.size(), &dp)) return s;
     if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &di)) return s;
-    TSR_CUDA(cudaMemcpyAsync(dp, mask->indptr, sizeof(int64_t) * (n_lists + 1),
-                             cudaMemcpyHostToDevice, st));
+    TSR_CUDA(cudaMemcpyAsync(dp, rebased.data(), sizeof(int64_t) * rebased.size(),
+                             cudaMemcpyHostToDevice, sp));
     if (n_idx)
-      TSR_CUDA(cudaMemcpyAsync(di, mask->indices, sizeof(int32_t) * n_idx, cudaMemcpyHostToDevice, st));
-    dm.indptr = static_cast<const int64_t*>(dp);
-    dm.indices = static_cast<const int32_t*>(di);
+      TSR_CUDA(cudaMemcpyAsync(di, mask->indices, sizeof(int32_t) * n_idx, cudaMemcpyHostToDevice, sp));
+    // the rebased copy must reach the device before the host vector goes away
+    TSR_CUDA(cudaStreamSynchronize(sp));
+    for (int64_t g = 0; g < G; ++g) {
+      views[g].indptr = static_cast<const int64_t*>(dp) + start[g];
+      views[g].indices = static_cast<const int32_t*>(di) + base[g];
+    }
   } else if (mask->kind == TSR_MASK_SVG) {
+    // head kinds of the flattened (b, h) order
+    std::vector<int8_t> kinds(BH);
+    for (int64_t i = 0; i < BH; ++i) kinds[i] = mask->head_kind[i % mask->H];
     void* dh;
-    if (tsr_status s = hc.get(7, mask->H, &dh)) return s;
-    TSR_CUDA(cudaMemcpyAsync(dh, mask->head_kind, mask->H, cudaMemcpyHostToDevice, st));
-    dm.head_kind = static_cast<const int8_t*>(dh);
+    if (tsr_status s = hc.get(7, BH, &dh)) return s;
+    TSR_CUDA(cudaMemcpyAsync(dh, kinds.data(), BH, cudaMemcpyHostToDevice, sp));
+    TSR_CUDA(cudaStreamSynchronize(sp));
+    for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + g * per;
   }
-  TSR_CUDA(cudaMemcpyAsync(dq, q, tb, cudaMemcpyHostToDevice, st));
-  TSR_CUDA(cudaMemcpyAsync(dk, k, tb, cudaMemcpyHostToDevice, st));
-  TSR_CUDA(cudaMemcpyAsync(dv, v, tb, cudaMemcpyHostToDevice, st));
-  tsr_plan_t plan = nullptr;
-  if (tsr_status s = tsr_plan(&dm, opts, &plan, st)) return s;
-  tsr_status s = tsr_bsa_forward(dq, dk, dv, plan, dout, static_cast<float*>(dlse), st);
-  if (s == TSR_OK) {
-    const cudaError_t e1 = cudaMemcpyAsync(out, dout, tb, cudaMemcpyDeviceToHost, st);
-    const cudaError_t e2 = cudaMemcpyAsync(lse, dlse, lb, cudaMemcpyDeviceToHost, st);
-    const cudaError_t e3 = cudaStreamSynchronize(st);
-    if (e1 != cudaSuccess) s = cuda_fail(e1, "copy of out to host");
-    else if (e2 != cudaSuccess) s = cuda_fail(e2, "copy of lse to host");
-    else if (e3 != cudaSuccess) s = cuda_fail(e3, "stream synchronize");
+  // 2. inputs, group by group (queued after the mask, which the copy engine
+  // would otherwise move only after every input)
+  const char* hq = static_cast<const char*>(q);
+  const char* hk = static_cast<const char*>(k);
+  const char* hv = static_cast<const char*>(v);
+  for (int64_t g = 0; g < G; ++g) {
+    const int64_t b0 = g * per, cnt = std::min(per, BH - b0);
+    const size_t off = b0 * row_b, n = cnt * row_b;
+    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dq) + off, hq + off, n, cudaMemcpyHostToDevice, hc.s_in));
+    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dk) + off, hk + off, n, cudaMemcpyHostToDevice, hc.s_in));
+    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dv) + off, hv + off, n, cudaMemcpyHostToDevice, hc.s_in));
+    TSR_CUDA(cudaEventRecord(hc.ev[3 * g], hc.s_in));
   }
-  if (s == TSR_OK) s = tsr_plan_device_status(plan, st);
-  tsr_plan_destroy(plan);
+  // 3. one plan per head group, kept from call to call while the grouping and
+  // options are unchanged (re-planned for the new mask)
+  const tsr_plan_opts zero{};
+  const tsr_plan_opts& o = opts ? *opts : zero;
+  if (static_cast<int64_t>(hc.plans.size()) != G) {
+    for (tsr_plan_t pl : hc.plans) tsr_plan_destroy(pl);
+    hc.plans.assign(G, nullptr);
+    hc.plan_key.assign(G, {});
+  }
+  for (int64_t g = 0; g < G; ++g) {
+    tsr_mask& vw = views[g];
+    vw.B = 1;
+    vw.H = static_cast<int32_t>(std::min(per, BH - g * per));
+    const std::array<int64_t, 9> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
+                                         o.flags, opts ? 1 : 0};
+    tsr_status s = TSR_OK;
+    if (hc.plans[g] && hc.plan_key[g] == key) {
+      s = tsr_plan_update(hc.plans[g], &vw, sp);
+    } else {
+      if (hc.plans[g]) tsr_plan_destroy(hc.plans[g]);
+      hc.plans[g] = nullptr;
+      s = tsr_plan(&vw, opts, &hc.plans[g], sp);
+      hc.plan_key[g] = key;
+    }
+    if (s != TSR_OK) {
+      // no copy may still read the caller's buffers after the return
+      cudaStreamSynchronize(hc.s_in);
+      cudaStreamSynchronize(sp);
+      return s;
+    }
+    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 1], sp));
+  }
+  // 4. attention per group once its inputs and plan are ready; 5. outputs back
+  tsr_status s = TSR_OK;
+  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+    const int64_t b0 = g * per;
+    const size_t off = b0 * row_b, n = std::min(per, BH - b0) * row_b;
+    TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g], 0));
+    TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g + 1], 0));
+    s = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
+                        static_cast<char*>(dv) + off, hc.plans[g], static_cast<char*>(dout) + off,
+                        static_cast<float*>(dlse) + b0 * mask->N, hc.stream);
+    if (s != TSR_OK) break;
+    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], hc.stream));
+    TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
+    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
+                             cudaMemcpyDeviceToHost, hc.s_out));
+    TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
+                             static_cast<size_t>(n / row_b) * mask->N * 4, cudaMemcpyDeviceToHost,
+                             hc.s_out));
+  }
+  const cudaError_t e1 = cudaStreamSynchronize(hc.s_out);
+  const cudaError_t e2 = cudaStreamSynchronize(hc.stream);
+  const cudaError_t e3 = cudaStreamSynchronize(hc.s_in);
+  if (s == TSR_OK && e1 != cudaSuccess) s = cuda_fail(e1, "copy of the outputs to host");
+  if (s == TSR_OK && e2 != cudaSuccess) s = cuda_fail(e2, "attention stream");
+  if (s == TSR_OK && e3 != cudaSuccess) s = cuda_fail(e3, "copy of the inputs");
+  for (int64_t g = 0; g < G && s == TSR_OK; ++g) s = tsr_plan_device_status(hc.plans[g], hc.stream);
   return s;
 }
 

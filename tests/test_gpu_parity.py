@@ -402,6 +402,34 @@ def test_host_entry_point_keylist():
     assert np.array_equal(lse.double().numpy(), L)
 
 
+@pytest.mark.parametrize("which", ["uniform", "svg", "keylist"])
+def test_host_entry_point_in_head_groups(which):
+    """Inputs above 160 MB are moved and attended in head groups on three
+    streams; with the regime forced the result is bit-identical to one device
+    call over all heads.  The SVG case has B = 3, H = 3, so a group spans two
+    batches and its head kinds come from the flattened (b, h) order; the
+    key-list case rebases each group's slice of indptr."""
+    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
+    if which == "uniform":
+        spec = W.video_block_mask(seed=5, H=8)
+        kw = dict(bq=64, bk=64, blocks=spec.blocks)
+    elif which == "svg":
+        spec = W.svg_mask(3, 3, n_frames=21, frame_size=1560, kinds=np.array([1, 0, 1], np.int8))
+        kw = dict(n_frames=21, frame_size=1560, head_kind=spec.head_kind)
+    else:
+        spec = W.keylist_mask(seed=6, H=4)
+        kw = dict(slice_m=64, indptr=spec.indptr, indices=spec.indices)
+    q, k, v = W.qkv(spec.B, spec.H, spec.N, 128, 17)
+    _, _, O, L = run(spec, 128, seed=0, opts=opts, qkv=(q, k, v))
+    out = torch.empty_like(q).pin_memory()
+    lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32).pin_memory()
+    for _ in range(2):      # the second call reuses the cached group plans
+        tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, 128, q.pin_memory(),
+                               k.pin_memory(), v.pin_memory(), out, lse, opts=opts, **kw)
+        assert np.array_equal(out.float().numpy(), O)
+        assert np.array_equal(lse.double().numpy(), L)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """Failure detection without a GPU fault: with the test-only stall flag the
     MMA issuer waits on a barrier nothing signals; the kernel gives up after its
