@@ -23,7 +23,8 @@ from . import _build
 __all__ = [
     "TsrError", "build", "lib", "make_mask", "Mask", "Plan", "tsr_plan", "tsr_plan_update",
     "tsr_bsa_forward",
-    "tsr_plan_device_status", "tsr_temporal_permute", "tsr_svg_route", "tsr_attention_host",
+    "tsr_bsa_forward_batch", "tsr_plan_device_status", "tsr_temporal_permute", "tsr_svg_route",
+    "tsr_attention_host",
     "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
     "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL",
@@ -59,6 +60,11 @@ class _Mask(ctypes.Structure):
     ]
 
 
+class _Request(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("plan", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
 class _Opts(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("flags", ctypes.c_int32),
@@ -82,7 +88,7 @@ class _Regime(ctypes.Structure):
 
 _LIB = None
 EXPORTS = ("tsr_abi_version", "tsr_status_string", "tsr_last_error", "tsr_plan", "tsr_plan_update",
-           "tsr_bsa_forward", "tsr_plan_device_status", "tsr_plan_destroy", "tsr_plan_get_stats",
+           "tsr_bsa_forward", "tsr_bsa_forward_batch", "tsr_plan_device_status", "tsr_plan_destroy", "tsr_plan_get_stats",
            "tsr_plan_export", "tsr_temporal_permute", "tsr_svg_route", "tsr_attention_host",
            "tsr_release_host_buffers", "tsr_regime_load", "tsr_regime_lookup")
 
@@ -113,6 +119,7 @@ def lib():
         "tsr_plan": ([P, P, P, P], ctypes.c_int),
         "tsr_plan_update": ([P, P, P], ctypes.c_int),
         "tsr_bsa_forward": ([P, P, P, P, P, P, P], ctypes.c_int),
+        "tsr_bsa_forward_batch": ([P, I32, P], ctypes.c_int),
         "tsr_plan_device_status": ([P, P], ctypes.c_int),
         "tsr_plan_destroy": ([P], ctypes.c_int),
         "tsr_plan_get_stats": ([P, P], ctypes.c_int),
@@ -284,6 +291,26 @@ def tsr_temporal_permute(src: torch.Tensor, dst: torch.Tensor, n_frames: int, fr
     _check(lib().tsr_temporal_permute(_dptr(src), _dptr(dst), B, H, n_frames, frame_size,
                                       row_bytes, hk, 1 if inverse else 0, _stream_ptr(stream)))
     return dst
+
+
+def tsr_bsa_forward_batch(requests, stream=None):
+    """Several requests in one launch (see include/tsr.h).  ``requests``: a
+    sequence of (q, k, v, plan) or (q, k, v, plan, out, lse); returns the list
+    of (out, lse)."""
+    n = len(requests)
+    arr = (_Request * max(1, n))()
+    outs = []
+    for i, rq in enumerate(requests):
+        q, k, v, plan = rq[:4]
+        out = rq[4] if len(rq) > 4 and rq[4] is not None else torch.empty_like(q)
+        lse = (rq[5] if len(rq) > 5 and rq[5] is not None else
+               torch.empty(q.shape[:3], dtype=torch.float32, device=q.device))
+        arr[i].q, arr[i].k, arr[i].v = _dptr(q), _dptr(k), _dptr(v)
+        arr[i].plan = plan.handle
+        arr[i].out, arr[i].lse = _dptr(out), _dptr(lse)
+        outs.append((out, lse))
+    _check(lib().tsr_bsa_forward_batch(ctypes.cast(arr, ctypes.c_void_p), n, _stream_ptr(stream)))
+    return outs
 
 
 def tsr_svg_route(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_frames: int,

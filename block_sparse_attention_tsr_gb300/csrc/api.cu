@@ -423,6 +423,34 @@ tsr_status tsr_bsa_forward(const void* q, const void* k, const void* v, tsr_plan
   return TSR_OK;
 }
 
+tsr_status tsr_bsa_forward_batch(const tsr_request* reqs, int32_t n, void* stream) {
+  set_error("");
+  if (!reqs || n < 1 || n > 16) return fail(TSR_ERR_INVALID_ARG, "1 to 16 requests per call");
+  int dev = 0;
+  TSR_CUDA(cudaGetDevice(&dev));
+  FwdArgs a[16];
+  for (int32_t r = 0; r < n; ++r) {
+    const tsr_request& q = reqs[r];
+    const std::string at = "request " + std::to_string(r) + ": ";
+    if (!q.plan) return fail(TSR_ERR_INVALID_ARG, at + "plan is NULL");
+    if (!q.q || !q.k || !q.v || !q.out || !q.lse)
+      return fail(TSR_ERR_INVALID_ARG, at + "NULL tensor pointer");
+    if (!aligned16(q.q) || !aligned16(q.k) || !aligned16(q.v) || !aligned16(q.out) ||
+        !aligned16(q.lse))
+      return fail(TSR_ERR_INVALID_ARG, at + "tensor pointers must be 16-byte aligned");
+    if (q.out == q.q || q.out == q.k || q.out == q.v)
+      return fail(TSR_ERR_INVALID_ARG, at + "out aliases an input");
+    if (dev != q.plan->device) return fail(TSR_ERR_INVALID_ARG, at + "plan was made on another device");
+    for (int32_t s2 = 0; s2 < r; ++s2)
+      if (reqs[s2].plan == q.plan)
+        return fail(TSR_ERR_INVALID_ARG, at + "a plan may appear once per batch");
+    a[r] = FwdArgs{q.q, q.k, q.v, q.out, q.lse, q.plan};
+  }
+  if (tsr_status e = launch_forward_batch(a, n, static_cast<cudaStream_t>(stream))) return e;
+  if (reqs[0].plan->flags & TSR_PLAN_SYNC_CHECK) return tsr_plan_device_status(reqs[0].plan, stream);
+  return TSR_OK;
+}
+
 tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   if (!plan || !s) return fail(TSR_ERR_INVALID_ARG, "NULL argument");
   memset(s, 0, sizeof *s);

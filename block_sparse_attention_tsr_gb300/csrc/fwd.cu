@@ -6,6 +6,8 @@
 
 #include <cmath>
 #include <cstring>
+#include <memory>
+#include <new>
 #include <string>
 
 #include "fwd_kernel.cuh"
@@ -80,52 +82,94 @@ bool variant_pick(int d, bool gathered, int bn, int stages, int ctas, int* out_b
 }
 
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream) {
-  const tsr_plan_impl* P = a.plan;
-  if (P->n_items == 0) return TSR_OK;
-  FwdParams prm;
-  memset(&prm, 0, sizeof prm);
-  const uint64_t D = P->d, N = P->N, BH = static_cast<uint64_t>(P->B) * P->H;
-  bool ok = encode_tmap_3d(&prm.tq, a.q, D, N, BH, 64, kBM) &&
-            encode_tmap_3d(&prm.tk, a.k, D, N, BH, 64, P->bn) &&
-            encode_tmap_3d(&prm.tv, a.v, D, N, BH, 64, P->bn);
-  if (!ok) return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
-  prm.items = static_cast<const int4*>(P->items);
-  prm.entries = static_cast<const int2*>(P->entries);
-  prm.descs = static_cast<const uint4*>(P->descs);
-  prm.out = static_cast<__nv_bfloat16*>(a.out);
-  prm.lse = a.lse;
-  prm.counter = P->counter;
-  prm.err = P->err;
-  prm.n_items = static_cast<int32_t>(P->n_items);
-  prm.N = P->N;
-  prm.F = P->F;
-  prm.S = P->S;
-  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P->d)));
-  prm.qg = static_cast<const __nv_bfloat16*>(a.q);
-  prm.kg = static_cast<const __nv_bfloat16*>(a.k);
-  prm.vg = static_cast<const __nv_bfloat16*>(a.v);
-  prm.gidx = P->gidx;
-  prm.slice_m = P->slice_m;
-  prm.test_stall = (P->flags & TSR_PLAN_TEST_STALL) ? 1 : 0;
-  prm.timeout_ns = prm.test_stall ? 100000000ull : kWaitTimeoutNs;
-  TSR_CUDA(cudaMemsetAsync(P->counter, 0, sizeof(int32_t), stream));
-  const int n = static_cast<int>(P->n_items), dev = P->device;
-  const int key = vkey(P->d, P->bn, P->stages, P->ctas);
+  return launch_forward_batch(&a, 1, stream);
+}
+
+tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t stream) {
+  if (n_req < 1 || n_req > fwd::kMaxBatch)
+    return fail(TSR_ERR_INVALID_ARG, "1 to " + std::to_string(fwd::kMaxBatch) + " requests per call");
+  const tsr_plan_impl* P0 = reqs[0].plan;
+  // one launch needs one kernel variant: the same head dimension, regime and
+  // gather mode for every request; temporal heads anywhere select the variant
+  // that may gather through the permutation
+  bool temporal = false;
+  for (int r = 0; r < n_req; ++r) {
+    const tsr_plan_impl* P = reqs[r].plan;
+    if (P->device != P0->device || P->d != P0->d || P->bn != P0->bn || P->stages != P0->stages ||
+        P->ctas != P0->ctas || P->gathered != P0->gathered)
+      return fail(TSR_ERR_UNSUPPORTED,
+                  "requests of one batch need the same d, regime (bn, stages, ctas) and mask "
+                  "family (key lists or not); plan them with the same tsr_plan_opts");
+    temporal = temporal || P->n_temporal > 0;
+  }
+  const int key = vkey(P0->d, P0->bn, P0->stages, P0->ctas);
+  auto fill = [&](auto& prm) -> tsr_status {
+    memset(&prm, 0, sizeof prm);
+    int64_t total = 0;
+    for (int r = 0; r < n_req; ++r) {
+      const FwdArgs& a = reqs[r];
+      const tsr_plan_impl* P = a.plan;
+      fwd::ReqParams& q = prm.req[r];
+      const uint64_t D = P->d, N = P->N, BH = static_cast<uint64_t>(P->B) * P->H;
+      const bool ok = encode_tmap_3d(&q.tq, a.q, D, N, BH, 64, kBM) &&
+                      encode_tmap_3d(&q.tk, a.k, D, N, BH, 64, P->bn) &&
+                      encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, P->bn);
+      if (!ok)
+        return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
+      q.items = static_cast<const int4*>(P->items);
+      q.entries = static_cast<const int2*>(P->entries);
+      q.descs = static_cast<const uint4*>(P->descs);
+      q.out = static_cast<__nv_bfloat16*>(a.out);
+      q.lse = a.lse;
+      q.qg = static_cast<const __nv_bfloat16*>(a.q);
+      q.kg = static_cast<const __nv_bfloat16*>(a.k);
+      q.vg = static_cast<const __nv_bfloat16*>(a.v);
+      q.gidx = P->gidx;
+      q.item_begin = static_cast<int32_t>(total);
+      q.N = P->N;
+      q.F = P->F;
+      q.S = P->S;
+      q.slice_m = P->slice_m;
+      total += P->n_items;
+    }
+    if (total >= (int64_t{1} << 31)) return fail(TSR_ERR_UNSUPPORTED, "more than 2^31 work items");
+    prm.n_req = n_req;
+    prm.n_items = static_cast<int32_t>(total);
+    prm.counter = P0->counter;
+    prm.err = P0->err;
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P0->d)));
+    prm.test_stall = (P0->flags & TSR_PLAN_TEST_STALL) ? 1 : 0;
+    prm.timeout_ns = prm.test_stall ? 100000000ull : kWaitTimeoutNs;
+    return TSR_OK;
+  };
   // KEYLIST plans gather K / V by key list; plans with temporal-major heads take
   // the variant that may gather through the permutation; the rest are TMA only.
+  auto launch = [&](const auto& prm) -> tsr_status {
+    if (prm.n_items == 0) return TSR_OK;
+    TSR_CUDA(cudaMemsetAsync(P0->counter, 0, sizeof(int32_t), stream));
+    const int n = prm.n_items, dev = P0->device;
+    if (P0->gathered) return fwd::launch_mode_list(prm, key, n, dev, stream);
+    if (temporal) return fwd::launch_mode_perm(prm, key, n, dev, stream);
+    return fwd::launch_mode_tma(prm, key, n, dev, stream);
+  };
   tsr_status st;
-  if (P->gathered)
-    st = fwd::launch_mode_list(prm, key, n, dev, stream);
-  else if (P->n_temporal > 0)
-    st = fwd::launch_mode_perm(prm, key, n, dev, stream);
-  else
-    st = fwd::launch_mode_tma(prm, key, n, dev, stream);
+  if (n_req == 1) {
+    FwdParams prm;
+    if (tsr_status e = fill(prm)) return e;
+    st = launch(prm);
+  } else {
+    std::unique_ptr<fwd::FwdParamsBatch> prm(new (std::nothrow) fwd::FwdParamsBatch);
+    if (!prm) return fail(TSR_ERR_OOM, "host allocation failed");
+    if (tsr_status e = fill(*prm)) return e;
+    st = launch(*prm);
+  }
   if (st != TSR_ERR_UNSUPPORTED) return st;
-  return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P->d) + " bn=" +
-                                       std::to_string(P->bn) + " stages=" +
-                                       std::to_string(P->stages) + " ctas=" +
-                                       std::to_string(P->ctas) +
-                                       (P->gathered ? " (gathered)" : ""));
+  return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P0->d) + " bn=" +
+                                       std::to_string(P0->bn) + " stages=" +
+                                       std::to_string(P0->stages) + " ctas=" +
+                                       std::to_string(P0->ctas) +
+                                       (P0->gathered ? " (gathered)" : "") +
+                                       (n_req > 1 ? " in batched launches" : ""));
 }
 
 }  // namespace tsr

@@ -49,27 +49,56 @@ namespace fwd {
 //   kModeList  K / V rows gathered from a key list (KEYLIST)
 enum : int { kModeTma = 0, kModePerm = 1, kModeList = 2 };
 
-struct FwdParams {
+// One attention request: its tensors and its tile plan.  A launch covers one
+// request (tsr_bsa_forward) or up to kMaxBatch requests of possibly different
+// shapes (tsr_bsa_forward_batch); their work items are numbered one after the
+// other, request r's from req[r].item_begin.
+constexpr int kMaxBatch = 16;
+
+struct ReqParams {
   CUtensorMap tq, tk, tv;        // caller layout, 3-D {d, N, B*H}
   const int4* items;             // tsr_plan_item, 2 x int4 each
   const int2* entries;
   const uint4* descs;            // 32 B each
   __nv_bfloat16* out;
   float* lse;
-  int32_t* counter;
-  uint32_t* err;
-  int32_t n_items, N, F, S;
-  float scale_log2;              // log2(e) / sqrt(d)
   // rows loaded by index: KEYLIST keys named by gidx, and every row of a
   // temporal-major (SVG temporal) item
   const __nv_bfloat16* qg;
   const __nv_bfloat16* kg;
   const __nv_bfloat16* vg;
   const int32_t* gidx;
-  int32_t slice_m;
+  int32_t item_begin, N, F, S, slice_m;
+};
+
+// Launch parameters for up to MAXR requests: MAXR = 1 for tsr_bsa_forward
+// (the request index is then a constant), kMaxBatch for batched launches.
+template <int MAXR>
+struct FwdParamsT {
+  int32_t* counter;
+  uint32_t* err;
+  int32_t n_items;               // over all requests
+  int32_t n_req;
+  float scale_log2;              // log2(e) / sqrt(d)
   int32_t test_stall;           // test only: the MMA issuer waits on a barrier nobody signals
   uint64_t timeout_ns;          // bound of every wait
+  ReqParams req[MAXR];
 };
+using FwdParams = FwdParamsT<1>;
+using FwdParamsBatch = FwdParamsT<kMaxBatch>;
+
+// The request holding work item `it` (requests are few: a linear scan).
+template <int MAXR>
+__device__ __forceinline__ int req_of(const FwdParamsT<MAXR>& p, int32_t it) {
+  if constexpr (MAXR == 1) {
+    return 0;
+  } else {
+    int r = 0;
+    for (int i = 1; i < p.n_req; ++i)
+      if (it >= p.req[i].item_begin) r = i;
+    return r;
+  }
+}
 
 // Rescale the running output only when the running maximum grew by more than
 // this many powers of two: P = 2^(x - m_ref) then stays below 2^8, far inside
@@ -193,8 +222,8 @@ __device__ __forceinline__ void gather_tile(const __nv_bfloat16* head_base,
   }
 }
 
-template <int D, int BN, int STAGES, int CTAS, int MODE>
-__global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
+template <int D, int BN, int STAGES, int CTAS, int MODE, int MAXR>
+__global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constant__ FwdParamsT<MAXR> p) {
   using C = Cfg<D, BN, STAGES, CTAS>;
   constexpr bool GATHER = MODE == kModeList;   // K / V rows named by a key list
   constexpr bool PERM = MODE == kModePerm;     // items may be temporal-major
@@ -245,9 +274,9 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.tq);
-      tma_prefetch_desc(&p.tk);
-      tma_prefetch_desc(&p.tv);
+      tma_prefetch_desc(&p.req[0].tq);
+      tma_prefetch_desc(&p.req[0].tk);
+      tma_prefetch_desc(&p.req[0].tv);
     }
     uint32_t item_seq = 0, kv_cnt = 0, q_cnt = 0, k_iss = 0, v_iss = 0;
     bool ok = true;
@@ -279,22 +308,24 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       }
       ++item_seq;
       if (done) break;
-      const int4 i0 = __ldg(&p.items[2 * it]);
-      const int4 i1 = __ldg(&p.items[2 * it + 1]);
+      const ReqParams& rq = p.req[req_of(p, it)];
+      const int32_t li = it - rq.item_begin;
+      const int4 i0 = __ldg(&rq.items[2 * li]);
+      const int4 i1 = __ldg(&rq.items[2 * li + 1]);
       const int32_t bh = i0.x, q_tile = i0.y, begin = i0.z, end = i0.w, layout = i1.x;
       if (end <= begin) continue;
-      const size_t head_off = static_cast<size_t>(bh) * p.N * D;
+      const size_t head_off = static_cast<size_t>(bh) * rq.N * D;
       const bool perm = PERM && layout != 0;
       // source row of a temporal-major row t' (rows past N read row 0; masked)
-      auto perm_row = [&](int32_t tp) -> int32_t { return tp < p.N ? unpermute(tp, p.F, p.S) : 0; };
+      auto perm_row = [&](int32_t tp) -> int32_t { return tp < rq.N ? unpermute(tp, rq.F, rq.S) : 0; };
       if (!wait_free(smem_u32(&ctrl.q_empty), (q_cnt & 1) ^ 1)) break;
       if (perm) {
         int32_t rows[C::BM / 32];
 #pragma unroll
         for (int m = 0; m < C::BM / 32; ++m) rows[m] = perm_row(q_tile * C::BM + 32 * m + lane);
-        gather_tile<D, C::BM, false>(p.qg + head_off, rows, sQ, smem_u32(&ctrl.q_full), lane);
+        gather_tile<D, C::BM, false>(rq.qg + head_off, rows, sQ, smem_u32(&ctrl.q_full), lane);
       } else {
-        tma_tile(&p.tq, sQ, smem_u32(&ctrl.q_full), q_tile * C::BM, C::BM, C::Q_BYTES, bh);
+        tma_tile(&rq.tq, sQ, smem_u32(&ctrl.q_full), q_tile * C::BM, C::BM, C::Q_BYTES, bh);
       }
       ++q_cnt;
       // Where tile e's rows come from: its first key row (TMA, temporal-major),
@@ -306,10 +337,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       auto tile_src = [&](int32_t e, int32_t (&rows)[BN / 32]) -> int32_t {
         if constexpr (GATHER) {
 #pragma unroll
-          for (int m = 0; m < BN / 32; ++m) rows[m] = __ldg(p.gidx + e * BN + 32 * m + lane);
+          for (int m = 0; m < BN / 32; ++m) rows[m] = __ldg(rq.gidx + e * BN + 32 * m + lane);
           return e * BN;
         } else {
-          return __ldg(&p.entries[e]).x;
+          return __ldg(&rq.entries[e]).x;
         }
       };
       // one K or V tile into stage buffer dst
@@ -343,7 +374,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             break;
           }
           if (!GATHER) kv_k = tile_src(begin + i, rows_k);
-          load_kv(&p.tk, p.kg, kv_k, rows_k, sK0 + s * C::KV_BYTES, smem_u32(&ctrl.k_full[s]));
+          load_kv(&rq.tk, rq.kg, kv_k, rows_k, sK0 + s * C::KV_BYTES, smem_u32(&ctrl.k_full[s]));
           ++k_iss;
         }
         if (i >= 1) {
@@ -354,7 +385,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             break;
           }
           if (!GATHER) kv_v = tile_src(begin + i - 1, rows_v);
-          load_kv(&p.tv, p.vg, kv_v, rows_v, sV0 + s * C::KV_BYTES, smem_u32(&ctrl.v_full[s]));
+          load_kv(&rq.tv, rq.vg, kv_v, rows_v, sV0 + s * C::KV_BYTES, smem_u32(&ctrl.v_full[s]));
           ++v_iss;
         }
         kv_v = kv_k;
@@ -393,12 +424,14 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
         ++item_seq;
         if (it < 0) break;
-        const int4 i0 = __ldg(&p.items[2 * it]);
+        const ReqParams& rq = p.req[req_of(p, it)];
+        const int32_t li = it - rq.item_begin;
+        const int4 i0 = __ldg(&rq.items[2 * li]);
         const int32_t n = i0.w - i0.z;
         if (n <= 0) continue;
         // tiles written by cp.async (generic proxy) are read by the tensor core
         // (async proxy): a proxy fence follows each of their full-barrier waits
-        const bool gathered = GATHER || (PERM && __ldg(&p.items[2 * it + 1]).x != 0);
+        const bool gathered = GATHER || (PERM && __ldg(&rq.items[2 * li + 1]).x != 0);
         if (!mbar_wait(smem_u32(&ctrl.q_full), q_cnt & 1, abort_flag, p.err, p.timeout_ns)) break;
         ++q_cnt;
         if (gathered) fence_proxy_async_smem();
@@ -494,8 +527,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(smem_u32(&ctrl.item_empty[slot]));
       ++item_seq;
       if (it < 0) break;
-      const int4 i0 = __ldg(&p.items[2 * it]);
-      const int4 i1 = __ldg(&p.items[2 * it + 1]);
+      const ReqParams& rq = p.req[req_of(p, it)];
+      const int32_t li = it - rq.item_begin;
+      const int4 i0 = __ldg(&rq.items[2 * li]);
+      const int4 i1 = __ldg(&rq.items[2 * li + 1]);
       const int32_t bh = i0.x, q_tile = i0.y, begin = i0.z, n = i0.w - i0.z, layout = i1.x;
       float m_ref = -INFINITY, l = 0.f;
       // The tile entry and its boundary descriptor are fetched one tile ahead so
@@ -503,10 +538,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       int32_t desc_next = -1;
       uint4 dn0 = make_uint4(0u, 0u, 0u, 0u), dn1 = dn0;
       if (n > 0) {
-        desc_next = __ldg(&p.entries[begin]).y;
+        desc_next = __ldg(&rq.entries[begin]).y;
         if (desc_next >= 0) {
-          dn0 = __ldg(&p.descs[2 * desc_next]);
-          dn1 = __ldg(&p.descs[2 * desc_next + 1]);
+          dn0 = __ldg(&rq.descs[2 * desc_next]);
+          dn1 = __ldg(&rq.descs[2 * desc_next + 1]);
         }
       }
       for (int32_t j = 0; j < n; ++j) {
@@ -515,10 +550,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         const int32_t desc = desc_next;
         const uint4 d0 = dn0, d1 = dn1;
         if (j + 1 < n) {
-          desc_next = __ldg(&p.entries[begin + j + 1]).y;
+          desc_next = __ldg(&rq.entries[begin + j + 1]).y;
           if (desc_next >= 0) {
-            dn0 = __ldg(&p.descs[2 * desc_next]);
-            dn1 = __ldg(&p.descs[2 * desc_next + 1]);
+            dn0 = __ldg(&rq.descs[2 * desc_next]);
+            dn1 = __ldg(&rq.descs[2 * desc_next + 1]);
           }
         }
         if (!mbar_wait(smem_u32(&ctrl.s_full[sb]), (t >> 1) & 1, abort_flag, p.err, p.timeout_ns)) {
@@ -541,7 +576,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         bool row_dead = false;
         if (GATHER && desc >= 0) {
           // list form: one BN-bit column mask per slice_m-row segment
-          const bool hi = (p.slice_m == 64) && (r >= 64);
+          const bool hi = (rq.slice_m == 64) && (r >= 64);
           const uint32_t w4[4] = {hi ? d1.x : d0.x, hi ? d1.y : d0.y, hi ? d1.z : d0.z,
                                   hi ? d1.w : d0.w};
           uint32_t any = 0u, all = 0xFFFFFFFFu;
@@ -680,9 +715,9 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       t_cnt += n;
       // ----------------------------------------------------------- epilogue
       const int32_t gr = q_tile * kBM + r;
-      const bool valid = gr < p.N;
-      const int32_t orow = (PERM && layout) ? unpermute(gr, p.F, p.S) : gr;
-      const size_t obase = (static_cast<size_t>(bh) * p.N + (valid ? orow : 0)) * D;
+      const bool valid = gr < rq.N;
+      const int32_t orow = (PERM && layout) ? unpermute(gr, rq.F, rq.S) : gr;
+      const size_t obase = (static_cast<size_t>(bh) * rq.N + (valid ? orow : 0)) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       if (n > 0) {
         // o_full completes once per non-empty item, after its last PV; the next
@@ -701,7 +736,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
             for (int i = 0; i < 16; ++i)
               pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
                                   __uint_as_float(rr[2 * i + 1]) * inv_l);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + obase + c0);
+            uint4* dst = reinterpret_cast<uint4*>(rq.out + obase + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -711,12 +746,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctrl.o_empty));
       } else if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + obase);
+        uint4* dst = reinterpret_cast<uint4*>(rq.out + obase);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       }
       if (valid)
-        p.lse[static_cast<size_t>(bh) * p.N + orow] =
+        rq.lse[static_cast<size_t>(bh) * rq.N + orow] =
             (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
@@ -729,10 +764,10 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
   }
 }
 
-template <int D, int BN, int STAGES, int CTAS, int MODE>
-tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStream_t stream) {
+template <int D, int BN, int STAGES, int CTAS, int MODE, int MAXR>
+tsr_status launch_variant(const FwdParamsT<MAXR>& prm, int n_items, int device, cudaStream_t stream) {
   using C = Cfg<D, BN, STAGES, CTAS>;
-  auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS, MODE>;
+  auto kern = bsa_fwd_kernel<D, BN, STAGES, CTAS, MODE, MAXR>;
   static bool attr_set[64] = {false};
   if (device < 0 || device >= 64 || !attr_set[device]) {
     TSR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
@@ -752,6 +787,9 @@ tsr_status launch_variant(const FwdParams& prm, int n_items, int device, cudaStr
   X(128, 128, 3, 1) X(128, 128, 2, 1) X(128, 64, 4, 1) X(128, 64, 2, 2) \
   X(64, 128, 4, 1) X(64, 64, 4, 1) X(64, 64, 3, 2)
 #define TSR_VARIANTS_GATHERED(X) X(128, 128, 3, 1) X(128, 64, 2, 2) X(64, 128, 4, 1) X(64, 64, 3, 2)
+// Variants also compiled for batched launches (the table's choices at long
+// sequences), in every mode.
+#define TSR_VARIANTS_BATCH(X) X(128, 64, 2, 2) X(64, 64, 3, 2)
 
 constexpr int vkey(int d, int bn, int stages, int ctas) {
   return d * 100000 + bn * 100 + stages * 10 + ctas;
@@ -763,6 +801,12 @@ constexpr int vkey(int d, int bn, int stages, int ctas) {
 tsr_status launch_mode_tma(const FwdParams& prm, int key, int n_items, int device, cudaStream_t stream);
 tsr_status launch_mode_perm(const FwdParams& prm, int key, int n_items, int device, cudaStream_t stream);
 tsr_status launch_mode_list(const FwdParams& prm, int key, int n_items, int device, cudaStream_t stream);
+tsr_status launch_mode_tma(const FwdParamsBatch& prm, int key, int n_items, int device,
+                           cudaStream_t stream);
+tsr_status launch_mode_perm(const FwdParamsBatch& prm, int key, int n_items, int device,
+                            cudaStream_t stream);
+tsr_status launch_mode_list(const FwdParamsBatch& prm, int key, int n_items, int device,
+                            cudaStream_t stream);
 
 }  // namespace fwd
 }  // namespace tsr

@@ -108,6 +108,8 @@ struct FwdArgs {
   const tsr_plan_impl* plan;
 };
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream);
+// Up to 16 requests in one launch (same d, regime and mask family).
+tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t stream);
 bool variant_exists(int d, int bn, int stages, int ctas, bool gathered);
 bool variant_pick(int d, bool gathered, int bn, int stages, int ctas, int* out_bn, int* out_st,
                   int* out_ct);

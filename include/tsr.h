@@ -204,6 +204,31 @@ tsr_status tsr_plan_update(tsr_plan_t plan, const tsr_mask *mask, void *stream);
 tsr_status tsr_bsa_forward(const void *q, const void *k, const void *v, tsr_plan_t plan,
                            void *out, float *lse, void *stream);
 
+/*
+ * tsr_bsa_forward_batch -- several BSA requests of possibly different shapes
+ * (B, H, N, mask) in ONE persistent launch (Tessera abstract: speedups are
+ * counted per BSA request; a serving step holds several).  Each request is
+ * what tsr_bsa_forward takes: device q, k, v, out (bf16 [B][H][N][d]), lse
+ * (fp32 [B][H][N]) and its own plan; the work items of all requests share one
+ * scheduler, request after request, each request's longest first.
+ * Requirements: 1 <= n <= 16; every plan on the current device, with the same
+ * d, the same regime (bn, stages, ctas_per_sm -- plan the batch's masks with the
+ * same tsr_plan_opts) and the same mask family (all KEYLIST or none); a plan
+ * at most once per batch.  Otherwise TSR_ERR_INVALID_ARG / TSR_ERR_UNSUPPORTED
+ * before any launch.  Device-side failures (a wait that timed out) go to the
+ * error word of the first request's plan; tsr_plan_device_status on that plan
+ * reports them.  The plans' storage must not be re-planned until the launch
+ * has completed.
+ */
+typedef struct {
+  const void *q, *k, *v;
+  tsr_plan_t plan;
+  void *out;
+  float *lse;
+} tsr_request;
+
+tsr_status tsr_bsa_forward_batch(const tsr_request *reqs, int32_t n, void *stream);
+
 /* Synchronise `stream` and return the plan's device error word as a status
    (TSR_OK, TSR_ERR_TIMEOUT or TSR_ERR_INTERNAL); clears it. */
 tsr_status tsr_plan_device_status(tsr_plan_t plan, void *stream);
