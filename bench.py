@@ -312,6 +312,68 @@ def run_sweep(args) -> None:
     print(json.dumps(line, default=str), flush=True)
 
 
+def run_batch(args) -> None:
+    """Several requests of different shapes served together: the same requests
+    run one launch each (tsr_bsa_forward, back to back on one stream) and in one
+    batched launch (tsr_bsa_forward_batch).  Requests (d = 128, regime BN 64 /
+    2 stages / 2 CTAs per SM for all): 480p block masks with 2, 4 and 6 heads,
+    SVG 480p with 4 heads, a 8,192-token block mask with 8 heads and a
+    2,048-token one with 16 heads.  One JSON line; planning is not timed."""
+    import torch
+    import block_sparse_attention_tsr_gb300 as tsr
+    import workloads as W
+
+    tsr.build()
+    tsr.lib()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
+    specs = [W.video_block_mask(seed=21, H=2), W.video_block_mask(seed=22, H=4),
+             W.video_block_mask(seed=23, H=6), W.svg_mask(1, 4, n_frames=21, frame_size=1560),
+             W.video_block_mask(seed=24, H=8, N=8192), W.video_block_mask(seed=25, H=16, N=2048)]
+    reqs, flops = [], 0.0
+    for i, spec in enumerate(specs):
+        q, k, v = (x.to(dev) for x in W.qkv(spec.B, spec.H, spec.N, D, seed=30 + i))
+        mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, D, **W.mask_tensors(spec, dev))
+        plan = tsr.tsr_plan(mask, opts, stream)
+        out = torch.empty_like(q)
+        lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32, device=dev)
+        reqs.append((q, k, v, plan, out, lse))
+        flops += 4.0 * D * allowed_pairs(spec)
+
+    def one_by_one():
+        for q, k, v, plan, out, lse in reqs:
+            tsr.tsr_bsa_forward(q, k, v, plan, out, lse, stream)
+
+    def batched():
+        tsr.tsr_bsa_forward_batch(reqs, stream)
+
+    res = {}
+    for name, fn in (("separate_launches", one_by_one), ("one_batched_launch", batched)):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        res[name] = {"ms": ms, "tflops": flops / ms / 1e9}
+    tsr.tsr_plan_device_status(reqs[0][3])
+    line = {"metric": METRIC, "value": res["one_batched_launch"]["tflops"], "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["one_batched_launch"]["ms"], "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "batch_6_requests_mixed_shapes_d128",
+                       "requests": [f"{s.meta.get('workload', s.kind)} H{s.H} N{s.N}" for s in specs],
+                       "step": "attention of all requests (plans made once)"},
+            "separate_launches": res["separate_launches"],
+            "one_batched_launch": res["one_batched_launch"]}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -325,7 +387,8 @@ def main():
     ap.add_argument("--ctas", type=int, default=0)
     ap.add_argument("--workload", default="video480p",
                     help="video480p (the benchmark), svg480p, keylist720p, sweepM (one member), "
-                         "sweep (regime-table regret over --sweep-masks members)")
+                         "sweep (regime-table regret over --sweep-masks members), "
+                         "batch (six requests: separate launches vs one batched launch)")
     ap.add_argument("--heads", type=int, default=24,
                     help="heads of the workload (24 = the benchmark; fewer for profiling)")
     ap.add_argument("--sweep-masks", type=int, default=32,
@@ -345,6 +408,10 @@ def main():
     if args.workload == "sweep":
         if rank == 0:
             run_sweep(args)
+        return
+    if args.workload == "batch":
+        if rank == 0:
+            run_batch(args)
         return
 
     import torch
