@@ -31,7 +31,7 @@ __all__ = [
 ]
 
 UNIFORM, SEGMENTS, SVG, KEYLIST = 0, 1, 2, 3
-PLAN_SYNC_CHECK, PLAN_NO_LPT, PLAN_TEST_STALL = 1, 2, 4
+PLAN_SYNC_CHECK, PLAN_NO_LPT, PLAN_TEST_STALL, PLAN_DEBUG_CHECKS = 1, 2, 4, 8
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory",
            5: "device wait timed out", 6: "internal error"}
 

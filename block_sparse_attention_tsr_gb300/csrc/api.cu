@@ -265,6 +265,27 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
   } else if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) {
     return s;
   }
+  if (P->flags & TSR_PLAN_DEBUG_CHECKS) {
+    if (tsr_status s = plan_check(P, st)) return s;
+    uint32_t e = 0;
+    TSR_CUDA(cudaMemcpyAsync(&e, P->err, sizeof e, cudaMemcpyDeviceToHost, st));
+    TSR_CUDA(cudaStreamSynchronize(st));
+    if (e) return fail(TSR_ERR_INTERNAL, "plan check failed (error word " + std::to_string(e) + ")");
+  }
+  return TSR_OK;
+}
+
+// Debug checks after a launch: the tiles the kernel computed against the plans.
+tsr_status check_tiles_done(const tsr_plan_s* const* plans, int n, cudaStream_t st) {
+  unsigned long long done = 0;
+  TSR_CUDA(cudaMemcpyAsync(&done, static_cast<unsigned long long*>(plans[0]->b_tot.p) + 7,
+                           sizeof done, cudaMemcpyDeviceToHost, st));
+  TSR_CUDA(cudaStreamSynchronize(st));
+  unsigned long long want = 0;
+  for (int i = 0; i < n; ++i) want += static_cast<unsigned long long>(plans[i]->n_entries);
+  if (done != want)
+    return fail(TSR_ERR_INTERNAL, "the kernel computed " + std::to_string(done) + " tiles, the plan has " +
+                                      std::to_string(want));
   return TSR_OK;
 }
 
@@ -419,6 +440,11 @@ tsr_status tsr_bsa_forward(const void* q, const void* k, const void* v, tsr_plan
   a.lse = lse;
   a.plan = plan;
   if (tsr_status e = launch_forward(a, st)) return e;
+  if (plan->flags & TSR_PLAN_DEBUG_CHECKS) {
+    if (tsr_status e = tsr_plan_device_status(plan, stream)) return e;
+    const tsr_plan_s* one[1] = {plan};
+    return check_tiles_done(one, 1, st);
+  }
   if (plan->flags & TSR_PLAN_SYNC_CHECK) return tsr_plan_device_status(plan, stream);
   return TSR_OK;
 }
@@ -447,6 +473,12 @@ tsr_status tsr_bsa_forward_batch(const tsr_request* reqs, int32_t n, void* strea
     a[r] = FwdArgs{q.q, q.k, q.v, q.out, q.lse, q.plan};
   }
   if (tsr_status e = launch_forward_batch(a, n, static_cast<cudaStream_t>(stream))) return e;
+  if (reqs[0].plan->flags & TSR_PLAN_DEBUG_CHECKS) {
+    if (tsr_status e = tsr_plan_device_status(reqs[0].plan, stream)) return e;
+    const tsr_plan_s* plans[16];
+    for (int32_t r = 0; r < n; ++r) plans[r] = reqs[r].plan;
+    return check_tiles_done(plans, n, static_cast<cudaStream_t>(stream));
+  }
   if (reqs[0].plan->flags & TSR_PLAN_SYNC_CHECK) return tsr_plan_device_status(reqs[0].plan, stream);
   return TSR_OK;
 }

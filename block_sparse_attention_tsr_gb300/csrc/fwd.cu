@@ -138,6 +138,9 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
     prm.counter = P0->counter;
     prm.err = P0->err;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P0->d)));
+    prm.tiles_done = ((P0->flags & TSR_PLAN_DEBUG_CHECKS) && P0->b_tot.p)
+                         ? static_cast<unsigned long long*>(P0->b_tot.p) + 7
+                         : nullptr;
     prm.test_stall = (P0->flags & TSR_PLAN_TEST_STALL) ? 1 : 0;
     prm.timeout_ns = prm.test_stall ? 100000000ull : kWaitTimeoutNs;
     return TSR_OK;
@@ -145,6 +148,8 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
   // KEYLIST plans gather K / V by key list; plans with temporal-major heads take
   // the variant that may gather through the permutation; the rest are TMA only.
   auto launch = [&](const auto& prm) -> tsr_status {
+    if (prm.tiles_done)
+      TSR_CUDA(cudaMemsetAsync(prm.tiles_done, 0, sizeof(unsigned long long), stream));
     if (prm.n_items == 0) return TSR_OK;
     TSR_CUDA(cudaMemsetAsync(P0->counter, 0, sizeof(int32_t), stream));
     const int n = prm.n_items, dev = P0->device;

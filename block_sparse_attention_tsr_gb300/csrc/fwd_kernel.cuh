@@ -77,6 +77,7 @@ template <int MAXR>
 struct FwdParamsT {
   int32_t* counter;
   uint32_t* err;
+  unsigned long long* tiles_done;   // debug checks: tiles computed, else null
   int32_t n_items;               // over all requests
   int32_t n_req;
   float scale_log2;              // log2(e) / sqrt(d)
@@ -506,6 +507,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
         t_cnt += n;
         kv_cnt += n;
       }
+      if (p.tiles_done) atomicAdd(p.tiles_done, static_cast<unsigned long long>(t_cnt));
       // every MMA issued has finished before TMEM is released
       mma_commit(smem_u32(&ctrl.final_bar));
       volatile int32_t dummy = 0;

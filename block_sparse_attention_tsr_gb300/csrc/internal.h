@@ -98,6 +98,9 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
                             int32_t* dbegin, int32_t* hist, void* items, void* entries,
                             void* descs, cudaStream_t stream);
 
+// device-side plan consistency checks (check.cu)
+tsr_status plan_check(const tsr_plan_impl* P, cudaStream_t stream);
+
 // forward kernels (fwd.cu)
 struct FwdArgs {
   const void* q;

@@ -143,6 +143,14 @@ typedef struct {
                                   runs: after 0.1 s it gives up, frees its resources
                                   and tsr_plan_device_status() returns
                                   TSR_ERR_TIMEOUT; the context stays usable      */
+#define TSR_PLAN_DEBUG_CHECKS 8  /* after every tsr_plan / tsr_plan_update, a device
+                                  pass checks every index of the plan (items,
+                                  entries, descriptors, gathered keys; each query
+                                  tile exactly once) and the call returns
+                                  TSR_ERR_INTERNAL on a violation; every
+                                  tsr_bsa_forward(_batch) also counts the tiles
+                                  the kernel computed and compares them with the
+                                  plan.  Both synchronise `stream`.             */
 
 typedef struct tsr_plan_s *tsr_plan_t;   /* opaque, library-owned */
 

@@ -93,3 +93,15 @@ def test_package_has_no_cpu_path():
     assert "import oracle" not in src and "from oracle" not in src
     for f in os.listdir(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f)).read()
+
+
+def test_plan_flags_match_the_header():
+    """The binding's flag values are the header's #defines."""
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "tsr.h")).read()
+    defs = dict(re.findall(r"#define (TSR_PLAN_\w+)\s+(\d+)", hdr))
+    assert int(defs["TSR_PLAN_SYNC_CHECK"]) == tsr.PLAN_SYNC_CHECK
+    assert int(defs["TSR_PLAN_NO_LPT"]) == tsr.PLAN_NO_LPT
+    assert int(defs["TSR_PLAN_TEST_STALL"]) == tsr.PLAN_TEST_STALL
+    assert int(defs["TSR_PLAN_DEBUG_CHECKS"]) == tsr.PLAN_DEBUG_CHECKS

@@ -67,6 +67,15 @@ def test_key_list_requests():
     _check(reqs, 128)
 
 
+def test_batch_with_debug_checks():
+    """The tile count of a batched launch is compared with all its plans."""
+    opts = dict(OPTS, flags=tsr.PLAN_DEBUG_CHECKS)
+    reqs = [_request(W.tiny_block_mask(seed=16, N=1024), 128, 16, opts),
+            _request(W.svg_mask(1, 2, n_frames=16, frame_size=48, kinds=np.array([0, 1], np.int8)),
+                     128, 17, opts)]
+    _check(reqs, 128)
+
+
 def test_single_request_batch_equals_forward():
     reqs = [_request(W.tiny_block_mask(seed=7, N=1024), 128, 7)]
     _check(reqs, 128)

@@ -430,6 +430,30 @@ def test_host_entry_point_in_head_groups(which):
         assert np.array_equal(lse.double().numpy(), L)
 
 
+@pytest.mark.parametrize("which", ["uniform", "segments", "svg", "keylist"])
+def test_debug_checks_pass_on_valid_plans(which):
+    """With TSR_PLAN_DEBUG_CHECKS every plan is checked index by index on the
+    device and every launch's computed tile count is compared with the plan;
+    valid plans of every mask form pass, and the results are unchanged."""
+    if which == "uniform":
+        spec = W.tiny_block_mask(seed=13, N=1000)
+    elif which == "segments":
+        spec = W.segment_mask(14, 1, 2, 1500, lo=16, hi=300)
+    elif which == "svg":
+        spec = W.svg_mask(2, 3, n_frames=16, frame_size=41, kinds=np.array([1, 0, 1], np.int8),
+                          temporal_radius=1)
+    else:
+        spec = W.random_keylist(15, 1, 2, 900, slice_m=64, lo=0, hi=300)
+    (q, k, v), plan, O, L = run(spec, 128, seed=13, opts={"flags": tsr.PLAN_DEBUG_CHECKS})
+    _, _, O2, L2 = run(spec, 128, seed=13, qkv=(q, k, v))
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
+    mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, 128, **W.mask_tensors(spec))
+    plan.update(mask)                                   # re-plan: checked again
+    out, lse = tsr.tsr_bsa_forward(q.cuda(), k.cuda(), v.cuda(), plan)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().cpu().numpy(), O)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """Failure detection without a GPU fault: with the test-only stall flag the
     MMA issuer waits on a barrier nothing signals; the kernel gives up after its
