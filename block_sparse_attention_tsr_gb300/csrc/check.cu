@@ -9,7 +9,8 @@
 //   * contiguous entries: key tile starts inside [0, N), multiples of the tile
 //     width, strictly ascending within an item; descriptor index -1 or inside
 //     the plan; grid-form descriptors with 1..8 row and column segments,
-//     ascending starts inside the tile;
+//     ascending starts inside the tile; band-form descriptors with a frame
+//     count of at least 1;
 //   * gathered entries: tile e at gidx offset e * BN, descriptor index -1 or e,
 //     and every gathered key index inside [0, N).
 // A violation sets DEV_ERR_INTERNAL in the plan's error word; nothing traps.
@@ -63,7 +64,13 @@ __global__ void plan_check_items_kernel(CheckArgs a) {
       if (di >= 0 && di < a.n_desc) {
         const uint8_t* d = a.descs + static_cast<int64_t>(di) * 32;
         const int n_r = d[0], n_c = d[1];
-        bad |= n_r < 1 || n_r > 8 || n_c < 1 || n_c > 8;
+        if (n_r == 0) {
+          // band form: no segments, bits = F << 32 | R with F >= 1
+          const uint32_t F = *reinterpret_cast<const uint32_t*>(d + 28);
+          bad |= n_c != 0 || F < 1;
+        } else {
+          bad |= n_r > 8 || n_c < 1 || n_c > 8;
+        }
         if (!(n_r < 1 || n_r > 8 || n_c < 1 || n_c > 8)) {
           bad |= d[2] != 0;                       // r_start[0]
           for (int r = 1; r < n_r; ++r) bad |= d[2 + r] <= d[1 + r] || d[2 + r] >= kBM;

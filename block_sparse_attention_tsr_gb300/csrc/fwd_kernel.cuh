@@ -537,10 +537,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       float m_ref = -INFINITY, l = 0.f;
       // The tile entry and its boundary descriptor are fetched one tile ahead so
       // that their global-memory latency hides behind the wait for S.
-      int32_t desc_next = -1;
+      int32_t desc_next = -1, kv_next = 0;
       uint4 dn0 = make_uint4(0u, 0u, 0u, 0u), dn1 = dn0;
       if (n > 0) {
-        desc_next = __ldg(&rq.entries[begin]).y;
+        const int2 en = __ldg(&rq.entries[begin]);
+        desc_next = en.y;
+        kv_next = en.x;
         if (desc_next >= 0) {
           dn0 = __ldg(&rq.descs[2 * desc_next]);
           dn1 = __ldg(&rq.descs[2 * desc_next + 1]);
@@ -549,10 +551,12 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       for (int32_t j = 0; j < n; ++j) {
         const uint32_t t = t_cnt + j;
         const uint32_t sb = t & 1;
-        const int32_t desc = desc_next;
+        const int32_t desc = desc_next, kv = kv_next;
         const uint4 d0 = dn0, d1 = dn1;
         if (j + 1 < n) {
-          desc_next = __ldg(&rq.entries[begin + j + 1]).y;
+          const int2 en = __ldg(&rq.entries[begin + j + 1]);
+          desc_next = en.y;
+          kv_next = en.x;
           if (desc_next >= 0) {
             dn0 = __ldg(&rq.descs[2 * desc_next]);
             dn1 = __ldg(&rq.descs[2 * desc_next + 1]);
@@ -593,6 +597,26 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
 #pragma unroll
             for (int c = 0; c < BN; ++c)
               if (!((w4[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+          }
+        } else if (!GATHER && desc >= 0 && (d0.x & 0xFF) == 0) {
+          // band form (SVG temporal heads, temporal-major order): the row sees
+          // keys whose F-token segment is within R of its own -- one interval
+          const int64_t Fb = d1.w, Rb = d1.z;
+          const int64_t tq = static_cast<int64_t>(q_tile) * kBM + r, seg = tq / Fb;
+          const int64_t lo_a = (seg - Rb) * Fb - kv, hi_a = (seg + Rb + 1) * Fb - kv;
+          const int64_t hi_n = static_cast<int64_t>(rq.N) - kv;
+          const int lo = static_cast<int>(lo_a > 0 ? lo_a : 0);
+          const int hi = static_cast<int>(hi_a < BN ? (hi_a < hi_n ? hi_a : hi_n) : (BN < hi_n ? BN : hi_n));
+          if (tq >= rq.N || lo >= hi) {
+            row_dead = true;
+          } else if (lo > 0 || hi < BN) {
+            uint32_t words[BN / 32];
+#pragma unroll
+            for (int w = 0; w < BN / 32; ++w) words[w] = 0u;
+            add_range<BN>(words, lo, hi);
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (!((words[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
           }
         } else if (desc >= 0) {
           const int n_r = d0.x & 0xFF, n_c = (d0.x >> 8) & 0xFF;

@@ -82,11 +82,35 @@ struct RowSegs {
   int n;
   int ids[kMaxSeg];
   int starts[kMaxSeg + 1];
+  int q0, q1;                // the tile's query rows [q0, q1)
 };
+
+// SVG temporal heads in temporal-major order: row t' may see keys whose
+// F-token segment is within R of its own, |t'/F - j/F| <= R.  Each row's keys
+// form one interval and the rows' intervals grow with the row, so a tile is
+// empty, full or "band" from its first and last rows.  Band tiles get a
+// descriptor with n_r = 0 and bits = F << 32 | R; the kernel masks each row to
+// its interval (any frame count: no per-tile segment limit).
+__device__ int classify_band(const MaskDev& m, int q0, int q1, int k0, int bn, tsr_tile_desc* desc) {
+  if (k0 >= m.N) return 0;
+  const int64_t F = m.F, R = m.R, k1 = min(m.N, k0 + bn);
+  const int64_t s_first = q0 / F, s_last = (q1 - 1) / F;
+  const int64_t lo_a = (s_first - R) * F, hi_a = (s_last + R + 1) * F;
+  const int64_t lo_u = lo_a > 0 ? lo_a : 0, hi_u = hi_a < m.N ? hi_a : m.N;
+  if (k1 <= lo_u || k0 >= hi_u) return 0;
+  if (k0 + bn <= m.N && (s_first + R + 1) * F >= k0 + bn && (s_last - R) * F <= k0) return 1;
+  if (desc) {
+    memset(desc, 0, sizeof(*desc));
+    desc->bits = (static_cast<uint64_t>(m.F) << 32) | static_cast<uint32_t>(m.R);
+  }
+  return 2;
+}
 
 // 0 empty, 1 full, 2 boundary, -1 unsupported.  desc is filled for boundary tiles.
 __device__ int classify(const MaskDev& m, int bh, int h, const RowSegs& rs, int k0, int bn,
                         int64_t nqs, int64_t nks, tsr_tile_desc* desc) {
+  if (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
+    return classify_band(m, rs.q0, rs.q1, k0, bn, desc);
   if (k0 >= m.N) return 0;
   const int k1 = min(m.N, k0 + bn);
   int cid[kMaxSeg], cst[kMaxSeg + 1];
@@ -181,7 +205,11 @@ __global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned
   if (warp >= n_items) return;
   const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
   RowSegs rs;
-  rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
+  rs.q0 = qt * kBM;
+  rs.q1 = min(m.N, qt * kBM + kBM);
+  rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
+             ? 0
+             : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
   int64_t nqs, nks;
   grid_dims(m, &nqs, &nks);
   const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), 128);
@@ -301,7 +329,11 @@ __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32
   if (warp >= n_items) return;
   const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
   RowSegs rs;
-  rs.n = tile_segments(m, h, 0, qt * kBM, min(m.N, qt * kBM + kBM), rs.ids, rs.starts);
+  rs.q0 = qt * kBM;
+  rs.q1 = min(m.N, qt * kBM + kBM);
+  rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
+             ? 0
+             : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
   int64_t nqs, nks;
   grid_dims(m, &nqs, &nks);
   const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), bn);

@@ -95,9 +95,9 @@ typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
  *           Temporal heads run in temporal-major order (t' = s * n_frames + f):
  *           the attention kernel reads their Q/K/V rows through the inverse
  *           permutation and writes O and lse back in the caller's order; nothing
- *           is copied.  frame_size >= 16 and n_frames >= 16 (a 128-token tile may
- *           hold at most 8 segments; smaller values give TSR_ERR_UNSUPPORTED),
- *           temporal_radius >= 0.
+ *           is copied.  Any n_frames >= 1; frame_size >= 16 when a head is
+ *           spatial (a 128-token tile may hold at most 8 frames; smaller frames
+ *           give TSR_ERR_UNSUPPORTED); temporal_radius >= 0.
  * KEYLIST : slice_m in {64, 128}.  indptr = int64 [B*H*ceil(N/slice_m) + 1] (CSR
  *           over (b, h, query block), indptr[0] = 0), indices = int32 keys, each
  *           list ascending, unique, in [0, N).  allowed(i, j) = j in the list of
@@ -300,6 +300,10 @@ typedef struct {
  * of range.  Element (row, col) is allowed iff bit (r*8 + c) of `bits` is set.
  * Gathered plans (list form): n_r = bm / slice_m row segments of slice_m rows;
  * column c is allowed for row segment r iff bit c of colmask[r] is set.
+ * Band form (temporal SVG heads; n_r = 0, n_c = 0, bits = F << 32 | R): with
+ * row token t = q_tile * bm + row and key token k = entry key start + col, both
+ * in temporal-major order, the element is allowed iff t < N, k < N and
+ * |t / F - k / F| <= R (integer division).
  */
 typedef struct {
   uint8_t n_r, n_c;

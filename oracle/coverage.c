@@ -78,8 +78,9 @@ typedef struct {
 
 static int32_t unpermute(int32_t tp, int32_t F, int32_t S) { return (tp % F) * S + tp / F; }
 
-/* Is element (row r, column c) of a tile selected by the tile itself? */
-static int tile_allows(const plan_view *p, const exp_entry *e, int32_t r, int32_t c) {
+/* Is element (row r, column c) of a tile selected by the tile itself?  q0 is
+   the item's first row in the head's layout. */
+static int tile_allows(const plan_view *p, const exp_entry *e, int32_t q0, int32_t r, int32_t c) {
   if (e->desc < 0) return 1;
   if (p->h->gathered) {
     const exp_desc_list *d = (const exp_desc_list *)(p->descs + (size_t)e->desc * 32);
@@ -87,6 +88,14 @@ static int tile_allows(const plan_view *p, const exp_entry *e, int32_t r, int32_
     return (d->colmask[seg][c >> 5] >> (c & 31)) & 1u;
   }
   const exp_desc_grid *d = (const exp_desc_grid *)(p->descs + (size_t)e->desc * 32);
+  if (d->n_r == 0) {
+    /* band form: segments of F tokens in the head's layout, |t / F - k / F| <= R */
+    const int64_t F = (int64_t)(d->bits >> 32), R = (int64_t)(uint32_t)d->bits;
+    const int64_t t = (int64_t)q0 + r, k = (int64_t)e->kv + c;
+    if (F <= 0 || t >= p->h->N || k >= p->h->N) return 0;
+    const int64_t dist = t / F - k / F;
+    return (dist <= R && -dist <= R) ? 1 : 0;
+  }
   if (c >= d->c_start[d->n_c]) return 0;
   int rs = 0, cs = 0;
   while (rs + 1 < d->n_r && d->r_start[rs + 1] <= r) ++rs;
@@ -221,7 +230,7 @@ int64_t coverage_check(const oracle_mask *m, const uint8_t *buf, size_t len, int
           const int32_t row_o = lay ? unpermute(q0 + r, F, S) : q0 + r;
           for (int32_t c = 0; c < BN; ++c) {
             const int64_t key = h->gathered ? (int64_t)p.gidx[E->kv + c] : (int64_t)E->kv + c;
-            if (!tile_allows(&p, E, r, c)) continue;
+            if (!tile_allows(&p, E, q0, r, c)) continue;
             ++sel;
             if (key < 0 || key >= N) {
               if (E->desc < 0) full_bad = 1;

@@ -127,14 +127,17 @@ def test_svg_small(d):
 
 @pytest.mark.parametrize("opts,F,S", [(None, 16, 41), ({"bn": 128, "stages": 3}, 24, 27),
                                       ({"bn": 64, "stages": 2, "ctas_per_sm": 2}, 16, 41),
-                                      ({"bn": 64, "stages": 3, "ctas_per_sm": 2}, 24, 27)])
+                                      ({"bn": 64, "stages": 3, "ctas_per_sm": 2}, 24, 27),
+                                      (None, 13, 50), ({"bn": 128, "stages": 3}, 5, 130),
+                                      ({"bn": 64, "stages": 2, "ctas_per_sm": 2}, 1, 700)])
 def test_svg_ragged_temporal_gather(opts, F, S):
     """Temporal-major heads load Q, K and V rows through the inverse permutation
-    inside the kernel; N = F x S (656 or 648) leaves a ragged last query and key
-    tile whose rows past N must neither be read as keys nor written as outputs.
-    Two batches and mixed head kinds put spatial (TMA) and temporal (gathered)
-    items in one launch.  (Fewer than 16 frames would put more than 8 temporal
-    segments in one 128-token tile, which planning rejects as unsupported.)"""
+    inside the kernel; N = F x S leaves a ragged last query and key tile whose
+    rows past N must neither be read as keys nor written as outputs.  Two
+    batches and mixed head kinds put spatial (TMA) and temporal (gathered)
+    items in one launch.  Frame counts below 16 (13, 5, 1) put more than 8
+    temporal segments in a 128-token tile: those tiles are masked by the band
+    rule, which has no segment limit."""
     d = 64 if opts and opts.get("stages") == 3 and opts.get("ctas_per_sm") == 2 else 128
     spec = W.svg_mask(2, 3, n_frames=F, frame_size=S, kinds=np.array([1, 0, 1], np.int8))
     (q, k, v), plan, O, L = run(spec, d, seed=21, opts=opts)
