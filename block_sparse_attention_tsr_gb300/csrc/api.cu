@@ -4,6 +4,7 @@
 // lookup table filled by offline profiling).
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <array>
 #include <cstring>
 #include <fstream>
@@ -615,8 +616,26 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   // copied out (three streams; the copy engines and the SMs overlap).
   const int64_t n_groups = std::max<int64_t>(
       1, std::min<int64_t>(BH, static_cast<int64_t>((3 * tb + (160u << 20) - 1) / (160u << 20))));
-  const int64_t per = (BH + n_groups - 1) / n_groups;
-  const int64_t G = (BH + per - 1) / per;
+  // Group g holds heads [gs[g], gs[g + 1]).  The first and the last groups are
+  // about a third of the others: the first group's copy-in and the last
+  // group's copy-out are the parts no attention overlaps.
+  std::vector<int64_t> gs{0};
+  {
+    const int64_t per = (BH + n_groups - 1) / n_groups;
+    const int64_t edge = (n_groups >= 3) ? std::max<int64_t>(1, per / 3) : 0;
+    if (edge > 0 && BH > 2 * edge) {
+      const int64_t mid = BH - 2 * edge, n_mid = n_groups - 1;
+      gs.push_back(edge);
+      for (int64_t i = 1; i <= n_mid; ++i) gs.push_back(edge + (mid * i + n_mid - 1) / n_mid);
+      gs.push_back(BH);
+    } else {
+      for (int64_t b = per; b < BH; b += per) gs.push_back(b);
+      gs.push_back(BH);
+    }
+    // drop empty groups
+    gs.erase(std::unique(gs.begin(), gs.end()), gs.end());
+  }
+  const int64_t G = static_cast<int64_t>(gs.size()) - 1;
   void *dq, *dk, *dv, *dout, *dlse;
   if (tsr_status s = hc.get(0, tb, &dq)) return s;
   if (tsr_status s = hc.get(1, tb, &dk)) return s;
@@ -653,7 +672,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       kb = pb + nq;
     }
     for (int64_t g = 0; g < G; ++g) {
-      views[g].blocks = static_cast<const uint8_t*>(db) + g * per * per_head;
+      views[g].blocks = static_cast<const uint8_t*>(db) + gs[g] * per_head;
       views[g].q_bounds = qb;
       views[g].k_bounds = kb;
     }
@@ -667,7 +686,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     rebased.reserve(n_lists + G);
     std::vector<int64_t> start(G), base(G);
     for (int64_t g = 0; g < G; ++g) {
-      const int64_t l0 = g * per * nqb, l1 = std::min(BH, (g + 1) * per) * nqb;
+      const int64_t l0 = gs[g] * nqb, l1 = gs[g + 1] * nqb;
       start[g] = static_cast<int64_t>(rebased.size());
       base[g] = mask->indptr[l0];
       for (int64_t l = l0; l <= l1; ++l) rebased.push_back(mask->indptr[l] - base[g]);
@@ -693,7 +712,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     if (tsr_status s = hc.get(7, BH, &dh)) return s;
     TSR_CUDA(cudaMemcpyAsync(dh, kinds.data(), BH, cudaMemcpyHostToDevice, sp));
     TSR_CUDA(cudaStreamSynchronize(sp));
-    for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + g * per;
+    for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + gs[g];
   }
   // 2. inputs, group by group (queued after the mask, which the copy engine
   // would otherwise move only after every input)
@@ -701,7 +720,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   const char* hk = static_cast<const char*>(k);
   const char* hv = static_cast<const char*>(v);
   for (int64_t g = 0; g < G; ++g) {
-    const int64_t b0 = g * per, cnt = std::min(per, BH - b0);
+    const int64_t b0 = gs[g], cnt = gs[g + 1] - gs[g];
     const size_t off = b0 * row_b, n = cnt * row_b;
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dq) + off, hq + off, n, cudaMemcpyHostToDevice, hc.s_in));
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dk) + off, hk + off, n, cudaMemcpyHostToDevice, hc.s_in));
@@ -720,7 +739,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   for (int64_t g = 0; g < G; ++g) {
     tsr_mask& vw = views[g];
     vw.B = 1;
-    vw.H = static_cast<int32_t>(std::min(per, BH - g * per));
+    vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
     const std::array<int64_t, 9> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
                                          o.flags, opts ? 1 : 0};
     tsr_status s = TSR_OK;
@@ -743,8 +762,8 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   // 4. attention per group once its inputs and plan are ready; 5. outputs back
   tsr_status s = TSR_OK;
   for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
-    const int64_t b0 = g * per;
-    const size_t off = b0 * row_b, n = std::min(per, BH - b0) * row_b;
+    const int64_t b0 = gs[g];
+    const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
     TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g], 0));
     TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g + 1], 0));
     s = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,

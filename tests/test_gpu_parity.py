@@ -408,13 +408,14 @@ def test_host_entry_point_keylist():
 @pytest.mark.parametrize("which", ["uniform", "svg", "keylist"])
 def test_host_entry_point_in_head_groups(which):
     """Inputs above 160 MB are moved and attended in head groups on three
-    streams; with the regime forced the result is bit-identical to one device
-    call over all heads.  The SVG case has B = 3, H = 3, so a group spans two
+    streams (with three or more groups the first and last are smaller); with
+    the regime forced the result is bit-identical to one device call over all
+    heads.  The SVG case has B = 3, H = 3, so a group spans two
     batches and its head kinds come from the flattened (b, h) order; the
     key-list case rebases each group's slice of indptr."""
     opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
     if which == "uniform":
-        spec = W.video_block_mask(seed=5, H=8)
+        spec = W.video_block_mask(seed=5, H=16)      # 3 x 134 MB: groups of 2, 6, 6, 2 heads
         kw = dict(bq=64, bk=64, blocks=spec.blocks)
     elif which == "svg":
         spec = W.svg_mask(3, 3, n_frames=21, frame_size=1560, kinds=np.array([1, 0, 1], np.int8))
