@@ -217,44 +217,82 @@ __global__ void __launch_bounds__(256) keylist_emit_kernel(
 // searching is needed.
 constexpr int32_t kBitmapMaxN = 196608;
 
-__device__ __forceinline__ void set_bits(uint32_t* bm, const int32_t* keys, int64_t n) {
-  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-    const int32_t k = keys[i];
-    atomicOr(&bm[k >> 5], 1u << (k & 31));
+__host__ __device__ constexpr int32_t bitmap_words(int32_t N) { return (N + 31) >> 5; }
+// one bitmap's words rounded up to 16 bytes (the second bitmap starts aligned)
+__host__ __device__ constexpr int32_t bitmap_words16(int32_t N) { return (bitmap_words(N) + 3) & ~3; }
+
+// One shared atomic per run of a thread's keys that share a bitmap word.
+__device__ __forceinline__ void or_keys4(uint32_t* bm, int4 v) {
+  uint32_t w = static_cast<uint32_t>(v.x) >> 5, bits = 1u << (v.x & 31);
+  const int32_t rest[3] = {v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const uint32_t wj = static_cast<uint32_t>(rest[j]) >> 5;
+    if (wj != w) {
+      atomicOr(&bm[w], bits);
+      w = wj;
+      bits = 0u;
+    }
+    bits |= 1u << (rest[j] & 31);
   }
+  atomicOr(&bm[w], bits);
 }
 
-// Exclusive scan over nw words of popcount(a | b) with one block of 256
-// threads; pre[w] receives the union rank of word w's first key.  Returns the
-// union size.
-__device__ int32_t union_prefix(const uint32_t* a, const uint32_t* b, int32_t* pre, int32_t nw,
-                                int* wsum) {
-  const int T = blockDim.x, tid = threadIdx.x;
-  const int per = (nw + T - 1) / T;
-  const int lo = min(nw, tid * per), hi = min(nw, lo + per);
-  int s = 0;
-  for (int w = lo; w < hi; ++w) s += __popc(a[w] | b[w]);
-  // block exclusive scan of s
-  const int lane = tid & 31, warp = tid >> 5;
-  int x = s;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
+// Sets one bit per key of a sorted list in a shared bitmap (all threads of the
+// block take part).  The list is read with 16-byte loads, four per thread in
+// flight: scalar keys up to the first 16-byte boundary, then whole vectors,
+// then a scalar tail.  With CHECK, a key outside [0, N) or not above its
+// predecessor is reported (return value) and its vector is not set; without it
+// the list must already be known to be valid.
+template <bool CHECK>
+__device__ bool set_bits_vec(uint32_t* bm, const int32_t* keys, int64_t n, int32_t N) {
+  bool bad = false;
+  const int lane = threadIdx.x & 31;
+  const int64_t head =
+      min(n, static_cast<int64_t>(((16u - (reinterpret_cast<uintptr_t>(keys) & 15u)) & 15u) >> 2));
+  const int64_t n4 = (n - head) >> 2;
+  auto scalar = [&](int64_t i) {
+    const int32_t k = keys[i];
+    if (CHECK && (k < 0 || k >= N || (i + 1 < n && keys[i + 1] <= k))) {
+      bad = true;
+      return;
+    }
+    atomicOr(&bm[static_cast<uint32_t>(k) >> 5], 1u << (k & 31));
+  };
+  if (threadIdx.x < head) scalar(threadIdx.x);
+  const int4* v4 = reinterpret_cast<const int4*>(keys + head);
+  const int64_t T = blockDim.x;
+  for (int64_t base = 0; base < n4; base += 4 * T) {
+    int4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = base + u * T + threadIdx.x;
+      v[u] = i < n4 ? __ldg(v4 + i) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = base + u * T + threadIdx.x;
+      if (CHECK) {
+        // the key after this vector: the next lane's first key, else a load
+        int32_t nx = __shfl_down_sync(0xFFFFFFFFu, v[u].x, 1);
+        if (lane == 31 || i + 1 >= n4) {
+          const int64_t after = head + 4 * i + 4;
+          nx = (i < n4 && after < n) ? keys[after] : INT32_MAX;
+        }
+        if (i < n4) {
+          const int4 k = v[u];
+          if (k.x < 0 || k.w >= N || k.y <= k.x || k.z <= k.y || k.w <= k.z || nx <= k.w) {
+            bad = true;
+            continue;
+          }
+        }
+      }
+      if (i < n4) or_keys4(bm, v[u]);
+    }
   }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  int before = 0, total = 0;
-  for (int i = 0; i < (T >> 5); ++i) {
-    if (i < warp) before += wsum[i];
-    total += wsum[i];
-  }
-  int run = before + x - s;
-  for (int w = lo; w < hi; ++w) {
-    pre[w] = run;
-    run += __popc(a[w] | b[w]);
-  }
-  __syncthreads();
-  return total;
+  const int64_t t0 = head + 4 * n4;
+  if (threadIdx.x < n - t0) scalar(t0 + threadIdx.x);
+  return bad;
 }
 
 // Count (bitmap form), validating the tile's lists on the way: indptr must run
@@ -266,28 +304,14 @@ __device__ __forceinline__ bool list_ok(const int64_t* indptr, int64_t row) {
   return indptr[row + 1] >= indptr[row] && (row != 0 || indptr[0] == 0);
 }
 
-__device__ __forceinline__ bool set_bits_checked(uint32_t* bm, const int32_t* keys, int64_t n,
-                                                 int32_t N) {
-  bool bad = false;
-  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-    const int32_t k = keys[i];
-    if (k < 0 || k >= N || (i + 1 < n && keys[i + 1] <= k)) {
-      bad = true;
-      continue;
-    }
-    atomicOr(&bm[k >> 5], 1u << (k & 31));
-  }
-  return bad;
-}
-
 __global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
     const int64_t* indptr, const int32_t* indices, int64_t n_items, int32_t nqt, int32_t nqb,
     int32_t slice_m, int32_t N, int32_t* cnt, unsigned long long* tot, uint32_t* err) {
-  extern __shared__ uint32_t sm[];
+  extern __shared__ __align__(16) uint32_t sm[];
   __shared__ int wsum[8];
-  const int32_t nw = (N + 31) >> 5;
+  const int32_t nw = bitmap_words(N), nw16 = bitmap_words16(N);
   uint32_t* bma = sm;
-  uint32_t* bmb = sm + nw;
+  uint32_t* bmb = sm + nw16;
   const int64_t item = blockIdx.x;
   const int64_t bh = item / nqt, qt = item % nqt;
   const int64_t qa = (slice_m == 64) ? 2 * qt : qt;
@@ -298,10 +322,10 @@ __global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
     return;
   }
   const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
-  for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
+  for (int w = threadIdx.x; w < 2 * nw16; w += blockDim.x) sm[w] = 0u;
   __syncthreads();
-  bool bad = set_bits_checked(bma, L.a, L.na, N);
-  bad = set_bits_checked(bmb, L.b, L.nb, N) || bad;
+  bool bad = set_bits_vec<true>(bma, L.a, L.na, N);
+  bad = set_bits_vec<true>(bmb, L.b, L.nb, N) || bad;
   if (bad) atomicOr(err, DEV_ERR_BAD_INPUT);
   __syncthreads();
   int s = 0;
@@ -324,63 +348,102 @@ __global__ void __launch_bounds__(256) keylist_count_bitmap_kernel(
   }
 }
 
-// Shared memory of the bitmap emit kernel, in 32-bit words: the two lists'
-// key bitmaps, the union rank of each bitmap word, and the two membership masks
-// in union-rank order (4 words of slack: the last tile's mask words may reach
-// past the union).
+// The emit kernel runs 8 warps; each stages the union keys of one 32-word
+// chunk of the bitmaps (at most 1024) before writing them out in rank order.
+constexpr int kEmitWarps = 8;
+constexpr int kStageKeys = 1024;
+
+// Shared memory of the bitmap emit kernel, in 32-bit words: the two lists' key
+// bitmaps, the two membership masks in union-rank order (8 words of slack: the
+// last tile's mask words may reach past the union), and the warps' stages.
 __host__ __device__ constexpr size_t emit_bitmap_words(int32_t N) {
-  return 5 * static_cast<size_t>((N + 31) / 32) + 8;
+  return 2 * static_cast<size_t>(bitmap_words16(N)) + 2 * static_cast<size_t>(bitmap_words(N) + 8) +
+         static_cast<size_t>(kEmitWarps) * kStageKeys;
 }
 
+// One block per query tile.  Warp w owns a contiguous range of 32-word chunks
+// of the bitmaps; a first pass counts the union keys of each warp's range (the
+// block scan of those counts gives each warp its first rank), the second walks
+// the chunks in order: a warp scan of the words' popcounts places each word's
+// keys in the warp's stage, and the stage goes out to gidx in 32-aligned rank
+// groups, whose membership bits are one ballot per list.
 __global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
     const int64_t* indptr, const int32_t* indices, int32_t nqt, int32_t nqb, int32_t slice_m,
     int32_t N, int32_t bn, const int32_t* cnt_e, const int32_t* ebegin, int2* entries,
     uint32_t* descs, int32_t* gidx) {
-  extern __shared__ uint32_t sm[];
-  __shared__ int wsum[8];
-  const int32_t nw = (N + 31) >> 5;
+  extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ int wtot[kEmitWarps];
+  const int32_t nw = bitmap_words(N), nw16 = bitmap_words16(N);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* bma = sm;
-  uint32_t* bmb = sm + nw;
-  int32_t* pre = reinterpret_cast<int32_t*>(sm + 2 * nw);
-  uint32_t* rka = sm + 3 * nw;                  // membership of list a, union-rank order
-  uint32_t* rkb = sm + 4 * nw + 4;              // membership of list b
+  uint32_t* bmb = sm + nw16;
+  uint32_t* rka = sm + 2 * nw16;                 // membership of list a, union-rank order
+  uint32_t* rkb = rka + nw + 8;                  // membership of list b
+  uint32_t* stage = rkb + nw + 8 + warp * kStageKeys;
   const int64_t item = blockIdx.x;
   const Lists L = tile_lists(indptr, indices, item, nqt, nqb, slice_m, N);
   const int64_t e0 = ebegin[item];
   const int32_t ne = cnt_e[item];
-  for (int w = threadIdx.x; w < 2 * nw; w += blockDim.x) sm[w] = 0u;
-  for (int w = threadIdx.x; w < 2 * nw + 8; w += blockDim.x) rka[w] = 0u;
+  for (int w = threadIdx.x; w < 2 * nw16 + 2 * (nw + 8); w += blockDim.x) sm[w] = 0u;
   __syncthreads();
-  set_bits(bma, L.a, L.na);
-  set_bits(bmb, L.b, L.nb);
+  set_bits_vec<false>(bma, L.a, L.na, N);
+  set_bits_vec<false>(bmb, L.b, L.nb, N);
   __syncthreads();
-  const int32_t u = union_prefix(bma, bmb, pre, nw, wsum);
+  const int32_t nch = (nw + 31) >> 5, cpw = (nch + kEmitWarps - 1) / kEmitWarps;
+  const int32_t c0 = warp * cpw, c1 = min(nch, c0 + cpw);
+  int cnt = 0;
+  for (int32_t c = c0; c < c1; ++c) {
+    const int32_t w = c * 32 + lane;
+    if (w < nw) cnt += __popc(bma[w] | bmb[w]);
+  }
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+  if (lane == 0) wtot[warp] = cnt;
+  __syncthreads();
+  int32_t rank = 0, u = 0;
+  for (int i = 0; i < kEmitWarps; ++i) {
+    if (i < warp) rank += wtot[i];
+    u += wtot[i];
+  }
   int32_t* gx = gidx + e0 * bn;
   uint32_t* dw = descs + e0 * 8;
-  // Each thread takes whole bitmap words: their union keys go to consecutive
-  // ranks starting at pre[w] (so a warp's stores are contiguous), and their
-  // membership bits, shifted to rank order, touch at most two mask words.
-  for (int w = threadIdx.x; w < nw; w += blockDim.x) {
-    const uint32_t A = bma[w], Bm = bmb[w];
+  for (int32_t c = c0; c < c1; ++c) {
+    const int32_t w = c * 32 + lane;
+    const uint32_t A = w < nw ? bma[w] : 0u, Bm = w < nw ? bmb[w] : 0u;
     uint32_t bits = A | Bm;
-    if (!bits) continue;
-    const int32_t rank = pre[w];
-    const int sh = rank & 31;
-    uint64_t pa = 0, pb = 0;
-    int k = 0;
+    const int x = __popc(bits);
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int ctot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    // keys are below 2^30: bits 30 and 31 carry membership in a and b
+    int k = incl - x;
     while (bits) {
       const int bit = __ffs(bits) - 1;
       bits &= bits - 1u;
-      gx[rank + k] = (w << 5) + bit;
-      pa |= static_cast<uint64_t>((A >> bit) & 1u) << (sh + k);
-      pb |= static_cast<uint64_t>((Bm >> bit) & 1u) << (sh + k);
-      ++k;
+      stage[k++] = (static_cast<uint32_t>(w) << 5 | static_cast<uint32_t>(bit)) |
+                   ((A >> bit) & 1u) << 30 | ((Bm >> bit) & 1u) << 31;
     }
-    const int g = rank >> 5;
-    if (static_cast<uint32_t>(pa)) atomicOr(&rka[g], static_cast<uint32_t>(pa));
-    if (pa >> 32) atomicOr(&rka[g + 1], static_cast<uint32_t>(pa >> 32));
-    if (static_cast<uint32_t>(pb)) atomicOr(&rkb[g], static_cast<uint32_t>(pb));
-    if (pb >> 32) atomicOr(&rkb[g + 1], static_cast<uint32_t>(pb >> 32));
+    __syncwarp();
+    for (int32_t p0 = rank & ~31; p0 < rank + ctot; p0 += 32) {
+      const int32_t pp = p0 + lane;
+      const bool valid = pp >= rank && pp < rank + ctot;
+      uint32_t e = 0u;
+      if (valid) {
+        e = stage[pp - rank];
+        gx[pp] = static_cast<int32_t>(e & 0x3FFFFFFFu);
+      }
+      const uint32_t ma = __ballot_sync(0xFFFFFFFFu, valid && ((e >> 30) & 1u));
+      const uint32_t mb = __ballot_sync(0xFFFFFFFFu, valid && (e >> 31));
+      if (lane == 0) {
+        if (ma) atomicOr(&rka[p0 >> 5], ma);
+        if (mb) atomicOr(&rkb[p0 >> 5], mb);
+      }
+    }
+    __syncwarp();
+    rank += ctot;
   }
   // padding of the last tile: any in-range key; its columns stay masked
   for (int64_t q = u + threadIdx.x; q < static_cast<int64_t>(ne) * bn; q += blockDim.x) gx[q] = 0;
@@ -423,7 +486,6 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
   const int threads = 256;
   const bool bitmap = N <= kBitmapMaxN;
-  const size_t nw = static_cast<size_t>((N + 31) / 32);
   unsigned long long* host_tot = P->host_tot;
   const char* bad_lists =
       "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward";
@@ -433,14 +495,15 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
     if (P->device < 0 || P->device >= 64 || !attr_done[P->device]) {
       TSR_CUDA(cudaFuncSetAttribute(keylist_count_bitmap_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(2 * 4 * ((kBitmapMaxN + 31) / 32))));
+                                    static_cast<int>(2 * 4 * bitmap_words16(kBitmapMaxN))));
       TSR_CUDA(cudaFuncSetAttribute(keylist_emit_bitmap_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(4 * emit_bitmap_words(kBitmapMaxN))));
       if (P->device >= 0 && P->device < 64) attr_done[P->device] = true;
     }
     if (n_items > 0) {
-      keylist_count_bitmap_kernel<<<static_cast<unsigned>(n_items), 256, 2 * 4 * nw, stream>>>(
+      keylist_count_bitmap_kernel<<<static_cast<unsigned>(n_items), 256,
+                                    2 * 4 * static_cast<size_t>(bitmap_words16(N)), stream>>>(
           mask->indptr, mask->indices, n_items, nqt, nqb, M, N, cnt, tot, P->err);
       TSR_CUDA(cudaGetLastError());
     }
