@@ -504,6 +504,9 @@ def main():
                                             indptr=spec.indptr, indices=spec.indices).items()
                 if v2 is not None}
         mask_bytes = sum(np.asarray(v2).nbytes for v2 in marr.values() if isinstance(v2, np.ndarray))
+        # the mask arrays are inputs of the step too: pinned like Q, K, V
+        marr = {k2: (torch.from_numpy(np.ascontiguousarray(v2)).pin_memory()
+                     if isinstance(v2, np.ndarray) else v2) for k2, v2 in marr.items()}
 
         def host_call():
             tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, D, qh, kh, vh, oh, lh, **marr)

@@ -295,8 +295,12 @@ tsr_status check_tiles_done(const tsr_plan_s* const* plans, int n, cudaStream_t 
 struct HostCache {
   void* buf[8] = {nullptr};
   size_t cap[8] = {0};
-  cudaStream_t stream = nullptr;               // attention
+  cudaStream_t stream = nullptr, stream2 = nullptr;   // attention, alternating by group
   cudaStream_t s_in = nullptr, s_out = nullptr, s_plan = nullptr;
+  uint32_t* host_err = nullptr;                // pinned: one error word per head group
+  size_t host_err_cap = 0;
+  int64_t* stage = nullptr;                    // pinned: rebased key-list indptr slices
+  size_t stage_cap = 0;
   std::vector<cudaEvent_t> ev;                 // 3 per head group: inputs, plan, attention
   std::vector<tsr_plan_t> plans;               // one per head group
   std::vector<std::array<int64_t, 9>> plan_key;
@@ -312,10 +316,16 @@ struct HostCache {
       buf[i] = nullptr;
       cap[i] = 0;
     }
-    for (cudaStream_t* s : {&stream, &s_in, &s_out, &s_plan}) {
+    for (cudaStream_t* s : {&stream, &stream2, &s_in, &s_out, &s_plan}) {
       if (*s) cudaStreamDestroy(*s);
       *s = nullptr;
     }
+    if (host_err) cudaFreeHost(host_err);
+    host_err = nullptr;
+    host_err_cap = 0;
+    if (stage) cudaFreeHost(stage);
+    stage = nullptr;
+    stage_cap = 0;
     device = -1;
   }
   ~HostCache() { release(); }
@@ -605,7 +615,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     hc.release();
     hc.device = dev;
   }
-  for (cudaStream_t* st : {&hc.stream, &hc.s_in, &hc.s_out, &hc.s_plan})
+  for (cudaStream_t* st : {&hc.stream, &hc.stream2, &hc.s_in, &hc.s_out, &hc.s_plan})
     if (!*st) TSR_CUDA(cudaStreamCreateWithFlags(st, cudaStreamNonBlocking));
   const int64_t BH = static_cast<int64_t>(mask->B) * mask->H;
   const size_t row_b = static_cast<size_t>(mask->N) * mask->d * 2;   // one head of Q, K, V or O
@@ -642,13 +652,16 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   if (tsr_status s = hc.get(2, tb, &dv)) return s;
   if (tsr_status s = hc.get(3, tb, &dout)) return s;
   if (tsr_status s = hc.get(4, lb, &dlse)) return s;
-  while (static_cast<int64_t>(hc.ev.size()) < 3 * G) {
+  while (static_cast<int64_t>(hc.ev.size()) < 4 * G) {
     cudaEvent_t e;
     TSR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     hc.ev.push_back(e);
   }
   // 1. the mask to the device, and one mask view per head group
   cudaStream_t sp = hc.s_plan;
+  std::vector<int64_t> kl_start, kl_base;      // key lists: per-group slices
+  void* kl_dp = nullptr;
+  void* kl_di = nullptr;
   std::vector<tsr_mask> views(G, *mask);
   const int64_t nqb = (mask->kind == TSR_MASK_KEYLIST) ? (mask->N + mask->slice_m - 1) / mask->slice_m : 0;
   if (mask->kind == TSR_MASK_UNIFORM || mask->kind == TSR_MASK_SEGMENTS) {
@@ -681,28 +694,31 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     const int64_t n_idx = mask->indptr[n_lists];   // HOST arrays here
     if (n_idx < 0 || mask->indptr[0] != 0)
       return fail(TSR_ERR_INVALID_ARG, "indptr must run upward from 0");
-    // each group's slice of indptr, rebased to start at 0
-    std::vector<int64_t> rebased;
-    rebased.reserve(n_lists + G);
-    std::vector<int64_t> start(G), base(G);
+    // each group's slice of indptr, rebased to start at 0, staged in pinned
+    // memory; the slices and their keys are copied per group in step 2
+    const size_t n_stage = static_cast<size_t>(n_lists + G);
+    if (hc.stage_cap < n_stage) {
+      if (hc.stage) cudaFreeHost(hc.stage);
+      hc.stage = nullptr;
+      hc.stage_cap = 0;
+      TSR_CUDA(cudaMallocHost(&hc.stage, sizeof(int64_t) * n_stage));
+      hc.stage_cap = n_stage;
+    }
+    kl_start.resize(G);
+    kl_base.resize(G + 1);
+    int64_t pos = 0;
     for (int64_t g = 0; g < G; ++g) {
       const int64_t l0 = gs[g] * nqb, l1 = gs[g + 1] * nqb;
-      start[g] = static_cast<int64_t>(rebased.size());
-      base[g] = mask->indptr[l0];
-      for (int64_t l = l0; l <= l1; ++l) rebased.push_back(mask->indptr[l] - base[g]);
+      kl_start[g] = pos;
+      kl_base[g] = mask->indptr[l0];
+      for (int64_t l = l0; l <= l1; ++l) hc.stage[pos++] = mask->indptr[l] - kl_base[g];
     }
-    void *dp, *di;
-    if (tsr_status s = hc.get(5, sizeof(int64_t) * rebased.size(), &dp)) return s;
-    if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &di)) return s;
-    TSR_CUDA(cudaMemcpyAsync(dp, rebased.data(), sizeof(int64_t) * rebased.size(),
-                             cudaMemcpyHostToDevice, sp));
-    if (n_idx)
-      TSR_CUDA(cudaMemcpyAsync(di, mask->indices, sizeof(int32_t) * n_idx, cudaMemcpyHostToDevice, sp));
-    // the rebased copy must reach the device before the host vector goes away
-    TSR_CUDA(cudaStreamSynchronize(sp));
+    kl_base[G] = n_idx;
+    if (tsr_status s = hc.get(5, sizeof(int64_t) * n_stage, &kl_dp)) return s;
+    if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &kl_di)) return s;
     for (int64_t g = 0; g < G; ++g) {
-      views[g].indptr = static_cast<const int64_t*>(dp) + start[g];
-      views[g].indices = static_cast<const int32_t*>(di) + base[g];
+      views[g].indptr = static_cast<const int64_t*>(kl_dp) + kl_start[g];
+      views[g].indices = static_cast<const int32_t*>(kl_di) + kl_base[g];
     }
   } else if (mask->kind == TSR_MASK_SVG) {
     // head kinds of the flattened (b, h) order
@@ -715,20 +731,35 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + gs[g];
   }
   // 2. inputs, group by group (queued after the mask, which the copy engine
-  // would otherwise move only after every input)
+  // would otherwise move only after every input); key lists go group by group
+  // too, each group's slice just ahead of its inputs, and its plan waits only
+  // for that slice
   const char* hq = static_cast<const char*>(q);
   const char* hk = static_cast<const char*>(k);
   const char* hv = static_cast<const char*>(v);
   for (int64_t g = 0; g < G; ++g) {
     const int64_t b0 = gs[g], cnt = gs[g + 1] - gs[g];
     const size_t off = b0 * row_b, n = cnt * row_b;
+    if (mask->kind == TSR_MASK_KEYLIST) {
+      const int64_t n_ptr = cnt * nqb + 1, k0 = kl_base[g], k1 = kl_base[g + 1];
+      TSR_CUDA(cudaMemcpyAsync(static_cast<int64_t*>(kl_dp) + kl_start[g], hc.stage + kl_start[g],
+                               sizeof(int64_t) * n_ptr, cudaMemcpyHostToDevice, hc.s_in));
+      if (k1 > k0)
+        TSR_CUDA(cudaMemcpyAsync(static_cast<int32_t*>(kl_di) + k0, mask->indices + k0,
+                                 sizeof(int32_t) * (k1 - k0), cudaMemcpyHostToDevice, hc.s_in));
+      TSR_CUDA(cudaEventRecord(hc.ev[3 * G + g], hc.s_in));
+    }
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dq) + off, hq + off, n, cudaMemcpyHostToDevice, hc.s_in));
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dk) + off, hk + off, n, cudaMemcpyHostToDevice, hc.s_in));
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dv) + off, hv + off, n, cudaMemcpyHostToDevice, hc.s_in));
     TSR_CUDA(cudaEventRecord(hc.ev[3 * g], hc.s_in));
   }
-  // 3. one plan per head group, kept from call to call while the grouping and
-  // options are unchanged (re-planned for the new mask)
+  // 3. per head group: its plan (kept from call to call while the grouping and
+  // options are unchanged, re-planned for the new mask), then its attention
+  // once its inputs and plan are ready, then its outputs back.  Planning group
+  // g + 1 (one host synchronisation on the plan stream) overlaps attention g.
+  // Consecutive groups alternate between two attention streams, so one
+  // persistent launch's last CTAs overlap the next launch's first.
   const tsr_plan_opts zero{};
   const tsr_plan_opts& o = opts ? *opts : zero;
   if (static_cast<int64_t>(hc.plans.size()) != G) {
@@ -736,13 +767,21 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     hc.plans.assign(G, nullptr);
     hc.plan_key.assign(G, {});
   }
-  for (int64_t g = 0; g < G; ++g) {
+  if (hc.host_err_cap < static_cast<size_t>(G)) {
+    if (hc.host_err) cudaFreeHost(hc.host_err);
+    hc.host_err = nullptr;
+    hc.host_err_cap = 0;
+    TSR_CUDA(cudaMallocHost(&hc.host_err, sizeof(uint32_t) * G));
+    hc.host_err_cap = G;
+  }
+  tsr_status s = TSR_OK;
+  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
     tsr_mask& vw = views[g];
     vw.B = 1;
     vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
     const std::array<int64_t, 9> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
                                          o.flags, opts ? 1 : 0};
-    tsr_status s = TSR_OK;
+    if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
     if (hc.plans[g] && hc.plan_key[g] == key) {
       s = tsr_plan_update(hc.plans[g], &vw, sp);
     } else {
@@ -751,40 +790,45 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       s = tsr_plan(&vw, opts, &hc.plans[g], sp);
       hc.plan_key[g] = key;
     }
-    if (s != TSR_OK) {
-      // no copy may still read the caller's buffers after the return
-      cudaStreamSynchronize(hc.s_in);
-      cudaStreamSynchronize(sp);
-      return s;
-    }
+    if (s != TSR_OK) break;
     TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 1], sp));
-  }
-  // 4. attention per group once its inputs and plan are ready; 5. outputs back
-  tsr_status s = TSR_OK;
-  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+    cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
     const int64_t b0 = gs[g];
     const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
-    TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g], 0));
-    TSR_CUDA(cudaStreamWaitEvent(hc.stream, hc.ev[3 * g + 1], 0));
+    TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
+    TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g + 1], 0));
     s = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
                         static_cast<char*>(dv) + off, hc.plans[g], static_cast<char*>(dout) + off,
-                        static_cast<float*>(dlse) + b0 * mask->N, hc.stream);
+                        static_cast<float*>(dlse) + b0 * mask->N, sa);
     if (s != TSR_OK) break;
-    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], hc.stream));
+    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
     TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
                              cudaMemcpyDeviceToHost, hc.s_out));
     TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
                              static_cast<size_t>(n / row_b) * mask->N * 4, cudaMemcpyDeviceToHost,
                              hc.s_out));
+    // the group's device error word (its kernels have run once s_out gets here)
+    TSR_CUDA(cudaMemcpyAsync(hc.host_err + g, hc.plans[g]->err, sizeof(uint32_t),
+                             cudaMemcpyDeviceToHost, hc.s_out));
+    TSR_CUDA(cudaMemsetAsync(hc.plans[g]->err, 0, sizeof(uint32_t), hc.s_out));
   }
+  // no copy may still read or write the caller's buffers after the return
   const cudaError_t e1 = cudaStreamSynchronize(hc.s_out);
   const cudaError_t e2 = cudaStreamSynchronize(hc.stream);
+  const cudaError_t e4 = cudaStreamSynchronize(hc.stream2);
   const cudaError_t e3 = cudaStreamSynchronize(hc.s_in);
+  const cudaError_t e5 = cudaStreamSynchronize(sp);
   if (s == TSR_OK && e1 != cudaSuccess) s = cuda_fail(e1, "copy of the outputs to host");
-  if (s == TSR_OK && e2 != cudaSuccess) s = cuda_fail(e2, "attention stream");
+  if (s == TSR_OK && (e2 != cudaSuccess || e4 != cudaSuccess))
+    s = cuda_fail(e2 != cudaSuccess ? e2 : e4, "attention stream");
   if (s == TSR_OK && e3 != cudaSuccess) s = cuda_fail(e3, "copy of the inputs");
-  for (int64_t g = 0; g < G && s == TSR_OK; ++g) s = tsr_plan_device_status(hc.plans[g], hc.stream);
+  if (s == TSR_OK && e5 != cudaSuccess) s = cuda_fail(e5, "plan stream");
+  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+    const uint32_t e = hc.host_err[g];
+    if (e & DEV_ERR_TIMEOUT) s = fail(TSR_ERR_TIMEOUT, "a device-side wait timed out");
+    else if (e) s = fail(TSR_ERR_INTERNAL, "device error word " + std::to_string(e));
+  }
   return s;
 }
 
