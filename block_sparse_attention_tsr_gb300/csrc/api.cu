@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <algorithm>
 #include <array>
+#include <cmath>
 #include <cstring>
 #include <fstream>
 #include <mutex>
@@ -621,29 +622,29 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   const size_t row_b = static_cast<size_t>(mask->N) * mask->d * 2;   // one head of Q, K, V or O
   const size_t tb = BH * row_b;
   const size_t lb = static_cast<size_t>(BH) * mask->N * 4;
-  // Heads are processed in groups of about 160 MB of Q, K and V: the inputs of
-  // group g + 1 are copied in while group g is attended and group g - 1 is
-  // copied out (three streams; the copy engines and the SMs overlap).
-  const int64_t n_groups = std::max<int64_t>(
-      1, std::min<int64_t>(BH, static_cast<int64_t>((3 * tb + (160u << 20) - 1) / (160u << 20))));
-  // Group g holds heads [gs[g], gs[g + 1]).  The first and the last groups are
-  // about a third of the others: the first group's copy-in and the last
-  // group's copy-out are the parts no attention overlaps.
+  // Heads are processed in groups: the inputs of group g + 1 are copied in while
+  // group g is attended and group g - 1 is copied out (copy engines and SMs
+  // overlap).  Only the first group's copy-in and the last group's copy-out are
+  // exposed, so the groups grow from one head by a factor of 1.5 (attention of
+  // a group then covers the copy-in of the next whenever attending a head takes
+  // at least 1.5x as long as copying it in) up to about 160 MB of Q, K and V,
+  // and the last two groups are two heads and one.
   std::vector<int64_t> gs{0};
   {
-    const int64_t per = (BH + n_groups - 1) / n_groups;
-    const int64_t edge = (n_groups >= 3) ? std::max<int64_t>(1, per / 3) : 0;
-    if (edge > 0 && BH > 2 * edge) {
-      const int64_t mid = BH - 2 * edge, n_mid = n_groups - 1;
-      gs.push_back(edge);
-      for (int64_t i = 1; i <= n_mid; ++i) gs.push_back(edge + (mid * i + n_mid - 1) / n_mid);
-      gs.push_back(BH);
-    } else {
-      for (int64_t b = per; b < BH; b += per) gs.push_back(b);
-      gs.push_back(BH);
+    const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>((160u << 20) / (3 * row_b)));
+    const int64_t tail = BH >= 8 ? 3 : 0;
+    int64_t left = BH - tail;
+    double r = 1.0;
+    while (left > 0) {
+      const int64_t sz = std::min<int64_t>({cap, static_cast<int64_t>(std::ceil(r)), left});
+      gs.push_back(gs.back() + sz);
+      left -= sz;
+      r *= 1.5;
     }
-    // drop empty groups
-    gs.erase(std::unique(gs.begin(), gs.end()), gs.end());
+    if (tail) {
+      gs.push_back(gs.back() + 2);
+      gs.push_back(gs.back() + 1);
+    }
   }
   const int64_t G = static_cast<int64_t>(gs.size()) - 1;
   void *dq, *dk, *dv, *dout, *dlse;
@@ -755,11 +756,13 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     TSR_CUDA(cudaEventRecord(hc.ev[3 * g], hc.s_in));
   }
   // 3. per head group: its plan (kept from call to call while the grouping and
-  // options are unchanged, re-planned for the new mask), then its attention
-  // once its inputs and plan are ready, then its outputs back.  Planning group
-  // g + 1 (one host synchronisation on the plan stream) overlaps attention g.
-  // Consecutive groups alternate between two attention streams, so one
-  // persistent launch's last CTAs overlap the next launch's first.
+  // options are unchanged, re-planned for the new mask), its attention once its
+  // inputs and plan are ready, and its outputs back.  Planning group g + 1 (one
+  // host synchronisation on the plan stream) overlaps attention g.  (Planning
+  // two groups ahead measured slower: a key-list plan then waits for a slice
+  // queued behind the next group's inputs.)  Consecutive groups alternate
+  // between two attention streams, so one persistent launch's last CTAs
+  // overlap the next one's first.
   const tsr_plan_opts zero{};
   const tsr_plan_opts& o = opts ? *opts : zero;
   if (static_cast<int64_t>(hc.plans.size()) != G) {
@@ -774,33 +777,37 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     TSR_CUDA(cudaMallocHost(&hc.host_err, sizeof(uint32_t) * G));
     hc.host_err_cap = G;
   }
-  tsr_status s = TSR_OK;
-  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+  auto plan_group = [&](int64_t g) -> tsr_status {
     tsr_mask& vw = views[g];
     vw.B = 1;
     vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
     const std::array<int64_t, 9> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
                                          o.flags, opts ? 1 : 0};
     if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
+    tsr_status st;
     if (hc.plans[g] && hc.plan_key[g] == key) {
-      s = tsr_plan_update(hc.plans[g], &vw, sp);
+      st = tsr_plan_update(hc.plans[g], &vw, sp);
     } else {
       if (hc.plans[g]) tsr_plan_destroy(hc.plans[g]);
       hc.plans[g] = nullptr;
-      s = tsr_plan(&vw, opts, &hc.plans[g], sp);
+      st = tsr_plan(&vw, opts, &hc.plans[g], sp);
       hc.plan_key[g] = key;
     }
-    if (s != TSR_OK) break;
+    if (st != TSR_OK) return st;
     TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 1], sp));
+    return TSR_OK;
+  };
+  auto launch_group = [&](int64_t g) -> tsr_status {
     cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
     const int64_t b0 = gs[g];
     const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
     TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
     TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g + 1], 0));
-    s = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
-                        static_cast<char*>(dv) + off, hc.plans[g], static_cast<char*>(dout) + off,
-                        static_cast<float*>(dlse) + b0 * mask->N, sa);
-    if (s != TSR_OK) break;
+    if (tsr_status st = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
+                                        static_cast<char*>(dv) + off, hc.plans[g],
+                                        static_cast<char*>(dout) + off,
+                                        static_cast<float*>(dlse) + b0 * mask->N, sa))
+      return st;
     TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
     TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
     TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
@@ -812,6 +819,12 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     TSR_CUDA(cudaMemcpyAsync(hc.host_err + g, hc.plans[g]->err, sizeof(uint32_t),
                              cudaMemcpyDeviceToHost, hc.s_out));
     TSR_CUDA(cudaMemsetAsync(hc.plans[g]->err, 0, sizeof(uint32_t), hc.s_out));
+    return TSR_OK;
+  };
+  tsr_status s = TSR_OK;
+  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+    s = plan_group(g);
+    if (s == TSR_OK) s = launch_group(g);
   }
   // no copy may still read or write the caller's buffers after the return
   const cudaError_t e1 = cudaStreamSynchronize(hc.s_out);
