@@ -232,6 +232,7 @@ void free_plan(tsr_plan_s* P) {
   cudaFree(P->err);
   cudaFree(P->head_kind_dev);
   if (P->host_tot) cudaFreeHost(P->host_tot);
+  if (P->host_kinds) cudaFreeHost(P->host_kinds);
   delete P;
 }
 
@@ -245,19 +246,17 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
     if (tsr_status s = check_bounds(mask->k_bounds, mask->n_kseg, mask->N, st)) return s;
   }
   if (mask->kind == TSR_MASK_SVG) {
-    TSR_CUDA(cudaMemcpyAsync(P->head_layout.data(), mask->head_kind, mask->H,
-                             cudaMemcpyDeviceToHost, st));
-    TSR_CUDA(cudaStreamSynchronize(st));
-    for (int32_t h = 0; h < mask->H; ++h) {
-      if (P->head_layout[h] != TSR_HEAD_SPATIAL && P->head_layout[h] != TSR_HEAD_TEMPORAL)
-        return fail(TSR_ERR_INVALID_ARG, "head_kind values must be 0 or 1");
-      P->n_temporal += P->head_layout[h];
-    }
+    // The head kinds, copied on the stream without a synchronisation of their
+    // own: the device copy feeds the planner kernels (which only compare a
+    // kind with TSR_HEAD_TEMPORAL, so an invalid value cannot misaddress), the
+    // pinned host copy is checked after the planner's count synchronisation.
     P->F = mask->n_frames;
     P->S = mask->frame_size;
     if (!P->head_kind_dev) TSR_CUDA(cudaMalloc(&P->head_kind_dev, mask->H));
-    TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, P->head_layout.data(), mask->H,
-                             cudaMemcpyHostToDevice, st));
+    if (!P->host_kinds) TSR_CUDA(cudaMallocHost(&P->host_kinds, mask->H));
+    TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, mask->head_kind, mask->H, cudaMemcpyDeviceToDevice,
+                             st));
+    TSR_CUDA(cudaMemcpyAsync(P->host_kinds, mask->head_kind, mask->H, cudaMemcpyDeviceToHost, st));
   }
   P->gathered = 0;
   P->slice_m = 0;

@@ -72,6 +72,7 @@ struct tsr_plan_impl {
   // storage reused when the plan is rebuilt for a new mask (tsr_plan_update)
   DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist, b_gidx;
   unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
+  int8_t* host_kinds = nullptr;             // pinned: SVG head kinds, read after the count sync
   bool has_opts = false;
   tsr_plan_opts opts{};
 };

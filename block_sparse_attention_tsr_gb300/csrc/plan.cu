@@ -35,11 +35,14 @@ constexpr int kMaxSeg = 8;
 
 // Logical segments of one axis (0 = queries, 1 = keys) that overlap tokens
 // [t0, t1) of head h.  ids[] receive segment ids, starts[] the first token of
-// each relative to t0, starts[n] = t1 - t0.  Returns the count, or -1 if more
-// than kMaxSeg segments overlap.
-__device__ int tile_segments(const MaskDev& m, int h, int axis, int t0, int t1, int* ids,
-                             int* starts) {
+// each relative to t0; entries from the count on hold t1 - t0 (so starts[n] =
+// t1 - t0).  Returns the count, or -1 if more than kMaxSeg segments overlap.
+// The overlapping segments are consecutive ids, so every array index below is
+// a compile-time constant and the arrays stay in registers.
+__device__ __forceinline__ int tile_segments(const MaskDev& m, int h, int axis, int t0, int t1,
+                                             int (&ids)[kMaxSeg], int (&starts)[kMaxSeg + 1]) {
   int n = 0;
+  bool more = false;                 // a (kMaxSeg + 1)-th segment overlaps
   if (m.kind == TSR_MASK_SEGMENTS) {
     const int32_t* bd = axis ? m.k_bounds : m.q_bounds;
     const int ns = axis ? m.n_kseg : m.n_qseg;
@@ -48,25 +51,33 @@ __device__ int tile_segments(const MaskDev& m, int h, int axis, int t0, int t1, 
       const int mid = (lo + hi + 1) >> 1;
       if (bd[mid] <= t0) lo = mid; else hi = mid - 1;
     }
-    for (int id = lo; id < ns && bd[id] < t1; ++id) {
-      if (n == kMaxSeg) return -1;
-      ids[n] = id;
-      starts[n] = max(bd[id], t0) - t0;
-      ++n;
+#pragma unroll
+    for (int k = 0; k < kMaxSeg; ++k) {
+      const int id = lo + k;
+      const int b = id < ns ? bd[id] : t1;
+      const bool v = b < t1;
+      ids[k] = id;
+      starts[k] = v ? max(b, t0) - t0 : t1 - t0;
+      n += v;
     }
+    more = lo + kMaxSeg < ns && bd[lo + kMaxSeg] < t1;
   } else {
     int size;
     if (m.kind == TSR_MASK_UNIFORM) size = axis ? m.bk : m.bq;
     else size = (m.head_kind[h] == TSR_HEAD_TEMPORAL) ? m.F : m.S;  // SVG
-    for (int id = t0 / size; id * size < t1; ++id) {
-      if (n == kMaxSeg) return -1;
-      ids[n] = id;
-      starts[n] = max(id * size, t0) - t0;
-      ++n;
+    const int first = t0 / size;
+#pragma unroll
+    for (int k = 0; k < kMaxSeg; ++k) {
+      const int id = first + k;
+      const bool v = id * size < t1;
+      ids[k] = id;
+      starts[k] = v ? max(id * size, t0) - t0 : t1 - t0;
+      n += v;
     }
+    more = (first + kMaxSeg) * size < t1;
   }
-  starts[n] = t1 - t0;
-  return n;
+  starts[kMaxSeg] = t1 - t0;
+  return more ? -1 : n;
 }
 
 __device__ __forceinline__ bool seg_allowed(const MaskDev& m, int bh, int h, int qid, int kid,
@@ -118,22 +129,37 @@ __device__ int classify(const MaskDev& m, int bh, int h, const RowSegs& rs, int 
   if (nc < 0 || rs.n < 0) return -1;
   uint64_t bits = 0;
   bool any = false, all = true;
-  for (int r = 0; r < rs.n; ++r)
-    for (int c = 0; c < nc; ++c) {
+#pragma unroll
+  for (int r = 0; r < kMaxSeg; ++r) {
+    if (r >= rs.n) break;
+#pragma unroll
+    for (int c = 0; c < kMaxSeg; ++c) {
+      if (c >= nc) break;
       const bool a = seg_allowed(m, bh, h, rs.ids[r], cid[c], nqs, nks);
       any |= a;
       all &= a;
       if (a) bits |= 1ull << (r * 8 + c);
     }
+  }
   if (!any) return 0;
   if (all && k1 - k0 == bn) return 1;
   if (desc) {
-    memset(desc, 0, sizeof(*desc));
-    desc->n_r = static_cast<uint8_t>(rs.n);
-    desc->n_c = static_cast<uint8_t>(nc);
-    for (int r = 0; r < rs.n; ++r) desc->r_start[r] = static_cast<uint8_t>(rs.starts[r]);
-    for (int c = 0; c <= nc; ++c) desc->c_start[c] = static_cast<uint8_t>(cst[c]);
-    desc->bits = bits;
+    // the 32-byte descriptor as 8 words: n_r, n_c, r_start[8], c_start[9], pad,
+    // bits (byte offsets 0, 1, 2..9, 10..18, 19..23, 24..31)
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    auto put = [&](int byte, uint32_t v) { w[byte >> 2] |= (v & 0xFFu) << ((byte & 3) * 8); };
+    put(0, static_cast<uint32_t>(rs.n));
+    put(1, static_cast<uint32_t>(nc));
+#pragma unroll
+    for (int r = 0; r < kMaxSeg; ++r)
+      if (r < rs.n) put(2 + r, static_cast<uint32_t>(rs.starts[r]));
+#pragma unroll
+    for (int c = 0; c <= kMaxSeg; ++c)
+      if (c <= nc) put(10 + c, static_cast<uint32_t>(cst[c]));
+    w[6] = static_cast<uint32_t>(bits);
+    w[7] = static_cast<uint32_t>(bits >> 32);
+    static_assert(sizeof(tsr_tile_desc) == 32, "descriptor size");
+    memcpy(desc, w, 32);
   }
   return 2;
 }
@@ -199,126 +225,192 @@ __device__ void grid_dims(const MaskDev& m, int64_t* nqs, int64_t* nks) {
 // longest item at BN=64 / 128, [6] allowed logical blocks.
 __global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
                                   uint32_t* err) {
+  __shared__ unsigned long long bsum[6];
+  if (threadIdx.x < 6) bsum[threadIdx.x] = 0;
+  __syncthreads();
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
-  if (warp >= n_items) return;
-  const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
-  RowSegs rs;
-  rs.q0 = qt * kBM;
-  rs.q1 = min(m.N, qt * kBM + kBM);
-  rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
-             ? 0
-             : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
-  int64_t nqs, nks;
-  grid_dims(m, &nqs, &nks);
-  const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), 128);
-  const int n_kt = kw.size();
-  int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
-  bool bad = false;
-  for (int i = lane; i < n_kt; i += 32) {
-    const int kt = kw.tile(i);
-    const int ca = classify(m, bh, h, rs, kt * 128, 64, nqs, nks, nullptr);
-    const int cb = classify(m, bh, h, rs, kt * 128 + 64, 64, nqs, nks, nullptr);
-    if (ca < 0 || cb < 0) {
-      bad = true;
-      continue;
+  if (warp < n_items) {
+    const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
+    RowSegs rs;
+    rs.q0 = qt * kBM;
+    rs.q1 = min(m.N, qt * kBM + kBM);
+    rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
+               ? 0
+               : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
+    int64_t nqs, nks;
+    grid_dims(m, &nqs, &nks);
+    const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), 128);
+    const int n_kt = kw.size();
+    int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
+    bool bad = false;
+    for (int i = lane; i < n_kt; i += 32) {
+      const int kt = kw.tile(i);
+      const int ca = classify(m, bh, h, rs, kt * 128, 64, nqs, nks, nullptr);
+      const int cb = classify(m, bh, h, rs, kt * 128 + 64, 64, nqs, nks, nullptr);
+      if (ca < 0 || cb < 0) {
+        bad = true;
+        continue;
+      }
+      e64 += (ca != 0) + (cb != 0);
+      b64 += (ca == 2) + (cb == 2);
+      if (ca != 0 || cb != 0) {
+        ++e128;
+        if (!(ca == 1 && cb == 1)) ++b128;
+      }
     }
-    e64 += (ca != 0) + (cb != 0);
-    b64 += (ca == 2) + (cb == 2);
-    if (ca != 0 || cb != 0) {
-      ++e128;
-      if (!(ca == 1 && cb == 1)) ++b128;
+    for (int o = 16; o > 0; o >>= 1) {
+      e64 += __shfl_xor_sync(0xFFFFFFFFu, e64, o);
+      b64 += __shfl_xor_sync(0xFFFFFFFFu, b64, o);
+      e128 += __shfl_xor_sync(0xFFFFFFFFu, e128, o);
+      b128 += __shfl_xor_sync(0xFFFFFFFFu, b128, o);
+    }
+    if (__any_sync(0xFFFFFFFFu, bad)) {
+      if (lane == 0) atomicOr(err, DEV_ERR_UNSUPPORTED);
+    } else if (lane == 0) {
+      cnt[0 * n_items + warp] = e64;
+      cnt[1 * n_items + warp] = b64;
+      cnt[2 * n_items + warp] = e128;
+      cnt[3 * n_items + warp] = b128;
+      atomicAdd(&bsum[0], static_cast<unsigned long long>(e64));
+      atomicAdd(&bsum[1], static_cast<unsigned long long>(b64));
+      atomicAdd(&bsum[2], static_cast<unsigned long long>(e128));
+      atomicAdd(&bsum[3], static_cast<unsigned long long>(b128));
+      atomicMax(&bsum[4], static_cast<unsigned long long>(e64));
+      atomicMax(&bsum[5], static_cast<unsigned long long>(e128));
     }
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    e64 += __shfl_xor_sync(0xFFFFFFFFu, e64, o);
-    b64 += __shfl_xor_sync(0xFFFFFFFFu, b64, o);
-    e128 += __shfl_xor_sync(0xFFFFFFFFu, e128, o);
-    b128 += __shfl_xor_sync(0xFFFFFFFFu, b128, o);
-  }
-  if (__any_sync(0xFFFFFFFFu, bad)) {
-    if (lane == 0) atomicOr(err, DEV_ERR_UNSUPPORTED);
-    return;
-  }
-  if (lane == 0) {
-    cnt[0 * n_items + warp] = e64;
-    cnt[1 * n_items + warp] = b64;
-    cnt[2 * n_items + warp] = e128;
-    cnt[3 * n_items + warp] = b128;
-    atomicAdd(&tot[0], static_cast<unsigned long long>(e64));
-    atomicAdd(&tot[1], static_cast<unsigned long long>(b64));
-    atomicAdd(&tot[2], static_cast<unsigned long long>(e128));
-    atomicAdd(&tot[3], static_cast<unsigned long long>(b128));
-    atomicMax(&tot[4], static_cast<unsigned long long>(e64));
-    atomicMax(&tot[5], static_cast<unsigned long long>(e128));
+  // one set of global atomics per block
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    if (bsum[threadIdx.x]) atomicAdd(&tot[threadIdx.x], bsum[threadIdx.x]);
+  } else if (threadIdx.x < 6) {
+    atomicMax(&tot[threadIdx.x], bsum[threadIdx.x]);
   }
 }
 
-// Number of allowed logical blocks (density for the regime table).
+// Number of allowed logical blocks (density for the regime table): 16 bytes
+// per load where the array is 16-byte aligned, single bytes for the rest.
 __global__ void logical_count_kernel(const uint8_t* blocks, int64_t n, unsigned long long* out) {
   unsigned long long c = 0;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    c += blocks[i] != 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t head = min(n, static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(blocks) & 15)) & 15));
+  const int64_t n16 = (n - head) >> 4;
+  const uint4* v = reinterpret_cast<const uint4*>(blocks + head);
+  auto nz = [](uint32_t w) {   // non-zero bytes of a word
+    return __popc(((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu | w) & 0x80808080u);
+  };
+  for (int64_t i = t; i < n16; i += stride) {
+    const uint4 x = __ldg(v + i);
+    c += nz(x.x) + nz(x.y) + nz(x.z) + nz(x.w);
+  }
+  for (int64_t i = t; i < head; i += stride) c += blocks[i] != 0;
+  for (int64_t i = head + 16 * n16 + t; i < n; i += stride) c += blocks[i] != 0;
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(out, c);
 }
 
-// Exclusive scan of n values with one block.
-__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int64_t n, int64_t* sh) {
-  const int T = blockDim.x, tid = threadIdx.x;
+// Exclusive scans of a[0, n) and, if b is not null, b[0, n) with one block
+// (a multiple of 32 threads, at most 1024): each thread sums a contiguous run
+// of ceil(n / T) values, warp shuffles and one shared array of warp totals give
+// every run its offset, and the run is written back (out may equal in).
+__device__ void block_scan_runs(const int32_t* a, const int32_t* b, int32_t* oa, int32_t* ob,
+                                int64_t n, int32_t* wa, int32_t* wb) {
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
   const int64_t per = (n + T - 1) / T;
   const int64_t lo = min(n, static_cast<int64_t>(tid) * per), hi = min(n, lo + per);
-  int64_t s = 0;
-  for (int64_t i = lo; i < hi; ++i) s += in[i];
-  sh[tid] = s;
-  __syncthreads();
-  for (int o = 1; o < T; o <<= 1) {
-    const int64_t v = (tid >= o) ? sh[tid - o] : 0;
-    __syncthreads();
-    sh[tid] += v;
-    __syncthreads();
-  }
-  int64_t run = sh[tid] - s;
+  int32_t sa = 0, sb = 0;
   for (int64_t i = lo; i < hi; ++i) {
-    const int32_t v = in[i];
-    out[i] = static_cast<int32_t>(run);
-    run += v;
+    sa += a[i];
+    if (b) sb += b[i];
+  }
+  int32_t xa = sa, xb = sb;                    // inclusive scan over the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t ya = __shfl_up_sync(0xFFFFFFFFu, xa, o), yb = __shfl_up_sync(0xFFFFFFFFu, xb, o);
+    if (lane >= o) {
+      xa += ya;
+      xb += yb;
+    }
+  }
+  if (lane == 31) {
+    wa[warp] = xa;
+    wb[warp] = xb;
+  }
+  __syncthreads();
+  if (warp == 0) {                             // exclusive scan of the warp totals
+    const int32_t va = lane < nw ? wa[lane] : 0, vb = lane < nw ? wb[lane] : 0;
+    int32_t ia = va, ib = vb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t ya = __shfl_up_sync(0xFFFFFFFFu, ia, o), yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+      if (lane >= o) {
+        ia += ya;
+        ib += yb;
+      }
+    }
+    if (lane < nw) {
+      wa[lane] = ia - va;
+      wb[lane] = ib - vb;
+    }
+  }
+  __syncthreads();
+  int32_t ra = wa[warp] + xa - sa, rb = wb[warp] + xb - sb;
+  for (int64_t i = lo; i < hi; ++i) {
+    const int32_t va = a[i];
+    oa[i] = ra;
+    ra += va;
+    if (b) {
+      const int32_t vb = b[i];
+      ob[i] = rb;
+      rb += vb;
+    }
   }
   __syncthreads();
 }
 
+// Largest LPT histogram kept in shared memory (32-bit buckets).
+constexpr int64_t kSharedBuckets = 12288;
+
 // One block: tile offsets, descriptor offsets and the work items.  With lpt the
 // items are ordered by head group (group_heads consecutive (b, h) per group,
 // sized so a group's K and V stay in L2), and longest first inside a group
-// (counting sort over n_groups x (max_len + 1) buckets).
+// (counting sort over n_groups x (max_len + 1) buckets, in shared memory when
+// there are at most kSharedBuckets, else in `hist`).
 __global__ void __launch_bounds__(1024) plan_schedule_kernel(
     const int32_t* cnt_e, const int32_t* cnt_b, int64_t n_items, int32_t nqt, int32_t H,
     const int8_t* head_kind, int32_t is_svg, int32_t max_len, int32_t lpt, int32_t group_heads,
     int64_t n_buckets, int32_t* ebegin, int32_t* dbegin, int32_t* hist, int4* items) {
-  __shared__ int64_t sh[1024];
-  block_exclusive_scan(cnt_e, ebegin, n_items, sh);
-  block_exclusive_scan(cnt_b, dbegin, n_items, sh);
+  extern __shared__ int32_t shist[];
+  __shared__ int32_t wa[32], wb[32];
+  block_scan_runs(cnt_e, cnt_b, ebegin, dbegin, n_items, wa, wb);
   const int T = blockDim.x, tid = threadIdx.x;
   const int64_t per_group = static_cast<int64_t>(group_heads) * nqt;
+  int32_t* hb = (n_buckets <= kSharedBuckets) ? shist : hist;
   if (lpt) {
-    for (int64_t i = tid; i < n_buckets; i += T) hist[i] = 0;
+    for (int64_t i = tid; i < n_buckets; i += T) hb[i] = 0;
     __syncthreads();
     for (int64_t i = tid; i < n_items; i += T)
-      atomicAdd(&hist[(i / per_group) * (max_len + 1) + (max_len - cnt_e[i])], 1);
+      atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - cnt_e[i])], 1);
     __syncthreads();
-    block_exclusive_scan(hist, hist, n_buckets, sh);   // in place: bucket start positions
+    block_scan_runs(hb, nullptr, hb, nullptr, n_buckets, wa, wb);   // bucket start positions
   }
   for (int64_t i = tid; i < n_items; i += T) {
     const int32_t len = cnt_e[i];
     const int64_t pos =
-        lpt ? atomicAdd(&hist[(i / per_group) * (max_len + 1) + (max_len - len)], 1) : i;
+        lpt ? atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - len)], 1) : i;
     const int32_t bh = static_cast<int32_t>(i / nqt), qt = static_cast<int32_t>(i % nqt);
     const int32_t layout = (is_svg && head_kind[bh % H] == TSR_HEAD_TEMPORAL) ? 1 : 0;
     items[2 * pos] = make_int4(bh, qt, ebegin[i], ebegin[i] + len);
     items[2 * pos + 1] = make_int4(layout, 0, 0, 0);
   }
+}
+
+// Dynamic shared memory of a plan_schedule_kernel launch.
+size_t schedule_smem(int64_t n_buckets) {
+  return n_buckets <= kSharedBuckets ? static_cast<size_t>(n_buckets) * 4 : 0;
 }
 
 __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32_t* ebegin,
@@ -387,7 +479,7 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
   const int threads = 256;
   const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
   const int32_t all_heads = static_cast<int32_t>(n_items / nqt);
-  plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, m.H, m.head_kind,
+  plan_schedule_kernel<<<1, 1024, schedule_smem(max_len + 1), stream>>>(cnt_e, cnt_b, n_items, nqt, m.H, m.head_kind,
                                                m.kind == TSR_MASK_SVG ? 1 : 0, max_len, 1,
                                                all_heads, max_len + 1, ebegin, dbegin, hist,
                                                static_cast<int4*>(items));
@@ -463,9 +555,10 @@ tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_
                               int32_t group_heads, int32_t* ebegin, int32_t* dbegin,
                               int32_t* hist, void* items, cudaStream_t stream) {
   const int64_t n_groups = (n_items / nqt + group_heads - 1) / group_heads;
-  plan_schedule_kernel<<<1, 1024, 0, stream>>>(cnt_e, cnt_b, n_items, nqt, H, nullptr, 0, max_len,
-                                               lpt, group_heads, n_groups * (max_len + 1), ebegin,
-                                               dbegin, hist, static_cast<int4*>(items));
+  const int64_t n_buckets = n_groups * (max_len + 1);
+  plan_schedule_kernel<<<1, 1024, schedule_smem(n_buckets), stream>>>(
+      cnt_e, cnt_b, n_items, nqt, H, nullptr, 0, max_len, lpt, group_heads, n_buckets, ebegin,
+      dbegin, hist, static_cast<int4*>(items));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;
 }
@@ -531,6 +624,16 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
                 "a 128-token tile overlaps more than 8 logical segments (blocks or segments "
                 "smaller than 16 tokens)");
   if (host_err) return fail(TSR_ERR_INTERNAL, "planner error word " + std::to_string(host_err));
+  if (m.kind == TSR_MASK_SVG) {
+    // the head kinds' host copy has arrived with the totals
+    for (int32_t h = 0; h < H; ++h) {
+      const int8_t k = P->host_kinds[h];
+      if (k != TSR_HEAD_SPATIAL && k != TSR_HEAD_TEMPORAL)
+        return fail(TSR_ERR_INVALID_ARG, "head_kind values must be 0 or 1");
+      P->head_layout[h] = k;
+      P->n_temporal += k;
+    }
+  }
 
   // density of the logical mask, for the regime table
   double density = 0.0;
@@ -583,7 +686,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   const int32_t* cnt_e = cnt + (2 * which) * n_items;
   const int32_t* cnt_b = cnt + (2 * which + 1) * n_items;
   const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
-  plan_schedule_kernel<<<1, 1024, 0, stream>>>(
+  plan_schedule_kernel<<<1, 1024, schedule_smem(n_buckets), stream>>>(
       cnt_e, cnt_b, n_items, nqt, H, P->head_kind_dev, m.kind == TSR_MASK_SVG ? 1 : 0,
       static_cast<int32_t>(P->max_item_len), lpt, group_heads, n_buckets, ebegin, dbegin, hist,
       static_cast<int4*>(P->items));
