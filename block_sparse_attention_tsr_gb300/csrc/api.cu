@@ -304,11 +304,20 @@ struct HostCache {
   std::vector<cudaEvent_t> ev;                 // 3 per head group: inputs, plan, attention
   std::vector<tsr_plan_t> plans;               // one per head group
   std::vector<std::array<int64_t, 9>> plan_key;
+  tsr_plan_t full_plan = nullptr;              // one plan over every head (one-plan mode)
+  std::array<int64_t, 10> full_key{};
+  int32_t* counters = nullptr;                 // one work counter per head group (one-plan mode)
+  size_t counters_cap = 0;
   int device = -1;
   void release() {
     for (tsr_plan_t pl : plans) tsr_plan_destroy(pl);
     plans.clear();
     plan_key.clear();
+    if (full_plan) tsr_plan_destroy(full_plan);
+    full_plan = nullptr;
+    cudaFree(counters);
+    counters = nullptr;
+    counters_cap = 0;
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     ev.clear();
     for (int i = 0; i < 8; ++i) {
@@ -348,6 +357,40 @@ struct HostCache {
 };
 thread_local HostCache g_host_cache;
 
+// tsr_plan with the heads per longest-first scheduling group fixed
+// (group_heads > 0; 0 = sized for L2).
+tsr_status plan_new(const tsr_mask* mask, const tsr_plan_opts* opts, int32_t group_heads,
+                    cudaStream_t st, tsr_plan_t* out) {
+  *out = nullptr;
+  if (tsr_status s = check_mask(mask)) return s;
+  if (opts && opts->bn && opts->bn != 64 && opts->bn != 128)
+    return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
+  tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
+  if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
+  struct Guard {
+    tsr_plan_s* p;
+    ~Guard() { free_plan(p); }
+  } guard{P};
+  TSR_CUDA(cudaGetDevice(&P->device));
+  P->B = mask->B;
+  P->H = mask->H;
+  P->N = mask->N;
+  P->d = mask->d;
+  P->group_heads = group_heads;
+  P->flags = opts ? opts->flags : 0;
+  if (opts) {
+    P->has_opts = true;
+    P->opts = *opts;
+  }
+  TSR_CUDA(cudaMalloc(&P->counter, sizeof(int32_t)));
+  TSR_CUDA(cudaMalloc(&P->err, sizeof(uint32_t)));
+  TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), st));
+  if (tsr_status s = plan_fill(P, mask, st)) return s;
+  guard.p = nullptr;
+  *out = P;
+  return TSR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -374,33 +417,7 @@ tsr_status tsr_plan(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_t*
   set_error("");
   if (!out) return fail(TSR_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (tsr_status s = check_mask(mask)) return s;
-  if (opts && opts->bn && opts->bn != 64 && opts->bn != 128)
-    return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
-  if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
-  struct Guard {
-    tsr_plan_s* p;
-    ~Guard() { free_plan(p); }
-  } guard{P};
-  TSR_CUDA(cudaGetDevice(&P->device));
-  P->B = mask->B;
-  P->H = mask->H;
-  P->N = mask->N;
-  P->d = mask->d;
-  P->flags = opts ? opts->flags : 0;
-  if (opts) {
-    P->has_opts = true;
-    P->opts = *opts;
-  }
-  TSR_CUDA(cudaMalloc(&P->counter, sizeof(int32_t)));
-  TSR_CUDA(cudaMalloc(&P->err, sizeof(uint32_t)));
-  TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), st));
-  if (tsr_status s = plan_fill(P, mask, st)) return s;
-  guard.p = nullptr;
-  *out = P;
-  return TSR_OK;
+  return plan_new(mask, opts, 0, static_cast<cudaStream_t>(stream), out);
 }
 
 tsr_status tsr_plan_update(tsr_plan_t plan, const tsr_mask* mask, void* stream) {
@@ -820,10 +837,78 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     TSR_CUDA(cudaMemsetAsync(hc.plans[g]->err, 0, sizeof(uint32_t), hc.s_out));
     return TSR_OK;
   };
+  // One-plan mode (every mask form but key lists, whose slices arrive group by
+  // group, and without the debug / synchronous-check / test flags, which check
+  // each launch): one plan over every head with one head per longest-first
+  // group, so head group g's work items are the contiguous range
+  // [gs[g] * nqt, gs[g + 1] * nqt); each group's launch takes its range and its
+  // own work counter.  Planning happens once, while the first inputs copy in.
+  const bool one_plan =
+      mask->kind != TSR_MASK_KEYLIST &&
+      !(o.flags & (TSR_PLAN_DEBUG_CHECKS | TSR_PLAN_SYNC_CHECK | TSR_PLAN_TEST_STALL));
+  int64_t n_err = G;
   tsr_status s = TSR_OK;
-  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
-    s = plan_group(g);
-    if (s == TSR_OK) s = launch_group(g);
+  if (one_plan) {
+    n_err = 1;
+    tsr_mask full = views[0];                  // device arrays from their start
+    full.B = mask->B;
+    full.H = mask->H;
+    const std::array<int64_t, 10> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
+                                          o.stages, o.ctas_per_sm, o.flags, opts ? 1 : 0};
+    if (hc.full_plan && hc.full_key == key) {
+      s = tsr_plan_update(hc.full_plan, &full, sp);
+    } else {
+      if (hc.full_plan) tsr_plan_destroy(hc.full_plan);
+      hc.full_plan = nullptr;
+      s = plan_new(&full, opts, 1, sp, &hc.full_plan);
+      hc.full_key = key;
+    }
+    if (s == TSR_OK && hc.counters_cap < static_cast<size_t>(G)) {
+      cudaFree(hc.counters);
+      hc.counters = nullptr;
+      hc.counters_cap = 0;
+      const cudaError_t e = cudaMalloc(&hc.counters, sizeof(int32_t) * G);
+      if (e != cudaSuccess) s = cuda_fail(e, "work counters");
+      else hc.counters_cap = G;
+    }
+    if (s == TSR_OK) TSR_CUDA(cudaEventRecord(hc.ev[1], sp));
+    const int64_t nqt = (mask->N + kBM - 1) / kBM;
+    for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+      cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
+      const int64_t b0 = gs[g];
+      const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
+      TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
+      TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[1], 0));
+      FwdArgs a;
+      a.q = dq;
+      a.k = dk;
+      a.v = dv;
+      a.out = dout;
+      a.lse = static_cast<float*>(dlse);
+      a.plan = hc.full_plan;
+      a.item_lo = gs[g] * nqt;
+      a.item_hi = gs[g + 1] * nqt;
+      a.counter = hc.counters + g;
+      s = launch_forward(a, sa);
+      if (s != TSR_OK) break;
+      TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
+      TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
+      TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
+                               cudaMemcpyDeviceToHost, hc.s_out));
+      TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
+                               static_cast<size_t>(n / row_b) * mask->N * 4,
+                               cudaMemcpyDeviceToHost, hc.s_out));
+    }
+    if (s == TSR_OK) {
+      TSR_CUDA(cudaMemcpyAsync(hc.host_err, hc.full_plan->err, sizeof(uint32_t),
+                               cudaMemcpyDeviceToHost, hc.s_out));
+      TSR_CUDA(cudaMemsetAsync(hc.full_plan->err, 0, sizeof(uint32_t), hc.s_out));
+    }
+  } else {
+    for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+      s = plan_group(g);
+      if (s == TSR_OK) s = launch_group(g);
+    }
   }
   // no copy may still read or write the caller's buffers after the return
   const cudaError_t e1 = cudaStreamSynchronize(hc.s_out);
@@ -836,7 +921,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     s = cuda_fail(e2 != cudaSuccess ? e2 : e4, "attention stream");
   if (s == TSR_OK && e3 != cudaSuccess) s = cuda_fail(e3, "copy of the inputs");
   if (s == TSR_OK && e5 != cudaSuccess) s = cuda_fail(e5, "plan stream");
-  for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+  for (int64_t g = 0; g < n_err && s == TSR_OK; ++g) {
     const uint32_t e = hc.host_err[g];
     if (e & DEV_ERR_TIMEOUT) s = fail(TSR_ERR_TIMEOUT, "a device-side wait timed out");
     else if (e) s = fail(TSR_ERR_INTERNAL, "device error word " + std::to_string(e));

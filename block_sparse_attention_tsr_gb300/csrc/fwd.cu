@@ -116,7 +116,9 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
                       encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, P->bn);
       if (!ok)
         return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
-      q.items = static_cast<const int4*>(P->items);
+      const int64_t lo = a.item_lo, hi = a.item_hi < 0 ? P->n_items : a.item_hi;
+      if (lo < 0 || hi > P->n_items || lo > hi) return fail(TSR_ERR_INTERNAL, "bad item range");
+      q.items = static_cast<const int4*>(P->items) + 2 * lo;
       q.entries = static_cast<const int2*>(P->entries);
       q.descs = static_cast<const uint4*>(P->descs);
       q.out = static_cast<__nv_bfloat16*>(a.out);
@@ -130,12 +132,12 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
       q.F = P->F;
       q.S = P->S;
       q.slice_m = P->slice_m;
-      total += P->n_items;
+      total += hi - lo;
     }
     if (total >= (int64_t{1} << 31)) return fail(TSR_ERR_UNSUPPORTED, "more than 2^31 work items");
     prm.n_req = n_req;
     prm.n_items = static_cast<int32_t>(total);
-    prm.counter = P0->counter;
+    prm.counter = reqs[0].counter ? reqs[0].counter : P0->counter;
     prm.err = P0->err;
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(P0->d)));
     prm.tiles_done = ((P0->flags & TSR_PLAN_DEBUG_CHECKS) && P0->b_tot.p)
@@ -151,7 +153,7 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
     if (prm.tiles_done)
       TSR_CUDA(cudaMemsetAsync(prm.tiles_done, 0, sizeof(unsigned long long), stream));
     if (prm.n_items == 0) return TSR_OK;
-    TSR_CUDA(cudaMemsetAsync(P0->counter, 0, sizeof(int32_t), stream));
+    TSR_CUDA(cudaMemsetAsync(prm.counter, 0, sizeof(int32_t), stream));
     const int n = prm.n_items, dev = P0->device;
     if (P0->gathered) return fwd::launch_mode_list(prm, key, n, dev, stream);
     if (temporal) return fwd::launch_mode_perm(prm, key, n, dev, stream);

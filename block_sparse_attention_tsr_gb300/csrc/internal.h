@@ -61,6 +61,7 @@ struct tsr_plan_impl {
   int64_t n_logical_on = 0, n_logical_total = 0, max_item_len = 0;
   std::vector<int8_t> head_layout;  // host copy: 1 = temporal-major
   int32_t n_temporal = 0;
+  int32_t group_heads = 0;    // > 0: heads per longest-first scheduling group (else sized for L2)
   // device buffers (owned)
   void* items = nullptr;     // tsr_plan_item [n_items]
   void* entries = nullptr;   // tsr_plan_entry [n_entries]
@@ -110,6 +111,12 @@ struct FwdArgs {
   void* out;
   float* lse;
   const tsr_plan_impl* plan;
+  // Work items [item_lo, item_hi) of the plan (item_hi < 0: all of them), and
+  // the launch's own work counter (null: the plan's).  Launches of one plan
+  // that may run at the same time need disjoint item ranges and their own
+  // counters, and no debug tile counting.
+  int64_t item_lo = 0, item_hi = -1;
+  int32_t* counter = nullptr;
 };
 tsr_status launch_forward(const FwdArgs& a, cudaStream_t stream);
 // Up to 16 requests in one launch (same d, regime and mask family).

@@ -551,7 +551,8 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
   if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
-  const int32_t group_heads = heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  const int32_t group_heads = P->group_heads > 0 ? P->group_heads
+                                                 : heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
   const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
   if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_groups * (P->max_item_len + 1) + 1)))
     return s;
