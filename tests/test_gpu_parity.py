@@ -434,6 +434,38 @@ def test_host_entry_point_in_head_groups(which):
         assert np.array_equal(lse.double().numpy(), L)
 
 
+def test_host_entry_point_alternating_shapes():
+    """Host calls that change shape and mask form from call to call: every
+    call re-plans into (or replaces) the cached plans and re-zeroes the work
+    counters of its head-group launches, so each result equals one device call
+    over all heads bit for bit (regime forced).  The block-mask, segment and
+    SVG calls take the one-plan path (one plan, one launch per head group over
+    its item range); the key-list call plans group by group."""
+    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
+    cases = [
+        (W.video_block_mask(seed=31, H=12, N=16384), dict(bq=64, bk=64)),
+        (W.segment_mask(32, 2, 5, 8000, lo=16, hi=300), {}),
+        (W.svg_mask(2, 3, n_frames=8, frame_size=512, kinds=np.array([0, 1, 1], np.int8)),
+         dict(n_frames=8, frame_size=512)),
+        (W.video_block_mask(seed=33, H=12, N=16384), dict(bq=64, bk=64)),
+        (W.keylist_mask(seed=34, H=9, N=8192), dict(slice_m=64)),
+        (W.video_block_mask(seed=31, H=12, N=16384), dict(bq=64, bk=64)),
+    ]
+    for i, (spec, kw) in enumerate(cases):
+        arrays = {k: getattr(spec, k) for k in ("blocks", "q_bounds", "k_bounds", "head_kind",
+                                                "indptr", "indices")
+                  if getattr(spec, k) is not None}
+        q, k, v = W.qkv(spec.B, spec.H, spec.N, 128, 40 + i)
+        _, _, O, L = run(spec, 128, seed=0, opts=opts, qkv=(q, k, v))
+        out = torch.empty_like(q).pin_memory()
+        lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32).pin_memory()
+        tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, 128, q.pin_memory(),
+                               k.pin_memory(), v.pin_memory(), out, lse, opts=opts, **kw,
+                               **arrays)
+        assert np.array_equal(out.float().numpy(), O), f"call {i}"
+        assert np.array_equal(lse.double().numpy(), L), f"call {i}"
+
+
 @pytest.mark.parametrize("which", ["uniform", "segments", "svg", "keylist"])
 def test_debug_checks_pass_on_valid_plans(which):
     """With TSR_PLAN_DEBUG_CHECKS every plan is checked index by index on the
