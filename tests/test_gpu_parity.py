@@ -405,17 +405,21 @@ def test_host_entry_point_keylist():
     assert np.array_equal(lse.double().numpy(), L)
 
 
-@pytest.mark.parametrize("which", ["uniform", "svg", "keylist"])
+@pytest.mark.parametrize("which", ["uniform", "uniform_debug", "svg", "keylist"])
 def test_host_entry_point_in_head_groups(which):
-    """Inputs above 160 MB are moved and attended in head groups on three
-    streams (with three or more groups the first and last are smaller); with
-    the regime forced the result is bit-identical to one device call over all
-    heads.  The SVG case has B = 3, H = 3, so a group spans two
+    """Heads are copied in, attended and copied out in groups (growing from one
+    head, ending with two and one); with the regime forced the result is
+    bit-identical to one device call over all heads.  The SVG case has B = 3, H = 3, so a group spans two
     batches and its head kinds come from the flattened (b, h) order; the
-    key-list case rebases each group's slice of indptr."""
+    key-list case rebases each group's slice of indptr.  Block masks and SVG
+    take one plan over all heads and launch each group over its item range;
+    with the debug checks (every plan checked on the device, every launch's
+    tile count compared) and for key lists each group has its own plan."""
     opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
-    if which == "uniform":
-        spec = W.video_block_mask(seed=5, H=16)      # 3 x 134 MB: groups of 2, 6, 6, 2 heads
+    if which == "uniform_debug":
+        opts = dict(opts, flags=tsr.PLAN_DEBUG_CHECKS)
+    if which in ("uniform", "uniform_debug"):
+        spec = W.video_block_mask(seed=5, H=16)      # groups of 1, 2, 3, 4, 3, 2, 1 heads
         kw = dict(bq=64, bk=64, blocks=spec.blocks)
     elif which == "svg":
         spec = W.svg_mask(3, 3, n_frames=21, frame_size=1560, kinds=np.array([1, 0, 1], np.int8))
