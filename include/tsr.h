@@ -369,7 +369,10 @@ tsr_status tsr_svg_route(const void *q, const void *k, const void *v, int32_t B,
  * and Q, K, V to the device, plans, runs the forward and copies O and lse back,
  * then synchronises.  Every pointer in `mask` and q, k, v, out, lse are HOST
  * pointers with the layouts above.  Device buffers are cached per thread between
- * calls (released by tsr_release_host_buffers()).
+ * calls (released by tsr_release_host_buffers()).  Heads are processed in
+ * groups so that copy-in, attention and copy-out overlap; host buffers in
+ * page-locked memory (cudaMallocHost, or pinned tensors) copy asynchronously,
+ * pageable ones are staged by the driver and copy much more slowly.
  */
 tsr_status tsr_attention_host(const tsr_mask *mask, const tsr_plan_opts *opts,
                               const void *q, const void *k, const void *v, void *out,
