@@ -12,19 +12,25 @@ Contents:
   * ``brute.py``   an independent dense NumPy brute force for tiny inputs;
   * ``coverage.c`` expansion of an exported tile plan into element sets, to be
                    compared bit-exactly with the oracle's allowed set;
+  * ``oracle_mask.h`` the mask description both C files share;
   * ``route.py``   SVG head routing by sampled queries (error of each pattern
                    against dense attention), built on ``oracle.c``.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, dense library attention for the all-ones mask, per-block dense
 attention for block-diagonal masks, Q = 0 / one-key / constant-V closed forms,
-counted densities, permutation invariance); ``route.py`` by
+counted densities, permutation invariance); ``coverage.c`` by
+``tests/test_coverage_pins.py`` (hand-built plan exports of every descriptor
+form, each planted plan mistake reported with its code); ``route.py`` by
 ``tests/test_oracle_route.py`` (K = 0 means, brute force, dense radius,
-structured heads).  The pages print no values for any
+structured heads).  ``tests/test_oracle_mutants.py`` plants one mistake at a
+time in copies of ``oracle.c`` and ``coverage.c`` and checks that a named pin
+fails on each.  The pages print no values for any
 input, so nothing is pinned to a worked example of the pages themselves.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -61,8 +67,9 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     out = os.path.join(_BUILD, "liboracle.so")
     srcs = [os.path.join(_HERE, f) for f in ("oracle.c", "coverage.c")]
+    deps = srcs + [os.path.join(_HERE, "oracle_mask.h")]
     if not force and os.path.exists(out) and all(
-            os.path.getmtime(out) >= os.path.getmtime(s) for s in srcs):
+            os.path.getmtime(out) >= os.path.getmtime(s) for s in deps):
         return out
     base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-o", out + ".tmp"] + srcs
     try:
@@ -74,28 +81,48 @@ def build(force: bool = False) -> str:
     return out
 
 
+def _bind(L):
+    """Declare the C functions' signatures on a loaded build of the oracle."""
+    P = ctypes.c_void_p
+    L.oracle_attention_rows.argtypes = [P, P, P, P, P, ctypes.c_int64, P, P, P, ctypes.c_int]
+    L.oracle_attention_rows.restype = ctypes.c_int
+    L.oracle_attention.argtypes = [P, P, P, P, P, P, ctypes.c_int]
+    L.oracle_attention.restype = ctypes.c_int
+    L.oracle_probs_row.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_int32, P, P, P, P]
+    L.oracle_probs_row.restype = ctypes.c_int64
+    L.oracle_row_keys.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+    L.oracle_row_keys.restype = ctypes.c_int64
+    L.oracle_count_allowed.argtypes = [P, P, ctypes.c_int]
+    L.oracle_count_allowed.restype = ctypes.c_int64
+    L.oracle_max_threads.restype = ctypes.c_int
+    L.coverage_check.argtypes = [P, P, ctypes.c_size_t, P, ctypes.c_int64, P, ctypes.c_int]
+    L.coverage_check.restype = ctypes.c_int64
+    return L
+
+
 def lib():
     global _LIB
     with _LOCK:
         if _LIB is None:
-            L = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            L.oracle_attention_rows.argtypes = [P, P, P, P, P, ctypes.c_int64, P, P, P, ctypes.c_int]
-            L.oracle_attention_rows.restype = ctypes.c_int
-            L.oracle_attention.argtypes = [P, P, P, P, P, P, ctypes.c_int]
-            L.oracle_attention.restype = ctypes.c_int
-            L.oracle_probs_row.argtypes = [P, P, P, P, ctypes.c_int32, ctypes.c_int32,
-                                           ctypes.c_int32, P, P, P, P]
-            L.oracle_probs_row.restype = ctypes.c_int64
-            L.oracle_row_keys.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
-            L.oracle_row_keys.restype = ctypes.c_int64
-            L.oracle_count_allowed.argtypes = [P, P, ctypes.c_int]
-            L.oracle_count_allowed.restype = ctypes.c_int64
-            L.oracle_max_threads.restype = ctypes.c_int
-            L.coverage_check.argtypes = [P, P, ctypes.c_size_t, P, ctypes.c_int64, P, ctypes.c_int]
-            L.coverage_check.restype = ctypes.c_int64
-            _LIB = L
+            _LIB = _bind(ctypes.CDLL(build()))
     return _LIB
+
+
+@contextlib.contextmanager
+def swapped_library(path: str):
+    """For the planted-mistake tests only: every function of this package runs
+    on another build of the C sources (a copy with one deliberate mistake) until
+    the block exits; the normal build is then restored."""
+    global _LIB
+    normal = lib()
+    with _LOCK:
+        _LIB = _bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        with _LOCK:
+            _LIB = normal
 
 
 def max_threads() -> int:

@@ -28,20 +28,7 @@
 #include <omp.h>
 #endif
 
-/* the oracle's mask description (same layout as in oracle.c) */
-typedef struct {
-  int32_t kind;
-  int32_t B, H, N, d;
-  int32_t bq, bk;
-  int32_t n_qseg, n_kseg;
-  const int32_t *q_bounds, *k_bounds;
-  const uint8_t *blocks;
-  int32_t n_frames, frame_size;
-  const int8_t *head_kind;
-  int32_t slice_m;
-  const int64_t *indptr;
-  const int32_t *indices;
-} oracle_mask;
+#include "oracle_mask.h"
 
 int64_t oracle_row_keys(const oracle_mask *m, int32_t b, int32_t h, int32_t i, int32_t *keys);
 
