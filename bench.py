@@ -79,6 +79,48 @@ def whole_job_rate(flops_per_rank: float, ms_step: float, world: int) -> float:
     return world * flops_per_rank / (ms_step * 1e-3) / 1e12
 
 
+def sum_over_ranks(x: float, dist, device) -> float:
+    """x summed over all ranks (x itself with one rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def head_range(H: int, world: int, rank: int):
+    """Heads [lo, hi) of an H-head request that rank `rank` of `world` runs: the
+    forward pass of every (b, h) is independent, so the request splits by head
+    with no exchange between ranks; the split is balanced to within one head."""
+    return (rank * H) // world, ((rank + 1) * H) // world
+
+
+def slice_heads(spec, lo: int, hi: int):
+    """The same mask restricted to heads [lo, hi) (every batch): block grids and
+    head kinds are sliced, key lists keep their (b, h, query block) order with
+    indptr rebased to the kept lists."""
+    import copy
+    import workloads as W
+    out = copy.copy(spec)
+    out.H = hi - lo
+    out.meta = dict(spec.meta, heads=(lo, hi))
+    if spec.blocks is not None:
+        out.blocks = np.ascontiguousarray(spec.blocks[:, lo:hi])
+    if spec.head_kind is not None:
+        out.head_kind = np.ascontiguousarray(spec.head_kind[lo:hi])
+    if spec.kind == W.MASK_KEYLIST:
+        nqb = -(-spec.N // spec.slice_m)
+        rows = np.concatenate([np.arange((b * spec.H + lo) * nqb, (b * spec.H + hi) * nqb)
+                               for b in range(spec.B)]) if hi > lo else np.zeros(0, np.int64)
+        lens = spec.indptr[rows + 1] - spec.indptr[rows]
+        out.indptr = np.zeros(len(rows) + 1, dtype=np.int64)
+        np.cumsum(lens, out=out.indptr[1:])
+        out.indices = (np.concatenate([spec.indices[spec.indptr[r]:spec.indptr[r + 1]] for r in rows])
+                       if len(rows) else np.zeros(0, np.int32)).astype(np.int32)
+    return out
+
+
 def read_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -111,30 +153,34 @@ def read_traffic(kernel_hash: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (its own 25 ms loop, each with its timestamp), started
+    before the warm-up; summary() keeps the samples taken inside the timed
+    region (a wall-clock window)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 25
 
     def __init__(self, gpu: int):
         self.gpu = gpu
         self.proc = None
         self.path = f"/tmp/tsr_clocks_{os.getpid()}.csv"
+        self.rows = []
 
     def __enter__(self):
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
             return self
         t0 = time.time()
         while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
-            time.sleep(0.05)
+            time.sleep(0.02)
         return self
 
     def __exit__(self, *a):
@@ -145,28 +191,40 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.fh.close()
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        t = _smi_time(parts[0])
+                        self.rows.append((t, float(parts[2]), float(parts[3]),
+                                          float(parts[4]), parts[6:10]))
+                    except ValueError:
+                        continue
 
-    def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+    def summary(self, t0: float, t1: float):
+        """Samples with wall time in [t0, t1] (the timed region)."""
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-                except ValueError:
-                    continue
+        rows = [r for r in self.rows if t0 <= r[0] <= t1]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        load = [r for r in rows if r[2] > 200.0] or rows
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples_total": len(self.rows)}
+        load = [r for r in rows if r[3] > 200.0] or rows
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({n for r in load for n, v in zip(names, r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+        reasons = sorted({n for r in load for n, v in zip(names, r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in load), "sm_max_mhz": max(r[2] for r in rows),
                 "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
-                "power_w_max": max(r[2] for r in rows)}
+                "period_ms": self.PERIOD_MS, "power_w_max": max(r[3] for r in rows)}
+
+
+def _smi_time(stamp: str) -> float:
+    """nvidia-smi's timestamp field ("YYYY/MM/DD HH:MM:SS.mmm", local time) as
+    seconds since the epoch, comparable with time.time()."""
+    import datetime
+    return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+
 
 
 def cpu_baseline(spec, q, k, v, target_s: float = 12.0) -> dict:
@@ -393,6 +451,82 @@ def run_batch(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def time_steps(tsr, plan, mask, qd, kd, vd, out, lse, stream, steps: int, warmup: int,
+               before_timed=None):
+    """Warm-up, then `steps` steps (re-plan + forward) on `stream`, each forward
+    bracketed by its own CUDA events.  Returns (total ms, per-step forward ms,
+    wall-clock window of the timed region)."""
+    import torch
+
+    def step(ev_pair=None):
+        # the mask is re-planned every step (dynamic masks); the plan's device
+        # storage is reused
+        plan.update(mask, stream)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        tsr.tsr_bsa_forward(qd, kd, vd, plan, out, lse, stream)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    tsr.tsr_plan_device_status(plan)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if before_timed is not None:
+        before_timed()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    tsr.tsr_plan_device_status(plan)
+    return t_start.elapsed_time(t_end), [a.elapsed_time(b) for a, b in evs], (w0, w1)
+
+
+def other_workloads(tsr, names, steps: int, warmup: int, dev, stream, peak: float) -> dict:
+    """The other full-size video workloads of the same path, timed the same way
+    (one request of 24 heads, re-plan + forward per step, Q/K/V drawn on the
+    device): forward and step times, effective TFLOP/s, fraction of the dense
+    bf16 peak and tile fill."""
+    import torch
+    import workloads as W
+    res = {}
+    for name in names:
+        spec = WORKLOADS[name][1](W, 24)
+        qd, kd, vd = W.qkv(spec.B, spec.H, spec.N, D, seed=7, device=str(dev))
+        mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, D, **W.mask_tensors(spec, dev))
+        out = torch.empty_like(qd)
+        lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32, device=dev)
+        plan = tsr.tsr_plan(mask, None, stream)
+        total_ms, fwd, _ = time_steps(tsr, plan, mask, qd, kd, vd, out, lse, stream, steps, warmup)
+        st = plan.stats()
+        flops = 4.0 * D * allowed_pairs(spec)
+        fwd_ms = sum(fwd) / len(fwd)
+        res[name] = {"workload": WORKLOADS[name][0], "step_ms": total_ms / steps,
+                     "forward_ms": fwd_ms, "plan_ms": total_ms / steps - fwd_ms,
+                     "step_tflops": flops / (total_ms / steps) / 1e9,
+                     "forward_tflops": flops / fwd_ms / 1e9,
+                     "forward_frac_of_peak": flops / fwd_ms / 1e9 / peak,
+                     "fill": fill_of(spec, st), "tiles": st["n_entries"],
+                     "regime": {k: st[k] for k in ("bm", "bn", "stages", "ctas_per_sm", "regime_id")}}
+        plan.destroy()
+        del qd, kd, vd, out, lse, mask
+        torch.cuda.empty_cache()
+    return res
+
+
+def fill_of(spec, stats) -> float:
+    """Allowed pairs over the elements of the computed physical tiles."""
+    computed = stats["n_entries"] * stats["bm"] * stats["bn"]
+    return allowed_pairs(spec) / computed if computed else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,9 +535,17 @@ def main():
     ap.add_argument("--impl", default="tsr", choices=["tsr", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the SVG 480p and 720p key-list workloads after the headline")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with several ranks: every rank runs the whole request (weak scaling) "
+                         "instead of its share of the heads")
     ap.add_argument("--bn", type=int, default=0, help="force the K/V tile width (0 = table)")
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--ctas", type=int, default=0)
+    ap.add_argument("--orient", type=int, default=0,
+                    help="force the tile orientation: 1 = 128 query rows, 2 = 64-query "
+                         "transposed tiles (0 = table)")
     ap.add_argument("--workload", default="video480p",
                     help="video480p (the benchmark), svg480p, keylist720p, sweepM (one member), "
                          "sweep (regime-table regret over --sweep-masks members), "
@@ -445,71 +587,52 @@ def main():
     tsr.build()
     tsr.lib()
 
-    spec, q, k, v = make_workload(args.heads, args.workload)
-    pairs = allowed_pairs(spec)
+    full_spec, q, k, v = make_workload(args.heads, args.workload)
+    # several ranks: each runs its share of the request's heads (no exchange),
+    # unless --replicas gives every rank the whole request
+    lo, hi = (0, full_spec.H) if (world == 1 or args.replicas) else head_range(full_spec.H, world, rank)
+    spec = slice_heads(full_spec, lo, hi) if (lo, hi) != (0, full_spec.H) else full_spec
+    q, k, v = (x[:, lo:hi].contiguous() for x in (q, k, v))
+    pairs = allowed_pairs(spec) if hi > lo else 0
     flops = 4.0 * D * pairs
     dev = torch.device("cuda", local)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    mt = W.mask_tensors(spec, dev)
-    mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, D, **mt)
-    out = torch.empty_like(qd)
-    lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    peaks = read_peaks()
 
     opts = None
-    if args.bn or args.stages or args.ctas:
-        opts = {"bn": args.bn, "stages": args.stages, "ctas_per_sm": args.ctas}
+    if args.bn or args.stages or args.ctas or args.orient:
+        opts = {"bn": args.bn, "stages": args.stages, "ctas_per_sm": args.ctas, "orient": args.orient}
 
-    plan = tsr.tsr_plan(mask, opts, stream)
-
-    def step(ev_pair=None):
-        # the mask is re-planned every step (dynamic masks); the plan's device
-        # storage is reused
-        plan.update(mask, stream)
-        if ev_pair is not None:
-            ev_pair[0].record(stream)
-        tsr.tsr_bsa_forward(qd, kd, vd, plan, out, lse, stream)
-        if ev_pair is not None:
-            ev_pair[1].record(stream)
-        return plan
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    tsr.tsr_plan_device_status(plan)
-    stats = plan.stats()
-    computed = stats["n_entries"] * 128 * stats["bn"]
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = [a.elapsed_time(b) for a, b in evs]
+    clk = ClockSampler(local)
+    stats, fwd_avg, total_ms, window = None, 0.0, 0.0, (0.0, 0.0)
+    with clk:
+        if hi > lo:
+            qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+            mask = tsr.make_mask(spec.kind, spec.B, spec.H, spec.N, D, **W.mask_tensors(spec, dev))
+            out = torch.empty_like(qd)
+            lse = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32, device=dev)
+            plan = tsr.tsr_plan(mask, opts, stream)
+            barrier = (lambda: dist.barrier()) if dist is not None else None
+            total_ms, fwd_ms, window = time_steps(tsr, plan, mask, qd, kd, vd, out, lse, stream,
+                                                  args.steps, args.warmup, barrier)
+            stats = plan.stats()
+            fwd_avg = sum(fwd_ms) / len(fwd_ms)
+        elif dist is not None:
+            dist.barrier()
+        if dist is not None:
+            dist.barrier()
     total_ms = max_over_ranks(total_ms, dist, dev)
-    tsr.tsr_plan_device_status(plan)
+    job_flops = sum_over_ranks(flops, dist, dev)
     ms_step = total_ms / args.steps
-    value = whole_job_rate(flops, ms_step, world)
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    peaks = read_peaks()
-    achieved = flops / (fwd_avg * 1e-3) / 1e12
+    value = job_flops / (ms_step * 1e-3) / 1e12
     long_region = total_ms > 2000.0
     peak = peaks["bf16_sustained"] if long_region else peaks["bf16"]
+    achieved = flops / (fwd_avg * 1e-3) / 1e12 if fwd_avg > 0 else 0.0
     khash = kernel_source_hash()
     traffic = read_traffic(khash)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and hi > lo:
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
         oh = torch.empty_like(qh).pin_memory()
         lh = torch.empty((spec.B, spec.H, spec.N), dtype=torch.float32).pin_memory()
@@ -525,7 +648,8 @@ def main():
                      if isinstance(v2, np.ndarray) else v2) for k2, v2 in marr.items()}
 
         def host_call():
-            tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, D, qh, kh, vh, oh, lh, **marr)
+            tsr.tsr_attention_host(spec.kind, spec.B, spec.H, spec.N, D, qh, kh, vh, oh, lh,
+                                   opts=opts, **marr)
 
         for _ in range(2):
             host_call()
@@ -536,13 +660,13 @@ def main():
         for _ in range(n_e2e):
             host_call()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, dist, dev)
-        e2e = {"value": whole_job_rate(flops, 1e3 * e2e_s, world), "unit": UNIT,
-               "h2d_bytes_per_step": 3 * qh.numel() * 2 + mask_bytes,
-               "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+        e2e = {"value": job_flops / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(sum_over_ranks(3 * qh.numel() * 2 + mask_bytes, dist, dev)),
+               "d2h_bytes_per_step": int(sum_over_ranks(oh.numel() * 2 + lh.numel() * 4, dist, dev)),
                "ms_per_step": 1e3 * e2e_s}
 
     route = None
-    if spec.kind == W.MASK_SVG:
+    if spec.kind == W.MASK_SVG and hi > lo:
         # the step before the path: routing the heads from 64 sampled query rows
         smp = np.sort(np.random.Generator(np.random.PCG64(64)).choice(spec.N, size=64,
                                                                       replace=False))
@@ -556,39 +680,55 @@ def main():
         torch.cuda.synchronize()
         route = {"samples": 64, "ms": a.elapsed_time(b) / 5, "timed": "separately, not in the step"}
 
+    others = None
+    if (rank == 0 and world == 1 and args.workload == "video480p" and args.heads == 24
+            and not args.no_other_workloads):
+        del qd, kd, vd, out, lse
+        torch.cuda.empty_cache()
+        others = other_workloads(tsr, ("svg480p", "keylist720p"), min(args.steps, 30),
+                                 args.warmup, dev, stream, peaks["bf16"])
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(spec, q, k, v)
         cpu.pop("seconds", None)
 
     wname = WORKLOADS[args.workload][0] if args.workload in WORKLOADS else args.workload
+    split = world > 1 and not args.replicas
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
             "config": {"workload": wname if args.heads == 24 else f"{wname}_heads{args.heads}",
-                       "B": spec.B, "H": spec.H, "N": spec.N, "d": D,
+                       "B": full_spec.B, "H": full_spec.H, "N": full_spec.N, "d": D,
+                       "parallelism": (f"heads split over {world} ranks, no collective" if split
+                                       else ("replicas" if world > 1 else "single GPU")),
+                       "rank0_heads": [lo, hi],
                        "mask_kind": int(spec.kind), "logical_block": [spec.bq, spec.bk],
                        "allowed_pairs": pairs,
-                       "density": pairs / (spec.B * spec.H * spec.N * spec.N),
+                       "density": pairs / max(1, spec.B * spec.H * spec.N * spec.N),
                        "step": "tsr_plan_update (re-plan of the mask) + tsr_bsa_forward",
                        "l2": "inputs (603 MB Q/K/V) exceed the 129 MB L2; no flush",
-                       "regime": {k2: stats[k2] for k2 in ("bn", "stages", "ctas_per_sm", "regime_id")},
-                       "tiles": stats["n_entries"], "boundary_tiles": stats["n_boundary"],
-                       "fill": pairs / computed if computed else None,
+                       "regime": ({k2: stats[k2] for k2 in ("bm", "bn", "stages", "ctas_per_sm",
+                                                             "regime_id")} if stats else None),
+                       "tiles": stats["n_entries"] if stats else 0,
+                       "boundary_tiles": stats["n_boundary"] if stats else 0,
+                       "fill": fill_of(spec, stats) if stats else None,
                        "forward_ms": fwd_avg, "plan_ms": ms_step - fwd_avg,
                        **({"svg_route": route} if route else {}),
+                       **({"other_workloads": others} if others else {}),
                        "forward_tflops": achieved,
                        "forward_frac_of_peak": achieved / peak},
-            "pct_of_peak": 100.0 * value / peak,
+            "pct_of_peak": 100.0 * value / (world * peak),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peaks['src']} bf16 "
                                         f"{'sustained' if long_region else 'burst'}",
                          "kernel": "bsa_fwd_kernel", "kernel_source_hash": khash},
-            "clocks": clk.summary(),
-            "gpu_launches": args.steps * launches_per_step(spec, stats),
+            "clocks": clk.summary(*window),
+            "gpu_launches": args.steps * launches_per_step(spec, stats or {}),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

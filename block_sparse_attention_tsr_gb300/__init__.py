@@ -27,10 +27,12 @@ __all__ = [
     "tsr_attention_host",
     "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
+    "ORIENT_ROWS", "ORIENT_KEYS",
     "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL",
 ]
 
 UNIFORM, SEGMENTS, SVG, KEYLIST = 0, 1, 2, 3
+ORIENT_ROWS, ORIENT_KEYS = 1, 2
 PLAN_SYNC_CHECK, PLAN_NO_LPT, PLAN_TEST_STALL, PLAN_DEBUG_CHECKS = 1, 2, 4, 8
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory",
            5: "device wait timed out", 6: "internal error"}
@@ -68,7 +70,7 @@ class _Request(ctypes.Structure):
 class _Opts(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("seed_reserved", ctypes.c_int64)]
+                ("orient", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class _Stats(ctypes.Structure):
@@ -78,7 +80,7 @@ class _Stats(ctypes.Structure):
                 ("n_entries", ctypes.c_int64), ("n_boundary", ctypes.c_int64),
                 ("n_logical_on", ctypes.c_int64), ("n_logical_total", ctypes.c_int64),
                 ("max_item_len", ctypes.c_int64), ("regime_id", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("orient", ctypes.c_int32)]
 
 
 class _Regime(ctypes.Structure):
@@ -233,7 +235,7 @@ class Plan:
 def _opts(opts) -> Optional[_Opts]:
     if opts is None:
         return None
-    unknown = set(opts) - {"bn", "stages", "ctas_per_sm", "flags"}
+    unknown = set(opts) - {"bn", "stages", "ctas_per_sm", "flags", "orient"}
     if unknown:
         raise ValueError(f"unknown plan option(s): {sorted(unknown)}")
     o = _Opts()
@@ -241,6 +243,7 @@ def _opts(opts) -> Optional[_Opts]:
     o.stages = int(opts.get("stages", 0))
     o.ctas_per_sm = int(opts.get("ctas_per_sm", 0))
     o.flags = int(opts.get("flags", 0))
+    o.orient = int(opts.get("orient", 0))
     return o
 
 
@@ -365,6 +368,7 @@ def tsr_attention_host(kind: int, B: int, H: int, N: int, d: int, q, k, v, out, 
     s.n_frames, s.frame_size = mask_arrays.get("n_frames", 0), mask_arrays.get("frame_size", 0)
     s.slice_m = mask_arrays.get("slice_m", 0)
     s.indptr, s.indices = hptr(mask_arrays.get("indptr")), hptr(mask_arrays.get("indices"))
+    s.temporal_radius = int(mask_arrays.get("temporal_radius", 0))
     o = _opts(opts)
     _check(lib().tsr_attention_host(ctypes.byref(s), ctypes.byref(o) if o is not None else None,
                                     hptr(q), hptr(k), hptr(v), hptr(out), hptr(lse)))

@@ -303,9 +303,9 @@ struct HostCache {
   size_t stage_cap = 0;
   std::vector<cudaEvent_t> ev;                 // 3 per head group: inputs, plan, attention
   std::vector<tsr_plan_t> plans;               // one per head group
-  std::vector<std::array<int64_t, 9>> plan_key;
+  std::vector<std::array<int64_t, 10>> plan_key;
   tsr_plan_t full_plan = nullptr;              // one plan over every head (one-plan mode)
-  std::array<int64_t, 10> full_key{};
+  std::array<int64_t, 11> full_key{};
   int32_t* counters = nullptr;                 // one work counter per head group (one-plan mode)
   size_t counters_cap = 0;
   int device = -1;
@@ -365,6 +365,10 @@ tsr_status plan_new(const tsr_mask* mask, const tsr_plan_opts* opts, int32_t gro
   if (tsr_status s = check_mask(mask)) return s;
   if (opts && opts->bn && opts->bn != 64 && opts->bn != 128)
     return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
+  if (opts && (opts->orient < 0 || opts->orient > TSR_ORIENT_KEYS || opts->reserved != 0))
+    return fail(TSR_ERR_INVALID_ARG, "opts->orient must be 0, 1 or 2 and opts->reserved 0");
+  if (opts && opts->orient == TSR_ORIENT_KEYS)
+    return fail(TSR_ERR_UNSUPPORTED, "TSR_ORIENT_KEYS tiles are not built in this library");
   tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
   if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
   struct Guard {
@@ -527,6 +531,7 @@ tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   s->n_logical_total = plan->n_logical_total;
   s->max_item_len = plan->max_item_len;
   s->regime_id = plan->regime_id;
+  s->orient = TSR_ORIENT_ROWS;
   return TSR_OK;
 }
 
@@ -797,8 +802,8 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     tsr_mask& vw = views[g];
     vw.B = 1;
     vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
-    const std::array<int64_t, 9> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
-                                         o.flags, opts ? 1 : 0};
+    const std::array<int64_t, 10> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
+                                          o.flags, o.orient, opts ? 1 : 0};
     if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
     tsr_status st;
     if (hc.plans[g] && hc.plan_key[g] == key) {
@@ -853,8 +858,8 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     tsr_mask full = views[0];                  // device arrays from their start
     full.B = mask->B;
     full.H = mask->H;
-    const std::array<int64_t, 10> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
-                                          o.stages, o.ctas_per_sm, o.flags, opts ? 1 : 0};
+    const std::array<int64_t, 11> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
+                                          o.stages, o.ctas_per_sm, o.flags, o.orient, opts ? 1 : 0};
     if (hc.full_plan && hc.full_key == key) {
       s = tsr_plan_update(hc.full_plan, &full, sp);
     } else {

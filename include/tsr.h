@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define TSR_ABI_VERSION 2
+#define TSR_ABI_VERSION 3
 
 typedef enum {
   TSR_OK = 0,
@@ -126,14 +126,27 @@ typedef struct {
   int32_t temporal_radius;
 } tsr_mask;
 
-/* Plan options (pass NULL for defaults). */
+/* Plan options (pass NULL for defaults; zero fields mean "from the table"). */
 typedef struct {
   int32_t bn;        /* 0 = from the regime table; 64 or 128 = force KV tile width   */
   int32_t stages;    /* 0 = from the regime table; else K/V pipeline depth (2..6)    */
   int32_t ctas_per_sm; /* 0 = from the regime table; 1 or 2                           */
   int32_t flags;     /* TSR_PLAN_* bits                                              */
-  int64_t seed_reserved;
+  int32_t orient;    /* tile orientation (ABI version 3): 0 = from the regime table,
+                        TSR_ORIENT_ROWS or TSR_ORIENT_KEYS                          */
+  int32_t reserved;  /* must be 0                                                    */
 } tsr_plan_opts;
+
+/* Physical tile orientations.
+ *   TSR_ORIENT_ROWS  128 query rows x bn keys per tile: S = Q K^T with the
+ *                    queries on the tensor core's M = 128 side.
+ *   TSR_ORIENT_KEYS  64 query rows x 64 keys per tile, two tiles of a query
+ *                    block's list computed together as S^T = K Q^T with 128 keys
+ *                    on the M side and the 64 queries on the N side (d = 128).
+ *                    A 64-row query block is never widened to 128 rows, so a
+ *                    key block is computed only for the query blocks that need it. */
+#define TSR_ORIENT_ROWS 1
+#define TSR_ORIENT_KEYS 2
 
 #define TSR_PLAN_SYNC_CHECK 1  /* tsr_bsa_forward synchronises and reads the device
                                   error word (slower; for debugging)               */
@@ -166,7 +179,7 @@ typedef struct {
   int64_t n_logical_total;
   int64_t max_item_len;
   int32_t regime_id;                    /* row of the regime table used (-1: opts) */
-  int32_t reserved;
+  int32_t orient;                       /* TSR_ORIENT_ROWS or TSR_ORIENT_KEYS       */
 } tsr_plan_stats;
 
 /*

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_strings(L):
-    assert tsr.tsr_abi_version() == 2
+    assert tsr.tsr_abi_version() == 3
     assert L.tsr_status_string(0) == b"ok"
     assert L.tsr_status_string(5) == b"device wait timed out"
 

@@ -63,14 +63,16 @@ class MaskSpec:
     meta: dict = field(default_factory=dict)
 
 
-def qkv(B: int, H: int, N: int, d: int, seed: int, scale: float = 1.0):
-    """bf16 Q, K, V of shape [B, H, N, d] drawn from N(0, scale^2), seeded."""
+def qkv(B: int, H: int, N: int, d: int, seed: int, scale: float = 1.0, device: str = "cpu"):
+    """bf16 Q, K, V of shape [B, H, N, d] drawn from N(0, scale^2), seeded.
+    ``device="cuda"`` draws them with the GPU's generator (same distribution,
+    other values; for timing runs that never compare against the oracle)."""
     import torch
-    g = torch.Generator(device="cpu")
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     out = []
     for _ in range(3):
-        t = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        t = torch.randn((B, H, N, d), generator=g, dtype=torch.float32, device=device)
         if scale != 1.0:
             t = t * scale
         out.append(t.to(torch.bfloat16))
@@ -119,13 +121,23 @@ def banded_blocks(B: int, H: int, nqb: int, nkb: int, densities: np.ndarray,
     scale = max(nqb, nkb)
     w = 1.0 + boost * np.exp(-np.abs(qi[:, None] - kj[None, :]) * scale / width)
     out = np.zeros((B, H, nqb, nkb), dtype=np.uint8)
+    # mean(min(1, c w)) from the sorted weights: the k weights below 1 / c
+    # contribute c * (their sum), the rest 1 each
+    ws = np.sort(w.ravel())
+    cum = np.concatenate([[0.0], np.cumsum(ws)])
+    n = ws.size
+
+    def mean_p(c: float) -> float:
+        k = int(np.searchsorted(ws, 1.0 / c, side="left"))
+        return (c * cum[k] + (n - k)) / n
+
     for b in range(B):
         for h in range(H):
             rho = float(densities[b, h])
             lo, hi = 0.0, 1.0 / w.min()
             for _ in range(60):
                 c = 0.5 * (lo + hi)
-                if np.minimum(1.0, c * w).mean() < rho:
+                if mean_p(c) < rho:
                     lo = c
                 else:
                     hi = c
