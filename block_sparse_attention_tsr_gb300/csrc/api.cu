@@ -206,7 +206,9 @@ tsr_status check_mask(const tsr_mask* m) {
     case TSR_MASK_KEYLIST:
       if (m->slice_m != 64 && m->slice_m != 128)
         return fail(TSR_ERR_UNSUPPORTED, "KEYLIST slice_m must be 64 or 128");
-      if (!m->indptr || !m->indices) return fail(TSR_ERR_INVALID_ARG, "indptr / indices missing");
+      // indices may be NULL when every list is empty (checked against indptr
+      // before anything reads a list)
+      if (!m->indptr) return fail(TSR_ERR_INVALID_ARG, "indptr missing");
       return TSR_OK;
     default:
       return fail(TSR_ERR_INVALID_ARG, "unknown mask kind");
@@ -367,8 +369,6 @@ tsr_status plan_new(const tsr_mask* mask, const tsr_plan_opts* opts, int32_t gro
     return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
   if (opts && (opts->orient < 0 || opts->orient > TSR_ORIENT_KEYS || opts->reserved != 0))
     return fail(TSR_ERR_INVALID_ARG, "opts->orient must be 0, 1 or 2 and opts->reserved 0");
-  if (opts && opts->orient == TSR_ORIENT_KEYS)
-    return fail(TSR_ERR_UNSUPPORTED, "TSR_ORIENT_KEYS tiles are not built in this library");
   tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
   if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
   struct Guard {
@@ -448,7 +448,8 @@ tsr_status tsr_plan_device_status(tsr_plan_t plan, void* stream) {
   TSR_CUDA(cudaMemcpyAsync(&e, plan->err, sizeof e, cudaMemcpyDeviceToHost, st));
   TSR_CUDA(cudaMemsetAsync(plan->err, 0, sizeof(uint32_t), st));
   TSR_CUDA(cudaStreamSynchronize(st));
-  if (e & DEV_ERR_TIMEOUT) return fail(TSR_ERR_TIMEOUT, "a device-side wait timed out");
+  if (e & DEV_ERR_TIMEOUT)
+    return fail(TSR_ERR_TIMEOUT, "a device-side wait timed out (error word " + std::to_string(e) + ")");
   if (e) return fail(TSR_ERR_INTERNAL, "device error word " + std::to_string(e));
   return TSR_OK;
 }
@@ -518,7 +519,7 @@ tsr_status tsr_bsa_forward_batch(const tsr_request* reqs, int32_t n, void* strea
 tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   if (!plan || !s) return fail(TSR_ERR_INVALID_ARG, "NULL argument");
   memset(s, 0, sizeof *s);
-  s->bm = kBM;
+  s->bm = plan->bm;
   s->bn = plan->bn;
   s->stages = plan->stages;
   s->ctas_per_sm = plan->ctas;
@@ -531,7 +532,7 @@ tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   s->n_logical_total = plan->n_logical_total;
   s->max_item_len = plan->max_item_len;
   s->regime_id = plan->regime_id;
-  s->orient = TSR_ORIENT_ROWS;
+  s->orient = plan->orient;
   return TSR_OK;
 }
 
@@ -555,7 +556,7 @@ tsr_status tsr_plan_export(tsr_plan_t plan, void* host_buf, size_t* bytes) {
   h.H = plan->H;
   h.N = plan->N;
   h.d = plan->d;
-  h.bm = kBM;
+  h.bm = plan->bm;
   h.bn = plan->bn;
   h.gathered = plan->gathered;
   h.n_frames = plan->n_temporal ? plan->F : 0;
@@ -877,7 +878,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       else hc.counters_cap = G;
     }
     if (s == TSR_OK) TSR_CUDA(cudaEventRecord(hc.ev[1], sp));
-    const int64_t nqt = (mask->N + kBM - 1) / kBM;
+    const int64_t nqt = hc.full_plan ? (mask->N + hc.full_plan->bm - 1) / hc.full_plan->bm : 0;
     for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
       cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
       const int64_t b0 = gs[g];

@@ -4,7 +4,8 @@
 // tile's coordinates, every boundary descriptor and every gathered key index are
 // used as addresses.  These kernels read a finished plan and verify, without
 // using any value as an address before it is checked:
-//   * each item names a (b*h, query tile) inside the problem, each pair exactly
+//   * each item names a (b*h, query tile of the plan's height) inside the
+//     problem, each pair exactly
 //     once, with an entry range inside the plan and a layout of 0 or 1;
 //   * contiguous entries: key tile starts inside [0, N), multiples of the tile
 //     width, strictly ascending within an item; descriptor index -1 or inside
@@ -30,7 +31,7 @@ struct CheckArgs {
   const uint8_t* descs;       // tsr_tile_desc, 32 bytes each
   const int32_t* gidx;
   int64_t n_items, n_entries, n_desc;
-  int32_t BH, nqt, N, bn, gathered;
+  int32_t BH, nqt, N, bm, bn, gathered;
   int32_t* seen;              // [BH * nqt], zeroed
   uint32_t* err;
 };
@@ -73,7 +74,7 @@ __global__ void plan_check_items_kernel(CheckArgs a) {
         }
         if (!(n_r < 1 || n_r > 8 || n_c < 1 || n_c > 8)) {
           bad |= d[2] != 0;                       // r_start[0]
-          for (int r = 1; r < n_r; ++r) bad |= d[2 + r] <= d[1 + r] || d[2 + r] >= kBM;
+          for (int r = 1; r < n_r; ++r) bad |= d[2 + r] <= d[1 + r] || d[2 + r] >= a.bm;
           bad |= d[10] != 0;                      // c_start[0]
           for (int c = 1; c <= n_c; ++c) bad |= d[10 + c] < d[9 + c];
           bad |= d[10 + n_c] > a.bn;
@@ -101,7 +102,7 @@ __global__ void plan_check_seen_kernel(const int32_t* seen, int64_t n, uint32_t*
 }  // namespace
 
 tsr_status plan_check(const tsr_plan_impl* P, cudaStream_t stream) {
-  const int32_t nqt = (P->N + kBM - 1) / kBM;
+  const int32_t nqt = (P->N + P->bm - 1) / P->bm;
   const int64_t BH = static_cast<int64_t>(P->B) * P->H;
   const int64_t n_pairs = BH * nqt;
   void* seen = nullptr;
@@ -119,6 +120,7 @@ tsr_status plan_check(const tsr_plan_impl* P, cudaStream_t stream) {
     a.BH = static_cast<int32_t>(BH);
     a.nqt = nqt;
     a.N = P->N;
+    a.bm = P->bm;
     a.bn = P->bn;
     a.gathered = P->gathered;
     a.seen = static_cast<int32_t*>(seen);

@@ -11,6 +11,7 @@
 #include <string>
 
 #include "fwd_kernel.cuh"
+#include "fwd_t_kernel.cuh"
 #include "internal.h"
 
 namespace tsr {
@@ -96,10 +97,10 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
   for (int r = 0; r < n_req; ++r) {
     const tsr_plan_impl* P = reqs[r].plan;
     if (P->device != P0->device || P->d != P0->d || P->bn != P0->bn || P->stages != P0->stages ||
-        P->ctas != P0->ctas || P->gathered != P0->gathered)
+        P->ctas != P0->ctas || P->gathered != P0->gathered || P->orient != P0->orient)
       return fail(TSR_ERR_UNSUPPORTED,
-                  "requests of one batch need the same d, regime (bn, stages, ctas) and mask "
-                  "family (key lists or not); plan them with the same tsr_plan_opts");
+                  "requests of one batch need the same d, regime (orientation, bn, stages, ctas) "
+                  "and mask family (key lists or not); plan them with the same tsr_plan_opts");
     temporal = temporal || P->n_temporal > 0;
   }
   const int key = vkey(P0->d, P0->bn, P0->stages, P0->ctas);
@@ -111,9 +112,13 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
       const tsr_plan_impl* P = a.plan;
       fwd::ReqParams& q = prm.req[r];
       const uint64_t D = P->d, N = P->N, BH = static_cast<uint64_t>(P->B) * P->H;
-      const bool ok = encode_tmap_3d(&q.tq, a.q, D, N, BH, 64, kBM) &&
-                      encode_tmap_3d(&q.tk, a.k, D, N, BH, 64, P->bn) &&
-                      encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, P->bn);
+      // key-major plans load 64-row boxes everywhere (a query block, and each
+      // 64-key tile of a step)
+      const uint32_t qrows = P->orient == TSR_ORIENT_KEYS ? 64 : kBM;
+      const uint32_t krows = P->orient == TSR_ORIENT_KEYS ? 64 : P->bn;
+      const bool ok = encode_tmap_3d(&q.tq, a.q, D, N, BH, 64, qrows) &&
+                      encode_tmap_3d(&q.tk, a.k, D, N, BH, 64, krows) &&
+                      encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, krows);
       if (!ok)
         return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
       const int64_t lo = a.item_lo, hi = a.item_hi < 0 ? P->n_items : a.item_hi;
@@ -155,6 +160,10 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
     if (prm.n_items == 0) return TSR_OK;
     TSR_CUDA(cudaMemsetAsync(prm.counter, 0, sizeof(int32_t), stream));
     const int n = prm.n_items, dev = P0->device;
+    if (P0->orient == TSR_ORIENT_KEYS) {
+      const int mode = P0->gathered ? fwd::kModeList : temporal ? fwd::kModePerm : fwd::kModeTma;
+      return fwd_t::launch_t_mode(prm, mode, n, dev, stream);
+    }
     if (P0->gathered) return fwd::launch_mode_list(prm, key, n, dev, stream);
     if (temporal) return fwd::launch_mode_perm(prm, key, n, dev, stream);
     return fwd::launch_mode_tma(prm, key, n, dev, stream);

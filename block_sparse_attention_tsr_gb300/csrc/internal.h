@@ -41,7 +41,11 @@ struct MaskDev {
 
 struct Regime {
   int32_t bn, stages, ctas, id;
+  int32_t orient = TSR_ORIENT_ROWS;   // TSR_ORIENT_ROWS or TSR_ORIENT_KEYS
 };
+
+// Query rows per physical tile of an orientation.
+constexpr int32_t bm_of(int32_t orient) { return orient == TSR_ORIENT_KEYS ? 64 : kBM; }
 
 // A grow-only device buffer owned by a plan.
 struct DevBuf {
@@ -54,6 +58,7 @@ struct tsr_plan_impl {
   int32_t B = 0, H = 0, N = 0, d = 0;
   int32_t kind = 0;
   int32_t bn = 128, stages = 3, ctas = 1, regime_id = -1;
+  int32_t orient = TSR_ORIENT_ROWS, bm = kBM;   // tile orientation and query rows per tile
   int32_t gathered = 0, slice_m = 0;
   int32_t F = 0, S = 0;
   int32_t flags = 0;

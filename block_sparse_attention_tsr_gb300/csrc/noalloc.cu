@@ -18,8 +18,13 @@
 //     the attention runs;
 //   * every call shares the array, and calls whose GPU work overlaps (two host
 //     threads, or two streams) race on it; serialise them;
-//   * the first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress); make that first call before any stream capture.
+//   * the first call on a device (and the first in each new CUDA context on it)
+//     looks up the array's device address (cudaGetSymbolAddress); make that
+//     first call before any stream capture begins;
+//   * every call synchronises its stream (to size the plan and to read the
+//     device error word).
+#include <cudaTypedefs.h>
+
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -39,21 +44,44 @@ namespace {
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[64] = {nullptr};
+CUcontext g_scratch_ctx[64] = {nullptr};   // the context each address belongs to
 
-// Device address of the scratch array on `device` (which must be current);
-// looked up once per device.
+// The calling thread's current CUDA context (the driver entry point is looked
+// up through the runtime, so the library needs no link against libcuda).
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        p == nullptr || q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }
+  CUcontext c = nullptr;
+  return fn(&c) == CUDA_SUCCESS ? c : nullptr;
+}
+
+// Device address of the scratch array on `device` (which must be current):
+// looked up on the first call on the device, and again whenever the current
+// context is not the one the cached address was taken in (after
+// cudaDeviceReset, or under another context), so a stale address is never used.
 tsr_status scratch_address(int device, unsigned char** out) {
   if (device < 0 || device >= 64) return fail(TSR_ERR_UNSUPPORTED, "device index above 63");
+  const CUcontext ctx = current_context();   // null before the runtime has set one up
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[device]) {
+  if (!g_scratch_addr[device] || ctx == nullptr || g_scratch_ctx[device] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      g_scratch_addr[device] = nullptr;
       return cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e,
                        "cudaGetSymbolAddress of the static scratch array");
     }
     g_scratch_addr[device] = p;
+    g_scratch_ctx[device] = current_context();   // the context the lookup ran in
   }
   *out = static_cast<unsigned char*>(g_scratch_addr[device]);
   return TSR_OK;
@@ -91,8 +119,8 @@ extern "C" tsr_status tsr_attention_noalloc(const tsr_mask* mask, const void* q,
   if (!mask) return fail(TSR_ERR_INVALID_ARG, "mask is NULL");
   if (mask->kind != TSR_MASK_UNIFORM && mask->kind != TSR_MASK_SEGMENTS)
     return fail(TSR_ERR_UNSUPPORTED,
-                "tsr_attention_noalloc takes UNIFORM and SEGMENTS masks only (temporal SVG heads "
-                "need a permuted copy of Q, K and V)");
+                "tsr_attention_noalloc plans UNIFORM and SEGMENTS masks only; use tsr_plan for "
+                "SVG and KEYLIST masks");
   if (mask->B <= 0 || mask->H <= 0 || mask->N <= 0 || (mask->d != 64 && mask->d != 128))
     return fail(TSR_ERR_INVALID_ARG, "B, H, N must be > 0 and d 64 or 128");
   if (mask->N > (1 << 24)) return fail(TSR_ERR_UNSUPPORTED, "N above 2^24");
@@ -162,7 +190,14 @@ extern "C" tsr_status tsr_attention_noalloc(const tsr_mask* mask, const void* q,
   if (host_err) return fail(TSR_ERR_INTERNAL, "planner error word " + std::to_string(host_err));
 
   const double density = static_cast<double>(host_tot[6]) / static_cast<double>(n_grid);
-  const Regime rg = regime_lookup(m.kind, m.bq, m.bk, N, density, mask->d);
+  // the table's regime, completed to a compiled variant of the 128-row tiles
+  // this planner builds
+  tsr_plan_opts rows_only{};
+  rows_only.orient = TSR_ORIENT_ROWS;
+  Regime rg;
+  if (tsr_status s = resolve_regime(regime_lookup(m.kind, m.bq, m.bk, N, density, mask->d),
+                                    &rows_only, mask->d, false, &rg))
+    return s;
   const int which = (rg.bn == 64) ? 0 : 1;
   const int64_t n_entries = static_cast<int64_t>(host_tot[2 * which]);
   const int64_t n_desc = static_cast<int64_t>(host_tot[2 * which + 1]);

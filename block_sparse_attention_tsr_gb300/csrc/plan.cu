@@ -223,8 +223,8 @@ __device__ void grid_dims(const MaskDev& m, int64_t* nqs, int64_t* nks) {
 // Per query tile: [0] tiles at BN=64, [1] boundary tiles at BN=64, [2] tiles at
 // BN=128, [3] boundary at BN=128.  Totals: the same four sums, then [4], [5] the
 // longest item at BN=64 / 128, [6] allowed logical blocks.
-__global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
-                                  uint32_t* err) {
+__global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t bm, int32_t* cnt,
+                                  unsigned long long* tot, uint32_t* err) {
   __shared__ unsigned long long bsum[6];
   if (threadIdx.x < 6) bsum[threadIdx.x] = 0;
   __syncthreads();
@@ -234,14 +234,14 @@ __global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t* cnt, unsigned
   if (warp < n_items) {
     const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
     RowSegs rs;
-    rs.q0 = qt * kBM;
-    rs.q1 = min(m.N, qt * kBM + kBM);
+    rs.q0 = qt * bm;
+    rs.q1 = min(m.N, qt * bm + bm);
     rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
                ? 0
                : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
     int64_t nqs, nks;
     grid_dims(m, &nqs, &nks);
-    const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), 128);
+    const KeyWindow kw = key_window(m, h, rs.q0, rs.q1, 128);
     const int n_kt = kw.size();
     int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
     bool bad = false;
@@ -413,22 +413,23 @@ size_t schedule_smem(int64_t n_buckets) {
   return n_buckets <= kSharedBuckets ? static_cast<size_t>(n_buckets) * 4 : 0;
 }
 
-__global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bn, const int32_t* ebegin,
-                                 const int32_t* dbegin, int2* entries, tsr_tile_desc* descs) {
+__global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bm, int32_t bn,
+                                 const int32_t* ebegin, const int32_t* dbegin, int2* entries,
+                                 tsr_tile_desc* descs) {
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
   if (warp >= n_items) return;
   const int bh = static_cast<int>(warp / nqt), qt = static_cast<int>(warp % nqt), h = bh % m.H;
   RowSegs rs;
-  rs.q0 = qt * kBM;
-  rs.q1 = min(m.N, qt * kBM + kBM);
+  rs.q0 = qt * bm;
+  rs.q1 = min(m.N, qt * bm + bm);
   rs.n = (m.kind == TSR_MASK_SVG && m.head_kind[h] == TSR_HEAD_TEMPORAL)
              ? 0
              : tile_segments(m, h, 0, rs.q0, rs.q1, rs.ids, rs.starts);
   int64_t nqs, nks;
   grid_dims(m, &nqs, &nks);
-  const KeyWindow kw = key_window(m, h, qt * kBM, min(m.N, qt * kBM + kBM), bn);
+  const KeyWindow kw = key_window(m, h, rs.q0, rs.q1, bn);
   const int n_kt = kw.size();
   int32_t e_pos = ebegin[warp], d_pos = dbegin[warp];
   for (int base = 0; base < n_kt; base += 32) {
@@ -461,7 +462,8 @@ tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned
   const int64_t n_items = static_cast<int64_t>(m.B) * m.H * nqt;
   const int threads = 256;
   const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
-  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, cnt, tot, err);
+  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, kBM, cnt, tot,
+                                                                             err);
   TSR_CUDA(cudaGetLastError());
   if (n_grid > 0) {
     logical_count_kernel<<<static_cast<unsigned>(std::min<int64_t>(1024, (n_grid + 255) / 256)),
@@ -485,7 +487,8 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
                                                static_cast<int4*>(items));
   TSR_CUDA(cudaGetLastError());
   plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
-      m, nqt, bn, ebegin, dbegin, static_cast<int2*>(entries), static_cast<tsr_tile_desc*>(descs));
+      m, nqt, kBM, bn, ebegin, dbegin, static_cast<int2*>(entries),
+      static_cast<tsr_tile_desc*>(descs));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;
 }
@@ -522,6 +525,24 @@ int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
 
 tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gathered,
                           Regime* out) {
+  // orientation: the caller's, else the table's; key-major tiles exist for
+  // d = 128 only (a table row naming them for d = 64 falls back to 128-row tiles)
+  int32_t orient = (opts && opts->orient) ? opts->orient : rg.orient;
+  if (orient != TSR_ORIENT_KEYS) orient = TSR_ORIENT_ROWS;
+  if (orient == TSR_ORIENT_KEYS && d != 128) {
+    if (opts && opts->orient == TSR_ORIENT_KEYS)
+      return fail(TSR_ERR_UNSUPPORTED, "key-major tiles (TSR_ORIENT_KEYS) need d = 128");
+    orient = TSR_ORIENT_ROWS;
+    if (rg.bn == 0) rg.bn = 64;
+  }
+  if (orient == TSR_ORIENT_KEYS) {
+    // one kernel: 64 x 64 tiles, two per step, fixed rings, one CTA per SM
+    if (opts && opts->bn && opts->bn != 64)
+      return fail(TSR_ERR_UNSUPPORTED, "key-major tiles are 64 keys wide (bn = 64)");
+    *out = Regime{64, 2, 1, (opts && (opts->bn || opts->stages || opts->ctas_per_sm || opts->orient))
+                                ? -1 : rg.id, TSR_ORIENT_KEYS};
+    return TSR_OK;
+  }
   if (opts && (opts->bn || opts->stages || opts->ctas_per_sm)) {
     if (opts->bn && opts->bn != 64 && opts->bn != 128)
       return fail(TSR_ERR_INVALID_ARG, "bn must be 64 or 128");
@@ -535,7 +556,7 @@ tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gath
                   "no kernel variant for d=" + std::to_string(d) + " bn=" + std::to_string(want_bn) +
                       " stages=" + std::to_string(want_st) + " ctas=" + std::to_string(want_ct) +
                       (gathered ? " (gathered)" : ""));
-    *out = Regime{bn, st, ct, -1};
+    *out = Regime{bn, st, ct, -1, TSR_ORIENT_ROWS};
     return TSR_OK;
   }
   if (!variant_exists(d, rg.bn, rg.stages, rg.ctas, gathered)) {
@@ -543,10 +564,11 @@ tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gath
     if (!variant_pick(d, gathered, rg.bn, 0, 0, &bn, &st, &ct) &&
         !variant_pick(d, gathered, 0, 0, 0, &bn, &st, &ct))
       return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(d));
-    *out = Regime{bn, st, ct, rg.id};
+    *out = Regime{bn, st, ct, rg.id, TSR_ORIENT_ROWS};
     return TSR_OK;
   }
   *out = rg;
+  out->orient = TSR_ORIENT_ROWS;
   return TSR_OK;
 }
 
@@ -566,11 +588,6 @@ tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_
 tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
                       cudaStream_t stream) {
   const int32_t B = mask->B, H = mask->H, N = mask->N;
-  const int32_t nqt = (N + kBM - 1) / kBM;
-  const int64_t n_items = static_cast<int64_t>(B) * H * nqt;
-  P->n_items = n_items;
-  if (n_items > (int64_t{1} << 30)) return fail(TSR_ERR_UNSUPPORTED, "too many query tiles");
-
   MaskDev m;
   memset(&m, 0, sizeof m);
   m.kind = mask->kind;
@@ -589,19 +606,15 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   m.R = mask->temporal_radius;
   m.head_kind = P->head_kind_dev;
 
-  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_tot, sizeof(unsigned long long) * 8)) return s;
   if (!P->host_tot) TSR_CUDA(cudaMallocHost(&P->host_tot, sizeof(unsigned long long) * 9));
-  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
   unsigned long long* tot = static_cast<unsigned long long*>(P->b_tot.p);
+  unsigned long long* host_tot = P->host_tot;
   TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
 
-  const int threads = 256;
-  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
-  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, cnt, tot,
-                                                                             P->err);
-  TSR_CUDA(cudaGetLastError());
+  // 1. the mask's density for the regime table (logical blocks counted on the
+  // GPU; SVG from the head kinds, whose host copy was queued by the caller)
   int64_t n_grid = 0;
   if (m.kind == TSR_MASK_UNIFORM) {
     n_grid = static_cast<int64_t>(B) * H * ((N + m.bq - 1) / m.bq) * ((N + m.bk - 1) / m.bk);
@@ -612,20 +625,11 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     logical_count_kernel<<<static_cast<unsigned>(std::min<int64_t>(1024, (n_grid + 255) / 256)),
                            256, 0, stream>>>(m.blocks, n_grid, tot + 6);
     TSR_CUDA(cudaGetLastError());
+    TSR_CUDA(cudaMemcpyAsync(host_tot + 6, tot + 6, sizeof(unsigned long long),
+                             cudaMemcpyDeviceToHost, stream));
   }
-  unsigned long long* host_tot = P->host_tot;
-  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 8, cudaMemcpyDeviceToHost,
-                           stream));
-  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
   TSR_CUDA(cudaStreamSynchronize(stream));
-  const uint32_t host_err = static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull);
-  if (host_err & DEV_ERR_UNSUPPORTED)
-    return fail(TSR_ERR_UNSUPPORTED,
-                "a 128-token tile overlaps more than 8 logical segments (blocks or segments "
-                "smaller than 16 tokens)");
-  if (host_err) return fail(TSR_ERR_INTERNAL, "planner error word " + std::to_string(host_err));
   if (m.kind == TSR_MASK_SVG) {
-    // the head kinds' host copy has arrived with the totals
     for (int32_t h = 0; h < H; ++h) {
       const int8_t k = P->host_kinds[h];
       if (k != TSR_HEAD_SPATIAL && k != TSR_HEAD_TEMPORAL)
@@ -634,8 +638,6 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
       P->n_temporal += k;
     }
   }
-
-  // density of the logical mask, for the regime table
   double density = 0.0;
   if (n_grid > 0) {
     P->n_logical_on = static_cast<int64_t>(host_tot[6]);
@@ -653,6 +655,8 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     P->n_logical_total = static_cast<int64_t>(B) * H * N * static_cast<int64_t>(N);
     density = on / (static_cast<double>(H) * N * static_cast<double>(N));
   }
+
+  // 2. the regime: tile orientation (query rows per tile), width, pipeline
   Regime rg;
   if (tsr_status s = resolve_regime(regime_lookup(m.kind, m.bq, m.bk, N, density, P->d), opts,
                                     P->d, false, &rg))
@@ -661,6 +665,32 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   P->stages = rg.stages;
   P->ctas = rg.ctas;
   P->regime_id = rg.id;
+  P->orient = rg.orient;
+  P->bm = bm_of(rg.orient);
+  const int32_t bm = P->bm;
+  const int32_t nqt = (N + bm - 1) / bm;
+  const int64_t n_items = static_cast<int64_t>(B) * H * nqt;
+  P->n_items = n_items;
+  if (n_items > (int64_t{1} << 30)) return fail(TSR_ERR_UNSUPPORTED, "too many query tiles");
+
+  // 3. tiles per query tile (both widths at the chosen height)
+  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items)) return s;
+  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
+  const int threads = 256;
+  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, bm, cnt, tot,
+                                                                             P->err);
+  TSR_CUDA(cudaGetLastError());
+  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 6, cudaMemcpyDeviceToHost,
+                           stream));
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+  const uint32_t host_err = static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull);
+  if (host_err & DEV_ERR_UNSUPPORTED)
+    return fail(TSR_ERR_UNSUPPORTED,
+                "a " + std::to_string(bm) + "-token tile overlaps more than 8 logical segments "
+                "(blocks or segments smaller than 16 tokens)");
+  if (host_err) return fail(TSR_ERR_INTERNAL, "planner error word " + std::to_string(host_err));
   const int which = (rg.bn == 64) ? 0 : 1;
   P->n_entries = static_cast<int64_t>(host_tot[2 * which]);
   P->n_desc = static_cast<int64_t>(host_tot[2 * which + 1]);
@@ -668,6 +698,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   if (P->n_entries >= (int64_t{1} << 31) || P->n_desc >= (int64_t{1} << 31))
     return fail(TSR_ERR_UNSUPPORTED, "plan has more than 2^31 tiles");
 
+  // 4. longest-first schedule and the tiles themselves
   if (tsr_status s = devbuf_reserve(P->b_items, sizeof(tsr_plan_item) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
   if (tsr_status s = devbuf_reserve(P->b_descs, sizeof(tsr_tile_desc) * P->n_desc)) return s;
@@ -693,7 +724,7 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
       static_cast<int4*>(P->items));
   TSR_CUDA(cudaGetLastError());
   plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
-      m, nqt, rg.bn, ebegin, dbegin, static_cast<int2*>(P->entries),
+      m, nqt, bm, rg.bn, ebegin, dbegin, static_cast<int2*>(P->entries),
       static_cast<tsr_tile_desc*>(P->descs));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;

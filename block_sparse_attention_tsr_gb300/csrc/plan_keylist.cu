@@ -14,6 +14,7 @@
 // both tile widths), the shared schedule kernel (longest first), emit (one
 // block per query tile merges the two lists).
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <string>
 
@@ -466,6 +467,155 @@ __global__ void __launch_bounds__(256) keylist_emit_bitmap_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Key-major plans (64-row query tiles, TSR_ORIENT_KEYS): one work item per
+// 64-query block with its own list, no union.  The list is cut into 64-key
+// gathered tiles in list order; only the last tile can be partly filled (its
+// unused slots are masked), every other tile is full.  gidx holds the lists
+// back to back, each padded to whole tiles with key 0.
+
+// One warp per 64-row query block: validate its list (indptr from 0 upward;
+// keys ascending, unique, inside [0, N)) and count its tiles.  With slice_m =
+// 128 the two 64-row halves of a block share its list.
+__global__ void keylist_t_count_kernel(const int64_t* indptr, const int32_t* indices,
+                                       int64_t n_items, int32_t nqb64, int32_t nqb, int32_t per,
+                                       int32_t N, int32_t* cnt_e, int32_t* cnt_b,
+                                       unsigned long long* tot, uint32_t* err) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n_items) return;
+  const int64_t bh = w / nqb64, qb = w % nqb64;
+  const int64_t row = bh * nqb + qb / per;
+  if (!list_ok(indptr, row)) {
+    if (lane == 0) atomicOr(err, DEV_ERR_BAD_INPUT);
+    return;
+  }
+  const int64_t b = indptr[row], e = indptr[row + 1];
+  bool bad = false;
+  for (int64_t base = b; base < e; base += 32) {
+    const int64_t q = base + lane;
+    const int32_t k = q < e ? indices[q] : INT32_MAX;
+    int32_t nx = __shfl_down_sync(0xFFFFFFFFu, k, 1);
+    if (lane == 31) nx = (q + 1 < e) ? indices[q + 1] : INT32_MAX;
+    if (q < e && (k < 0 || k >= N || (q + 1 < e && nx <= k))) bad = true;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+    if (lane == 0) atomicOr(err, DEV_ERR_BAD_INPUT);
+    return;
+  }
+  if (lane == 0) {
+    const int64_t len = e - b;
+    const int32_t ne = static_cast<int32_t>((len + 63) / 64);
+    const int32_t nb = (len % 64) ? 1 : 0;
+    cnt_e[w] = ne;
+    cnt_b[w] = nb;
+    atomicAdd(&tot[0], static_cast<unsigned long long>(ne));
+    atomicAdd(&tot[1], static_cast<unsigned long long>(nb));
+    atomicMax(&tot[2], static_cast<unsigned long long>(ne));
+  }
+}
+
+// One warp per 64-row query block: its list into gidx (tile t of the block at
+// offset (ebegin + t) * 64, padding slots = key 0), the tiles' entries, and a
+// list-form descriptor per tile (slot e for entry e) marking its listed slots.
+__global__ void keylist_t_emit_kernel(const int64_t* indptr, const int32_t* indices,
+                                      int64_t n_items, int32_t nqb64, int32_t nqb, int32_t per,
+                                      const int32_t* cnt_e, const int32_t* ebegin, int2* entries,
+                                      uint4* descs, int32_t* gidx) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n_items) return;
+  const int64_t bh = w / nqb64, qb = w % nqb64;
+  const int64_t row = bh * nqb + qb / per;
+  const int64_t b = indptr[row], len = indptr[row + 1] - b;
+  const int64_t e0 = ebegin[w];
+  const int32_t ne = cnt_e[w];
+  int32_t* dst = gidx + e0 * 64;
+  for (int64_t i = lane; i < static_cast<int64_t>(ne) * 64; i += 32) dst[i] = i < len ? indices[b + i] : 0;
+  for (int32_t t = lane; t < ne; t += 32) {
+    const int64_t valid = min(static_cast<int64_t>(64), len - static_cast<int64_t>(t) * 64);
+    const uint32_t lo = valid >= 32 ? 0xFFFFFFFFu : ((1u << valid) - 1u);
+    const uint32_t hi = valid >= 64 ? 0xFFFFFFFFu : (valid > 32 ? ((1u << (valid - 32)) - 1u) : 0u);
+    const int64_t e = e0 + t;
+    entries[e] = make_int2(static_cast<int32_t>(e * 64), valid == 64 ? -1 : static_cast<int32_t>(e));
+    descs[2 * e] = make_uint4(lo, hi, 0u, 0u);
+    descs[2 * e + 1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+}  // namespace
+
+namespace {
+
+// Key-major plan of a KEYLIST mask (the regime is known).
+tsr_status plan_build_keylist_t(const tsr_mask* mask, const tsr_plan_opts* opts, const Regime& rg,
+                                tsr_plan_impl* P, cudaStream_t stream) {
+  const int32_t B = mask->B, H = mask->H, N = mask->N, M = mask->slice_m;
+  const int32_t nqb64 = (N + 63) / 64, nqb = (N + M - 1) / M, per = M / 64;
+  const int64_t n_items = static_cast<int64_t>(B) * H * nqb64;
+  P->n_items = n_items;
+  P->bn = 64;
+  P->stages = rg.stages;
+  P->ctas = rg.ctas;
+  P->regime_id = rg.id;
+  P->orient = TSR_ORIENT_KEYS;
+  P->bm = 64;
+  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 2 * n_items)) return s;
+  int32_t* cnt_e = static_cast<int32_t*>(P->b_cnt.p);
+  int32_t* cnt_b = cnt_e + n_items;
+  unsigned long long* tot = static_cast<unsigned long long*>(P->b_tot.p);
+  unsigned long long* host_tot = P->host_tot;
+  const int threads = 256;
+  const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
+  if (n_items > 0) {
+    keylist_t_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
+        mask->indptr, mask->indices, n_items, nqb64, nqb, per, N, cnt_e, cnt_b, tot, P->err);
+    TSR_CUDA(cudaGetLastError());
+  }
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 3, cudaMemcpyDeviceToHost,
+                           stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+  if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
+    return fail(TSR_ERR_INVALID_ARG,
+                "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward");
+  P->n_entries = static_cast<int64_t>(host_tot[0]);
+  P->n_desc = P->n_entries;
+  P->n_gidx = P->n_entries * 64;
+  P->max_item_len = static_cast<int64_t>(host_tot[2]);
+  if (P->n_gidx >= (int64_t{1} << 31))
+    return fail(TSR_ERR_UNSUPPORTED, "gathered plan has more than 2^31 key slots");
+  if (tsr_status s = devbuf_reserve(P->b_items, sizeof(tsr_plan_item) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_entries, sizeof(tsr_plan_entry) * P->n_entries)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_descs, 32 * static_cast<size_t>(P->n_desc))) return s;
+  if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
+  if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
+  const int32_t group_heads = P->group_heads > 0 ? P->group_heads
+                                                 : heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
+  if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_groups * (P->max_item_len + 1) + 1)))
+    return s;
+  P->items = P->b_items.p;
+  P->entries = P->b_entries.p;
+  P->descs = P->b_descs.p;
+  P->gidx = static_cast<int32_t*>(P->b_gidx.p);
+  int32_t* ebegin = static_cast<int32_t*>(P->b_ebegin.p);
+  const int lpt = (opts && (opts->flags & TSR_PLAN_NO_LPT)) ? 0 : 1;
+  if (tsr_status s = plan_schedule_into(cnt_e, cnt_b, n_items, nqb64, H, lpt,
+                                        static_cast<int32_t>(P->max_item_len), group_heads, ebegin,
+                                        static_cast<int32_t*>(P->b_dbegin.p),
+                                        static_cast<int32_t*>(P->b_hist.p), P->items, stream))
+    return s;
+  if (n_items > 0) {
+    keylist_t_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
+        mask->indptr, mask->indices, n_items, nqb64, nqb, per, cnt_e, ebegin,
+        static_cast<int2*>(P->entries), static_cast<uint4*>(P->descs), P->gidx);
+    TSR_CUDA(cudaGetLastError());
+  }
+  return TSR_OK;
+}
+
 }  // namespace
 
 tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_impl* P,
@@ -474,21 +624,41 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   const int32_t nqt = (N + kBM - 1) / kBM, nqb = (N + M - 1) / M;
   const int64_t n_items = static_cast<int64_t>(B) * H * nqt;
   const int64_t n_lists = static_cast<int64_t>(B) * H * nqb;
-  P->n_items = n_items;
   P->gathered = 1;
   P->slice_m = M;
-  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 3 * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_tot, sizeof(unsigned long long) * 8)) return s;
   if (!P->host_tot) TSR_CUDA(cudaMallocHost(&P->host_tot, sizeof(unsigned long long) * 9));
-  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
   unsigned long long* tot = static_cast<unsigned long long*>(P->b_tot.p);
+  unsigned long long* host_tot = P->host_tot;
   TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 8, stream));
   TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
-  const int threads = 256;
-  const bool bitmap = N <= kBitmapMaxN;
-  unsigned long long* host_tot = P->host_tot;
   const char* bad_lists =
       "KEYLIST lists must be ascending, unique and inside [0, N), indptr from 0 upward";
+  // the lists' total length (density for the regime table, which picks the
+  // tile orientation before the lists are counted)
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 6, mask->indptr, sizeof(int64_t), cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaMemcpyAsync(host_tot + 7, mask->indptr + n_lists, sizeof(int64_t),
+                           cudaMemcpyDeviceToHost, stream));
+  TSR_CUDA(cudaStreamSynchronize(stream));
+  const int64_t first = static_cast<int64_t>(host_tot[6]), total = static_cast<int64_t>(host_tot[7]);
+  if (first != 0 || total < 0) return fail(TSR_ERR_INVALID_ARG, bad_lists);
+  if (!mask->indices && total > 0)
+    return fail(TSR_ERR_INVALID_ARG, "indices is NULL but the key lists are not empty");
+  P->n_logical_on = total;
+  P->n_logical_total = n_lists * static_cast<int64_t>(N);
+  const double density = static_cast<double>(total) / static_cast<double>(n_lists) / N;
+  Regime rg;
+  if (tsr_status s = resolve_regime(regime_lookup(TSR_MASK_KEYLIST, M, 1, N, density, P->d), opts,
+                                    P->d, true, &rg))
+    return s;
+  if (rg.orient == TSR_ORIENT_KEYS) return plan_build_keylist_t(mask, opts, rg, P, stream);
+  P->orient = TSR_ORIENT_ROWS;
+  P->bm = kBM;
+  P->n_items = n_items;
+  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 3 * n_items)) return s;
+  int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
+  const int threads = 256;
+  const bool bitmap = N <= kBitmapMaxN;
   if (bitmap) {
     // validation runs inside the count kernel
     static bool attr_done[64] = {false};
@@ -526,13 +696,6 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   if (static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull) & DEV_ERR_BAD_INPUT)
     return fail(TSR_ERR_INVALID_ARG, bad_lists);
 
-  P->n_logical_on = static_cast<int64_t>(host_tot[4]);
-  P->n_logical_total = n_lists * static_cast<int64_t>(N);
-  const double density = static_cast<double>(host_tot[4]) / static_cast<double>(n_lists) / N;
-  Regime rg;
-  if (tsr_status s = resolve_regime(regime_lookup(TSR_MASK_KEYLIST, M, 1, N, density, P->d), opts,
-                                    P->d, true, &rg))
-    return s;
   P->bn = rg.bn;
   P->stages = rg.stages;
   P->ctas = rg.ctas;

@@ -101,7 +101,8 @@ typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
  * KEYLIST : slice_m in {64, 128}.  indptr = int64 [B*H*ceil(N/slice_m) + 1] (CSR
  *           over (b, h, query block), indptr[0] = 0), indices = int32 keys, each
  *           list ascending, unique, in [0, N).  allowed(i, j) = j in the list of
- *           (b, h, i / slice_m).  Violations give TSR_ERR_INVALID_ARG.
+ *           (b, h, i / slice_m).  Violations give TSR_ERR_INVALID_ARG.  indices
+ *           may be NULL when every list is empty.
  *
  * The device arrays must stay valid until the work tsr_plan() queues completes.
  */
@@ -413,10 +414,12 @@ void tsr_release_host_buffers(void);
  *   - All calls share the array and it keeps the last call's contents (the call
  *     clears what must start at zero).  Calls whose GPU work overlaps -- from two
  *     host threads or on two streams -- race on it and must be serialised.
- *   - The first call on a device looks up the array's device address; make that
- *     first call before any stream capture.
- *   - Synchronises `stream` (to size the plan, and at the end to read the device
- *     error word, returned as TSR_ERR_TIMEOUT / TSR_ERR_INTERNAL).
+ *   - The first call on a device looks up the array's device address (again
+ *     whenever the calling thread's CUDA context has changed since, e.g. after
+ *     cudaDeviceReset); make that first call before any stream capture begins.
+ *   - Every call synchronises `stream` (to size the plan, and at the end to read
+ *     the device error word, returned as TSR_ERR_TIMEOUT / TSR_ERR_INTERNAL).
+ *   - Plans 128-row tiles (TSR_ORIENT_ROWS) whatever the regime table picks.
  */
 tsr_status tsr_attention_noalloc(const tsr_mask *mask, const void *q, const void *k,
                                  const void *v, void *out, float *lse, void *stream);

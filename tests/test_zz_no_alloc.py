@@ -4,7 +4,8 @@ Callers whose device memory all comes from their own pool, or who cannot afford
 cudaMalloc / cudaFree on their path, get one entry point that plans into and
 runs over a fixed 32 MiB scratch array inside the library.  These tests call it
 through the C ABI and check it against the allocating path (tsr_plan +
-tsr_bsa_forward) with the parity tolerances, on two calls in a row with
+tsr_bsa_forward) and against the CPU oracle with the parity tolerances, on two
+calls in a row with
 different masks (the shared scratch keeps the previous call's contents), and
 check that a plan too large for the scratch is refused with a clear error.
 
@@ -18,6 +19,7 @@ import pytest
 import torch
 
 import block_sparse_attention_tsr_gb300 as tsr
+import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -42,8 +44,10 @@ def _noalloc(L, mask, q, k, v, out, lse):
 
 
 def _close(o_a, l_a, o_b, l_b):
-    o_a, o_b = o_a.float().cpu().numpy(), o_b.float().cpu().numpy()
-    l_a, l_b = l_a.double().cpu().numpy(), l_b.double().cpu().numpy()
+    """o_a, l_a: the call under test; o_b, l_b: the reference (tensors or arrays)."""
+    as_np = lambda t, f: t if isinstance(t, np.ndarray) else f(t).cpu().numpy()
+    o_a, o_b = as_np(o_a, lambda t: t.float()), as_np(o_b, lambda t: t.float())
+    l_a, l_b = as_np(l_a, lambda t: t.double()), as_np(l_b, lambda t: t.double())
     fin = np.isfinite(l_b)
     assert np.array_equal(np.isfinite(l_a), fin)
     assert np.all(o_a[~fin] == 0.0)
@@ -73,6 +77,8 @@ def test_noalloc_matches_allocating_path_two_calls(L):
         o_ref, l_ref = tsr.tsr_bsa_forward(q, k, v, plan)
         torch.cuda.synchronize()
         _close(out, lse, o_ref, l_ref)
+        o_or, l_or = oracle.attention(spec, q.cpu(), k.cpu(), v.cpu())
+        _close(out, lse, o_or, l_or)
 
 
 def test_noalloc_refuses_plans_beyond_the_scratch(L):
