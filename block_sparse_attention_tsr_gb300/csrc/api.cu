@@ -680,242 +680,249 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     TSR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     hc.ev.push_back(e);
   }
-  // 1. the mask to the device, and one mask view per head group
+  // Steps 1 to 3 run in one function so that every failure, once a copy that
+  // reads or writes the caller's buffers may be queued, still reaches the
+  // synchronisation below.
   cudaStream_t sp = hc.s_plan;
-  std::vector<int64_t> kl_start, kl_base;      // key lists: per-group slices
-  void* kl_dp = nullptr;
-  void* kl_di = nullptr;
-  std::vector<tsr_mask> views(G, *mask);
-  const int64_t nqb = (mask->kind == TSR_MASK_KEYLIST) ? (mask->N + mask->slice_m - 1) / mask->slice_m : 0;
-  if (mask->kind == TSR_MASK_UNIFORM || mask->kind == TSR_MASK_SEGMENTS) {
-    const int64_t per_head = (mask->kind == TSR_MASK_UNIFORM)
-                                 ? static_cast<int64_t>((mask->N + mask->bq - 1) / mask->bq) *
-                                       ((mask->N + mask->bk - 1) / mask->bk)
-                                 : static_cast<int64_t>(mask->n_qseg) * mask->n_kseg;
-    void* db;
-    if (tsr_status s = hc.get(5, BH * per_head, &db)) return s;
-    TSR_CUDA(cudaMemcpyAsync(db, mask->blocks, BH * per_head, cudaMemcpyHostToDevice, sp));
-    const int32_t* qb = nullptr;
-    const int32_t* kb = nullptr;
-    if (mask->kind == TSR_MASK_SEGMENTS) {
-      void* dbnd;
-      const size_t nq = mask->n_qseg + 1, nk = mask->n_kseg + 1;
-      if (tsr_status s = hc.get(6, 4 * (nq + nk), &dbnd)) return s;
-      int32_t* pb = static_cast<int32_t*>(dbnd);
-      TSR_CUDA(cudaMemcpyAsync(pb, mask->q_bounds, 4 * nq, cudaMemcpyHostToDevice, sp));
-      TSR_CUDA(cudaMemcpyAsync(pb + nq, mask->k_bounds, 4 * nk, cudaMemcpyHostToDevice, sp));
-      qb = pb;
-      kb = pb + nq;
-    }
-    for (int64_t g = 0; g < G; ++g) {
-      views[g].blocks = static_cast<const uint8_t*>(db) + gs[g] * per_head;
-      views[g].q_bounds = qb;
-      views[g].k_bounds = kb;
-    }
-  } else if (mask->kind == TSR_MASK_KEYLIST) {
-    const int64_t n_lists = BH * nqb;
-    const int64_t n_idx = mask->indptr[n_lists];   // HOST arrays here
-    if (n_idx < 0 || mask->indptr[0] != 0)
-      return fail(TSR_ERR_INVALID_ARG, "indptr must run upward from 0");
-    // each group's slice of indptr, rebased to start at 0, staged in pinned
-    // memory; the slices and their keys are copied per group in step 2
-    const size_t n_stage = static_cast<size_t>(n_lists + G);
-    if (hc.stage_cap < n_stage) {
-      if (hc.stage) cudaFreeHost(hc.stage);
-      hc.stage = nullptr;
-      hc.stage_cap = 0;
-      TSR_CUDA(cudaMallocHost(&hc.stage, sizeof(int64_t) * n_stage));
-      hc.stage_cap = n_stage;
-    }
-    kl_start.resize(G);
-    kl_base.resize(G + 1);
-    int64_t pos = 0;
-    for (int64_t g = 0; g < G; ++g) {
-      const int64_t l0 = gs[g] * nqb, l1 = gs[g + 1] * nqb;
-      kl_start[g] = pos;
-      kl_base[g] = mask->indptr[l0];
-      for (int64_t l = l0; l <= l1; ++l) hc.stage[pos++] = mask->indptr[l] - kl_base[g];
-    }
-    kl_base[G] = n_idx;
-    if (tsr_status s = hc.get(5, sizeof(int64_t) * n_stage, &kl_dp)) return s;
-    if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &kl_di)) return s;
-    for (int64_t g = 0; g < G; ++g) {
-      views[g].indptr = static_cast<const int64_t*>(kl_dp) + kl_start[g];
-      views[g].indices = static_cast<const int32_t*>(kl_di) + kl_base[g];
-    }
-  } else if (mask->kind == TSR_MASK_SVG) {
-    // head kinds of the flattened (b, h) order
-    std::vector<int8_t> kinds(BH);
-    for (int64_t i = 0; i < BH; ++i) kinds[i] = mask->head_kind[i % mask->H];
-    void* dh;
-    if (tsr_status s = hc.get(7, BH, &dh)) return s;
-    TSR_CUDA(cudaMemcpyAsync(dh, kinds.data(), BH, cudaMemcpyHostToDevice, sp));
-    TSR_CUDA(cudaStreamSynchronize(sp));
-    for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + gs[g];
-  }
-  // 2. inputs, group by group (queued after the mask, which the copy engine
-  // would otherwise move only after every input); key lists go group by group
-  // too, each group's slice just ahead of its inputs, and its plan waits only
-  // for that slice
-  const char* hq = static_cast<const char*>(q);
-  const char* hk = static_cast<const char*>(k);
-  const char* hv = static_cast<const char*>(v);
-  for (int64_t g = 0; g < G; ++g) {
-    const int64_t b0 = gs[g], cnt = gs[g + 1] - gs[g];
-    const size_t off = b0 * row_b, n = cnt * row_b;
-    if (mask->kind == TSR_MASK_KEYLIST) {
-      const int64_t n_ptr = cnt * nqb + 1, k0 = kl_base[g], k1 = kl_base[g + 1];
-      TSR_CUDA(cudaMemcpyAsync(static_cast<int64_t*>(kl_dp) + kl_start[g], hc.stage + kl_start[g],
-                               sizeof(int64_t) * n_ptr, cudaMemcpyHostToDevice, hc.s_in));
-      if (k1 > k0)
-        TSR_CUDA(cudaMemcpyAsync(static_cast<int32_t*>(kl_di) + k0, mask->indices + k0,
-                                 sizeof(int32_t) * (k1 - k0), cudaMemcpyHostToDevice, hc.s_in));
-      TSR_CUDA(cudaEventRecord(hc.ev[3 * G + g], hc.s_in));
-    }
-    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dq) + off, hq + off, n, cudaMemcpyHostToDevice, hc.s_in));
-    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dk) + off, hk + off, n, cudaMemcpyHostToDevice, hc.s_in));
-    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dv) + off, hv + off, n, cudaMemcpyHostToDevice, hc.s_in));
-    TSR_CUDA(cudaEventRecord(hc.ev[3 * g], hc.s_in));
-  }
-  // 3. per head group: its plan (kept from call to call while the grouping and
-  // options are unchanged, re-planned for the new mask), its attention once its
-  // inputs and plan are ready, and its outputs back.  Planning group g + 1 (one
-  // host synchronisation on the plan stream) overlaps attention g.  (Planning
-  // two groups ahead measured slower: a key-list plan then waits for a slice
-  // queued behind the next group's inputs.)  Consecutive groups alternate
-  // between two attention streams, so one persistent launch's last CTAs
-  // overlap the next one's first.
-  const tsr_plan_opts zero{};
-  const tsr_plan_opts& o = opts ? *opts : zero;
-  if (static_cast<int64_t>(hc.plans.size()) != G) {
-    for (tsr_plan_t pl : hc.plans) tsr_plan_destroy(pl);
-    hc.plans.assign(G, nullptr);
-    hc.plan_key.assign(G, {});
-  }
-  if (hc.host_err_cap < static_cast<size_t>(G)) {
-    if (hc.host_err) cudaFreeHost(hc.host_err);
-    hc.host_err = nullptr;
-    hc.host_err_cap = 0;
-    TSR_CUDA(cudaMallocHost(&hc.host_err, sizeof(uint32_t) * G));
-    hc.host_err_cap = G;
-  }
-  auto plan_group = [&](int64_t g) -> tsr_status {
-    tsr_mask& vw = views[g];
-    vw.B = 1;
-    vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
-    const std::array<int64_t, 10> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
-                                          o.flags, o.orient, opts ? 1 : 0};
-    if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
-    tsr_status st;
-    if (hc.plans[g] && hc.plan_key[g] == key) {
-      st = tsr_plan_update(hc.plans[g], &vw, sp);
-    } else {
-      if (hc.plans[g]) tsr_plan_destroy(hc.plans[g]);
-      hc.plans[g] = nullptr;
-      st = tsr_plan(&vw, opts, &hc.plans[g], sp);
-      hc.plan_key[g] = key;
-    }
-    if (st != TSR_OK) return st;
-    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 1], sp));
-    return TSR_OK;
-  };
-  auto launch_group = [&](int64_t g) -> tsr_status {
-    cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
-    const int64_t b0 = gs[g];
-    const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
-    TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
-    TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g + 1], 0));
-    if (tsr_status st = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
-                                        static_cast<char*>(dv) + off, hc.plans[g],
-                                        static_cast<char*>(dout) + off,
-                                        static_cast<float*>(dlse) + b0 * mask->N, sa))
-      return st;
-    TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
-    TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
-    TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
-                             cudaMemcpyDeviceToHost, hc.s_out));
-    TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
-                             static_cast<size_t>(n / row_b) * mask->N * 4, cudaMemcpyDeviceToHost,
-                             hc.s_out));
-    // the group's device error word (its kernels have run once s_out gets here)
-    TSR_CUDA(cudaMemcpyAsync(hc.host_err + g, hc.plans[g]->err, sizeof(uint32_t),
-                             cudaMemcpyDeviceToHost, hc.s_out));
-    TSR_CUDA(cudaMemsetAsync(hc.plans[g]->err, 0, sizeof(uint32_t), hc.s_out));
-    return TSR_OK;
-  };
-  // One-plan mode (every mask form but key lists, whose slices arrive group by
-  // group, and without the debug / synchronous-check / test flags, which check
-  // each launch): one plan over every head with one head per longest-first
-  // group, so head group g's work items are the contiguous range
-  // [gs[g] * nqt, gs[g + 1] * nqt); each group's launch takes its range and its
-  // own work counter.  Planning happens once, while the first inputs copy in.
-  const bool one_plan =
-      mask->kind != TSR_MASK_KEYLIST &&
-      !(o.flags & (TSR_PLAN_DEBUG_CHECKS | TSR_PLAN_SYNC_CHECK | TSR_PLAN_TEST_STALL));
   int64_t n_err = G;
-  tsr_status s = TSR_OK;
-  if (one_plan) {
-    n_err = 1;
-    tsr_mask full = views[0];                  // device arrays from their start
-    full.B = mask->B;
-    full.H = mask->H;
-    const std::array<int64_t, 11> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
-                                          o.stages, o.ctas_per_sm, o.flags, o.orient, opts ? 1 : 0};
-    if (hc.full_plan && hc.full_key == key) {
-      s = tsr_plan_update(hc.full_plan, &full, sp);
-    } else {
-      if (hc.full_plan) tsr_plan_destroy(hc.full_plan);
-      hc.full_plan = nullptr;
-      s = plan_new(&full, opts, 1, sp, &hc.full_plan);
-      hc.full_key = key;
+  const tsr_status s_run = [&]() -> tsr_status {
+    // 1. the mask to the device, and one mask view per head group
+    std::vector<int64_t> kl_start, kl_base;      // key lists: per-group slices
+    void* kl_dp = nullptr;
+    void* kl_di = nullptr;
+    std::vector<tsr_mask> views(G, *mask);
+    const int64_t nqb = (mask->kind == TSR_MASK_KEYLIST) ? (mask->N + mask->slice_m - 1) / mask->slice_m : 0;
+    if (mask->kind == TSR_MASK_UNIFORM || mask->kind == TSR_MASK_SEGMENTS) {
+      const int64_t per_head = (mask->kind == TSR_MASK_UNIFORM)
+                                   ? static_cast<int64_t>((mask->N + mask->bq - 1) / mask->bq) *
+                                         ((mask->N + mask->bk - 1) / mask->bk)
+                                   : static_cast<int64_t>(mask->n_qseg) * mask->n_kseg;
+      void* db;
+      if (tsr_status s = hc.get(5, BH * per_head, &db)) return s;
+      TSR_CUDA(cudaMemcpyAsync(db, mask->blocks, BH * per_head, cudaMemcpyHostToDevice, sp));
+      const int32_t* qb = nullptr;
+      const int32_t* kb = nullptr;
+      if (mask->kind == TSR_MASK_SEGMENTS) {
+        void* dbnd;
+        const size_t nq = mask->n_qseg + 1, nk = mask->n_kseg + 1;
+        if (tsr_status s = hc.get(6, 4 * (nq + nk), &dbnd)) return s;
+        int32_t* pb = static_cast<int32_t*>(dbnd);
+        TSR_CUDA(cudaMemcpyAsync(pb, mask->q_bounds, 4 * nq, cudaMemcpyHostToDevice, sp));
+        TSR_CUDA(cudaMemcpyAsync(pb + nq, mask->k_bounds, 4 * nk, cudaMemcpyHostToDevice, sp));
+        qb = pb;
+        kb = pb + nq;
+      }
+      for (int64_t g = 0; g < G; ++g) {
+        views[g].blocks = static_cast<const uint8_t*>(db) + gs[g] * per_head;
+        views[g].q_bounds = qb;
+        views[g].k_bounds = kb;
+      }
+    } else if (mask->kind == TSR_MASK_KEYLIST) {
+      const int64_t n_lists = BH * nqb;
+      const int64_t n_idx = mask->indptr[n_lists];   // HOST arrays here
+      if (n_idx < 0 || mask->indptr[0] != 0)
+        return fail(TSR_ERR_INVALID_ARG, "indptr must run upward from 0");
+      // each group's slice of indptr, rebased to start at 0, staged in pinned
+      // memory; the slices and their keys are copied per group in step 2
+      const size_t n_stage = static_cast<size_t>(n_lists + G);
+      if (hc.stage_cap < n_stage) {
+        if (hc.stage) cudaFreeHost(hc.stage);
+        hc.stage = nullptr;
+        hc.stage_cap = 0;
+        TSR_CUDA(cudaMallocHost(&hc.stage, sizeof(int64_t) * n_stage));
+        hc.stage_cap = n_stage;
+      }
+      kl_start.resize(G);
+      kl_base.resize(G + 1);
+      int64_t pos = 0;
+      for (int64_t g = 0; g < G; ++g) {
+        const int64_t l0 = gs[g] * nqb, l1 = gs[g + 1] * nqb;
+        kl_start[g] = pos;
+        kl_base[g] = mask->indptr[l0];
+        for (int64_t l = l0; l <= l1; ++l) hc.stage[pos++] = mask->indptr[l] - kl_base[g];
+      }
+      kl_base[G] = n_idx;
+      if (tsr_status s = hc.get(5, sizeof(int64_t) * n_stage, &kl_dp)) return s;
+      if (tsr_status s = hc.get(6, sizeof(int32_t) * static_cast<size_t>(n_idx), &kl_di)) return s;
+      for (int64_t g = 0; g < G; ++g) {
+        views[g].indptr = static_cast<const int64_t*>(kl_dp) + kl_start[g];
+        views[g].indices = static_cast<const int32_t*>(kl_di) + kl_base[g];
+      }
+    } else if (mask->kind == TSR_MASK_SVG) {
+      // head kinds of the flattened (b, h) order
+      std::vector<int8_t> kinds(BH);
+      for (int64_t i = 0; i < BH; ++i) kinds[i] = mask->head_kind[i % mask->H];
+      void* dh;
+      if (tsr_status s = hc.get(7, BH, &dh)) return s;
+      TSR_CUDA(cudaMemcpyAsync(dh, kinds.data(), BH, cudaMemcpyHostToDevice, sp));
+      TSR_CUDA(cudaStreamSynchronize(sp));
+      for (int64_t g = 0; g < G; ++g) views[g].head_kind = static_cast<const int8_t*>(dh) + gs[g];
     }
-    if (s == TSR_OK && hc.counters_cap < static_cast<size_t>(G)) {
-      cudaFree(hc.counters);
-      hc.counters = nullptr;
-      hc.counters_cap = 0;
-      const cudaError_t e = cudaMalloc(&hc.counters, sizeof(int32_t) * G);
-      if (e != cudaSuccess) s = cuda_fail(e, "work counters");
-      else hc.counters_cap = G;
+    // 2. inputs, group by group (queued after the mask, which the copy engine
+    // would otherwise move only after every input); key lists go group by group
+    // too, each group's slice just ahead of its inputs, and its plan waits only
+    // for that slice
+    const char* hq = static_cast<const char*>(q);
+    const char* hk = static_cast<const char*>(k);
+    const char* hv = static_cast<const char*>(v);
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t b0 = gs[g], cnt = gs[g + 1] - gs[g];
+      const size_t off = b0 * row_b, n = cnt * row_b;
+      if (mask->kind == TSR_MASK_KEYLIST) {
+        const int64_t n_ptr = cnt * nqb + 1, k0 = kl_base[g], k1 = kl_base[g + 1];
+        TSR_CUDA(cudaMemcpyAsync(static_cast<int64_t*>(kl_dp) + kl_start[g], hc.stage + kl_start[g],
+                                 sizeof(int64_t) * n_ptr, cudaMemcpyHostToDevice, hc.s_in));
+        if (k1 > k0)
+          TSR_CUDA(cudaMemcpyAsync(static_cast<int32_t*>(kl_di) + k0, mask->indices + k0,
+                                   sizeof(int32_t) * (k1 - k0), cudaMemcpyHostToDevice, hc.s_in));
+        TSR_CUDA(cudaEventRecord(hc.ev[3 * G + g], hc.s_in));
+      }
+      TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dq) + off, hq + off, n, cudaMemcpyHostToDevice, hc.s_in));
+      TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dk) + off, hk + off, n, cudaMemcpyHostToDevice, hc.s_in));
+      TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(dv) + off, hv + off, n, cudaMemcpyHostToDevice, hc.s_in));
+      TSR_CUDA(cudaEventRecord(hc.ev[3 * g], hc.s_in));
     }
-    if (s == TSR_OK) TSR_CUDA(cudaEventRecord(hc.ev[1], sp));
-    const int64_t nqt = hc.full_plan ? (mask->N + hc.full_plan->bm - 1) / hc.full_plan->bm : 0;
-    for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+    // 3. per head group: its plan (kept from call to call while the grouping and
+    // options are unchanged, re-planned for the new mask), its attention once its
+    // inputs and plan are ready, and its outputs back.  Planning group g + 1 (one
+    // host synchronisation on the plan stream) overlaps attention g.  (Planning
+    // two groups ahead measured slower: a key-list plan then waits for a slice
+    // queued behind the next group's inputs.)  Consecutive groups alternate
+    // between two attention streams, so one persistent launch's last CTAs
+    // overlap the next one's first.
+    const tsr_plan_opts zero{};
+    const tsr_plan_opts& o = opts ? *opts : zero;
+    if (static_cast<int64_t>(hc.plans.size()) != G) {
+      for (tsr_plan_t pl : hc.plans) tsr_plan_destroy(pl);
+      hc.plans.assign(G, nullptr);
+      hc.plan_key.assign(G, {});
+    }
+    if (hc.host_err_cap < static_cast<size_t>(G)) {
+      if (hc.host_err) cudaFreeHost(hc.host_err);
+      hc.host_err = nullptr;
+      hc.host_err_cap = 0;
+      TSR_CUDA(cudaMallocHost(&hc.host_err, sizeof(uint32_t) * G));
+      hc.host_err_cap = G;
+    }
+    auto plan_group = [&](int64_t g) -> tsr_status {
+      tsr_mask& vw = views[g];
+      vw.B = 1;
+      vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
+      const std::array<int64_t, 10> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
+                                            o.flags, o.orient, opts ? 1 : 0};
+      if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
+      tsr_status st;
+      if (hc.plans[g] && hc.plan_key[g] == key) {
+        st = tsr_plan_update(hc.plans[g], &vw, sp);
+      } else {
+        if (hc.plans[g]) tsr_plan_destroy(hc.plans[g]);
+        hc.plans[g] = nullptr;
+        st = tsr_plan(&vw, opts, &hc.plans[g], sp);
+        hc.plan_key[g] = key;
+      }
+      if (st != TSR_OK) return st;
+      TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 1], sp));
+      return TSR_OK;
+    };
+    auto launch_group = [&](int64_t g) -> tsr_status {
       cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
       const int64_t b0 = gs[g];
       const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
       TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
-      TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[1], 0));
-      FwdArgs a;
-      a.q = dq;
-      a.k = dk;
-      a.v = dv;
-      a.out = dout;
-      a.lse = static_cast<float*>(dlse);
-      a.plan = hc.full_plan;
-      a.item_lo = gs[g] * nqt;
-      a.item_hi = gs[g + 1] * nqt;
-      a.counter = hc.counters + g;
-      s = launch_forward(a, sa);
-      if (s != TSR_OK) break;
+      TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g + 1], 0));
+      if (tsr_status st = tsr_bsa_forward(static_cast<char*>(dq) + off, static_cast<char*>(dk) + off,
+                                          static_cast<char*>(dv) + off, hc.plans[g],
+                                          static_cast<char*>(dout) + off,
+                                          static_cast<float*>(dlse) + b0 * mask->N, sa))
+        return st;
       TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
       TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
       TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
                                cudaMemcpyDeviceToHost, hc.s_out));
       TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
-                               static_cast<size_t>(n / row_b) * mask->N * 4,
+                               static_cast<size_t>(n / row_b) * mask->N * 4, cudaMemcpyDeviceToHost,
+                               hc.s_out));
+      // the group's device error word (its kernels have run once s_out gets here)
+      TSR_CUDA(cudaMemcpyAsync(hc.host_err + g, hc.plans[g]->err, sizeof(uint32_t),
                                cudaMemcpyDeviceToHost, hc.s_out));
+      TSR_CUDA(cudaMemsetAsync(hc.plans[g]->err, 0, sizeof(uint32_t), hc.s_out));
+      return TSR_OK;
+    };
+    // One-plan mode (every mask form but key lists, whose slices arrive group by
+    // group, and without the debug / synchronous-check / test flags, which check
+    // each launch): one plan over every head with one head per longest-first
+    // group, so head group g's work items are the contiguous range
+    // [gs[g] * nqt, gs[g + 1] * nqt); each group's launch takes its range and its
+    // own work counter.  Planning happens once, while the first inputs copy in.
+    const bool one_plan =
+        mask->kind != TSR_MASK_KEYLIST &&
+        !(o.flags & (TSR_PLAN_DEBUG_CHECKS | TSR_PLAN_SYNC_CHECK | TSR_PLAN_TEST_STALL));
+    tsr_status s = TSR_OK;
+    if (one_plan) {
+      n_err = 1;
+      tsr_mask full = views[0];                  // device arrays from their start
+      full.B = mask->B;
+      full.H = mask->H;
+      const std::array<int64_t, 11> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
+                                            o.stages, o.ctas_per_sm, o.flags, o.orient, opts ? 1 : 0};
+      if (hc.full_plan && hc.full_key == key) {
+        s = tsr_plan_update(hc.full_plan, &full, sp);
+      } else {
+        if (hc.full_plan) tsr_plan_destroy(hc.full_plan);
+        hc.full_plan = nullptr;
+        s = plan_new(&full, opts, 1, sp, &hc.full_plan);
+        hc.full_key = key;
+      }
+      if (s == TSR_OK && hc.counters_cap < static_cast<size_t>(G)) {
+        cudaFree(hc.counters);
+        hc.counters = nullptr;
+        hc.counters_cap = 0;
+        const cudaError_t e = cudaMalloc(&hc.counters, sizeof(int32_t) * G);
+        if (e != cudaSuccess) s = cuda_fail(e, "work counters");
+        else hc.counters_cap = G;
+      }
+      if (s == TSR_OK) TSR_CUDA(cudaEventRecord(hc.ev[1], sp));
+      const int64_t nqt = hc.full_plan ? (mask->N + hc.full_plan->bm - 1) / hc.full_plan->bm : 0;
+      for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+        cudaStream_t sa = (g & 1) ? hc.stream2 : hc.stream;
+        const int64_t b0 = gs[g];
+        const size_t off = b0 * row_b, n = (gs[g + 1] - gs[g]) * row_b;
+        TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[3 * g], 0));
+        TSR_CUDA(cudaStreamWaitEvent(sa, hc.ev[1], 0));
+        FwdArgs a;
+        a.q = dq;
+        a.k = dk;
+        a.v = dv;
+        a.out = dout;
+        a.lse = static_cast<float*>(dlse);
+        a.plan = hc.full_plan;
+        a.item_lo = gs[g] * nqt;
+        a.item_hi = gs[g + 1] * nqt;
+        a.counter = hc.counters + g;
+        s = launch_forward(a, sa);
+        if (s != TSR_OK) break;
+        TSR_CUDA(cudaEventRecord(hc.ev[3 * g + 2], sa));
+        TSR_CUDA(cudaStreamWaitEvent(hc.s_out, hc.ev[3 * g + 2], 0));
+        TSR_CUDA(cudaMemcpyAsync(static_cast<char*>(out) + off, static_cast<char*>(dout) + off, n,
+                                 cudaMemcpyDeviceToHost, hc.s_out));
+        TSR_CUDA(cudaMemcpyAsync(lse + b0 * mask->N, static_cast<float*>(dlse) + b0 * mask->N,
+                                 static_cast<size_t>(n / row_b) * mask->N * 4,
+                                 cudaMemcpyDeviceToHost, hc.s_out));
+      }
+      if (s == TSR_OK) {
+        TSR_CUDA(cudaMemcpyAsync(hc.host_err, hc.full_plan->err, sizeof(uint32_t),
+                                 cudaMemcpyDeviceToHost, hc.s_out));
+        TSR_CUDA(cudaMemsetAsync(hc.full_plan->err, 0, sizeof(uint32_t), hc.s_out));
+      }
+    } else {
+      for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
+        s = plan_group(g);
+        if (s == TSR_OK) s = launch_group(g);
+      }
     }
-    if (s == TSR_OK) {
-      TSR_CUDA(cudaMemcpyAsync(hc.host_err, hc.full_plan->err, sizeof(uint32_t),
-                               cudaMemcpyDeviceToHost, hc.s_out));
-      TSR_CUDA(cudaMemsetAsync(hc.full_plan->err, 0, sizeof(uint32_t), hc.s_out));
-    }
-  } else {
-    for (int64_t g = 0; g < G && s == TSR_OK; ++g) {
-      s = plan_group(g);
-      if (s == TSR_OK) s = launch_group(g);
-    }
-  }
+    return s;
+  }();
+  tsr_status s = s_run;
   // no copy may still read or write the caller's buffers after the return
   const cudaError_t e1 = cudaStreamSynchronize(hc.s_out);
   const cudaError_t e2 = cudaStreamSynchronize(hc.stream);

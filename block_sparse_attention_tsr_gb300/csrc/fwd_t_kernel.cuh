@@ -17,14 +17,16 @@
 // abstract: physical tiles chosen by mask shape, here subdividing the 128-row
 // tile; FG-Attn abstract: skipping at 64-query x 1-key slice granularity).
 //
-// One CTA per SM works on one item at a time, 352 threads:
+// One CTA per SM works on one item at a time, 384 threads:
 //   warp 0      K producer: the item's 64-row query tile, then per step its two
-//               64-key tiles of K (two-slot ring), by TMA, or by row gathers
-//               for key lists and temporal-major items
-//   warp 1      MMA issuer (one thread): QK of step i, then PV of step i - 3,
-//               so three steps of S^T are in flight while their softmax runs
-//   warp 2      V producer: the same for V (two-slot ring); V loads wait for
-//               PVs, so they run in a warp of their own and never hold up K
+//               64-key tiles of K, by TMA, or by row gathers for key lists and
+//               temporal-major items; step j goes to slot j & 1
+//   warp 2      V producer: the same for V; V loads wait for PVs, so they run
+//               in a warp of their own and never hold up K
+//   warps 1, 11 MMA issuers (one thread each), one per softmax group: QK of the
+//               group's step t, then PV of its step t - 1.  One issuing thread
+//               leaves the tensor pipe idle whenever it waits on a barrier (its
+//               queue holds only a few MMAs); two keep it fed
 //   warps 3..6  softmax group 0: the item's even steps
 //   warps 7..10 softmax group 1: the item's odd steps
 // Each group keeps its own running maximum, row sums, two P^T buffers and O^T
@@ -50,6 +52,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cmath>
 #include <cstring>
 
@@ -69,9 +72,8 @@ using fwd::ReqParams;
 constexpr int D = 128;                 // head dimension of this kernel
 constexpr int QB = 64;                 // query rows per item
 constexpr int KT = 64;                 // keys per plan tile (two per step)
-constexpr int KS = 2, VS = 2;          // K and V ring slots
-constexpr int LAG = 3;                 // QK of step i is issued before PV of step i - LAG
-constexpr int kThreads = 352;
+constexpr int KS = 2, VS = 2;          // K and V slots: slot g feeds group g's steps
+constexpr int kThreads = 384;
 constexpr float kFixThreshold = 16.0f; // base-2 units above the reference maximum
 constexpr float kClamp = 64.0f;        // exponent cap of the optimistic pass (2^64 stays finite)
 constexpr float kMrefInit = -1.0e30f;  // reference maximum of a query with no key yet
@@ -110,11 +112,11 @@ struct alignas(16) CtrlT {
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], o_full, o_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t grp[2], pair;
-  uint64_t final_bar, never;
+  uint64_t final_bar[2], never;
   int32_t item_slot[2];
   int32_t fixflag[2][2];
-  float mref[2][QB];
-  float mold[2][QB];          // the reference before the last raise (correction path)
+  alignas(16) float mref[2][QB];   // read as float4 by the softmax
+  alignas(16) float mold[2][QB];   // the reference before the last raise (correction path)
   float alpha[2][QB];
   float red[2][4][QB];
   float lsum[2][QB];
@@ -123,6 +125,10 @@ struct alignas(16) CtrlT {
   uint32_t tmem_base;
   int32_t abort_flag;
 };
+
+// The softmax reads 4 reference maxima at a time (16-byte loads).
+static_assert(offsetof(CtrlT, mref) % 16 == 0 && offsetof(CtrlT, mold) % 16 == 0,
+              "reference maxima must be 16-byte aligned");
 
 __device__ __forceinline__ int32_t unpermute(int32_t tp, int32_t F, int32_t S) {
   return (tp % F) * S + tp / F;
@@ -189,33 +195,77 @@ __device__ __forceinline__ void warp_reduce(float (&v)[NV], int lane) {
 // second tile repeats the first tile's rows) and temporal-major items (rows
 // through the inverse permutation; rows past N read row 0).  Gathered rows
 // complete on the barrier through cp.async arrive plus lane 0's arrival.
-template <bool GATHER, bool PERM>
-__device__ __forceinline__ void load_kv_step(const ReqParams& rq, int32_t bh, int32_t begin, int32_t n,
-                                             int32_t layout, int32_t step, const CUtensorMap* map,
+// The item's plan entries held in a producer warp's lanes, one 32-entry chunk
+// ahead of use: lane l holds entry begin + 32 c + l of the current chunk c and
+// of chunk c + 1.  A step's two key tiles are then read with shuffles, and the
+// load of the next chunk is issued 16 steps before it is needed, so no copy
+// waits behind a dependent global load.  All 32 lanes call every member.
+struct EntryWindow {
+  int32_t cur, nxt, chunk;
+  __device__ __forceinline__ void start(const ReqParams& rq, int32_t begin, int32_t n, int lane) {
+    chunk = 0;
+    cur = lane < n ? __ldg(&rq.entries[begin + lane]).x : 0;
+    nxt = 32 + lane < n ? __ldg(&rq.entries[begin + 32 + lane]).x : 0;
+  }
+  // Key block of tile t (t = 2 * step + h); steps advance one at a time.
+  __device__ __forceinline__ int32_t tile(const ReqParams& rq, int32_t begin, int32_t n, int32_t t,
+                                          int lane) {
+    const int32_t c = t >> 5;
+    if (c != chunk) {
+      chunk = c;
+      cur = nxt;
+      const int32_t e = 32 * (c + 1) + lane;
+      nxt = e < n ? __ldg(&rq.entries[begin + e]).x : 0;
+    }
+    return __shfl_sync(0xFFFFFFFFu, cur, t & 31);
+  }
+};
+
+// The two key tiles of step `step`: kv0, and kv1 for the second (a missing
+// second tile: rq.N for TMA, which then reads rows past N as zeros; the first
+// tile again for gathers).
+__device__ __forceinline__ void step_tiles(EntryWindow& win, const ReqParams& rq, int32_t begin,
+                                           int32_t n, int32_t step, bool gath, int lane,
+                                           int32_t& kv0, int32_t& kv1) {
+  kv0 = win.tile(rq, begin, n, 2 * step, lane);
+  const int32_t t1 = win.tile(rq, begin, n, 2 * step + 1, lane);
+  kv1 = (2 * step + 1 < n) ? t1 : (gath ? kv0 : rq.N);
+}
+
+// Source rows of a gathered step, tile h rows lane and lane + 32 in rows[h]:
+// key-list rows named by gidx, or temporal-major rows through the inverse
+// permutation (rows past N read row 0).
+template <bool GATHER>
+__device__ __forceinline__ void step_rows(const ReqParams& rq, int32_t kv0, int32_t kv1, int lane,
+                                          int32_t (&rows)[2][2]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int32_t kv = h ? kv1 : kv0;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      if (GATHER) {
+        rows[h][m] = __ldg(rq.gidx + kv + 32 * m + lane);
+      } else {
+        const int32_t tp = kv + 32 * m + lane;
+        rows[h][m] = tp < rq.N ? unpermute(tp, rq.F, rq.S) : 0;
+      }
+    }
+  }
+}
+
+// One step's K (or V) rows for the two key tiles into a ring slot
+// ([d chunk][128 rows][128 B], the first tile in rows 0..63): TMA for
+// contiguous tiles, row gathers (rows from step_rows) for key lists and
+// temporal-major items.  Gathered rows complete on the barrier through
+// cp.async arrive plus lane 0's arrival.
+__device__ __forceinline__ void load_kv_step(bool gath, int32_t bh, int32_t N, int32_t kv0, int32_t kv1,
+                                             const int32_t (&rows)[2][2], const CUtensorMap* map,
                                              const __nv_bfloat16* src, uint32_t dst, uint32_t bar,
                                              int lane) {
-  const bool gath = GATHER || (PERM && layout != 0);
-  const int32_t e0 = begin + 2 * step, e1 = e0 + 1;
-  const bool has1 = e1 < begin + n;
-  const int32_t kv0 = __ldg(&rq.entries[e0]).x;
-  const int32_t kv1 = has1 ? __ldg(&rq.entries[e1]).x : (gath ? kv0 : rq.N);
   if (gath) {
-    const __nv_bfloat16* head = src + static_cast<size_t>(bh) * rq.N * D;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int32_t kv = h ? kv1 : kv0;
-      int32_t rows[2];
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        if (GATHER) {
-          rows[m] = __ldg(rq.gidx + kv + 32 * m + lane);
-        } else {
-          const int32_t tp = kv + 32 * m + lane;
-          rows[m] = tp < rq.N ? unpermute(tp, rq.F, rq.S) : 0;
-        }
-      }
-      gather64(head, rows, dst + h * KT * 128, 2 * KT * 128, lane);
-    }
+    const __nv_bfloat16* head = src + static_cast<size_t>(bh) * N * D;
+    gather64(head, rows[0], dst, 2 * KT * 128, lane);
+    gather64(head, rows[1], dst + KT * 128, 2 * KT * 128, lane);
     cp_async_arrive(bar);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
@@ -225,6 +275,36 @@ __device__ __forceinline__ void load_kv_step(const ReqParams& rq, int32_t bh, in
       for (int c = 0; c < 2; ++c)
         tma_load_3d(dst + c * (2 * KT * 128) + h * KT * 128, map, bar, c * 64, h ? kv1 : kv0, bh);
   }
+}
+
+// The K or V stream of one item, steps [0, ns): step j goes to slot j & 1, the
+// slot of the group that consumes it (group j & 1), so each slot is a channel
+// between the producer and one MMA issuer; cnt[s] counts the loads into slot s.
+// The next step's tiles (and, for gathers, its source rows) are read while the
+// current step's slot is awaited.  Returns false when a wait gave up.
+template <bool GATHER, bool PERM, typename WaitFn>
+__device__ __forceinline__ bool stream_item(const ReqParams& rq, int32_t bh, int32_t begin, int32_t n,
+                                            int32_t layout, int32_t ns, const CUtensorMap* map,
+                                            const __nv_bfloat16* src, uint32_t ring, uint64_t* full,
+                                            uint64_t* empty, uint32_t (&cnt)[2], int site, int lane,
+                                            WaitFn&& wait) {
+  const bool gath = GATHER || (PERM && layout != 0);
+  EntryWindow win;
+  win.start(rq, begin, n, lane);
+  int32_t kv0, kv1, rows[2][2] = {{0, 0}, {0, 0}};
+  step_tiles(win, rq, begin, n, 0, gath, lane, kv0, kv1);
+  if (gath) step_rows<GATHER>(rq, kv0, kv1, lane, rows);
+  for (int32_t i = 0; i < ns; ++i) {
+    const int s = i & 1;
+    if (!wait(smem_u32(&empty[s]), (cnt[s] & 1) ^ 1, site)) return false;
+    load_kv_step(gath, bh, rq.N, kv0, kv1, rows, map, src, ring + s * KV_BYTES, smem_u32(&full[s]), lane);
+    ++cnt[s];
+    if (i + 1 < ns) {
+      step_tiles(win, rq, begin, n, i + 1, gath, lane, kv0, kv1);
+      if (gath) step_rows<GATHER>(rq, kv0, kv1, lane, rows);
+    }
+  }
+  return true;
 }
 
 template <int MODE, int MAXR>
@@ -240,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctrl.q_full), 1);
-    mbar_init(smem_u32(&ctrl.q_empty), 1);
+    mbar_init(smem_u32(&ctrl.q_empty), 2);                // both MMA issuers
     for (int s = 0; s < KS; ++s) {
       mbar_init(smem_u32(&ctrl.k_full[s]), 1);
       mbar_init(smem_u32(&ctrl.k_empty[s]), 1);
@@ -259,12 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
       mbar_init(smem_u32(&ctrl.grp[g]), 4);
       ctrl.fixflag[g][0] = ctrl.fixflag[g][1] = -1;
       mbar_init(smem_u32(&ctrl.item_full[g]), 1);
-      mbar_init(smem_u32(&ctrl.item_empty[g]), 10);  // MMA issuer, V producer, 8 softmax warps
+      mbar_init(smem_u32(&ctrl.item_empty[g]), 11);  // 2 MMA issuers, V producer, 8 softmax warps
+      mbar_init(smem_u32(&ctrl.final_bar[g]), 1);
     }
-    mbar_init(smem_u32(&ctrl.o_full), 1);
+    mbar_init(smem_u32(&ctrl.o_full), 2);                 // both MMA issuers
     mbar_init(smem_u32(&ctrl.o_empty), 8);
     mbar_init(smem_u32(&ctrl.pair), 8);
-    mbar_init(smem_u32(&ctrl.final_bar), 1);
     mbar_init(smem_u32(&ctrl.never), 1);
     ctrl.abort_flag = 0;
     fence_mbar_init();
@@ -301,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
       tma_prefetch_desc(&p.req[0].tk);
       tma_prefetch_desc(&p.req[0].tv);
     }
-    uint32_t kc = 0, qc = 0, seq = 0;
+    uint32_t kc[2] = {0u, 0u}, qc = 0, seq = 0;
     bool ok = true;
     while (ok) {
       int32_t it = 0;
@@ -345,25 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
             tma_load_3d(base + OFF_Q + c * QB * 128, &rq.tq, bar, c * 64, qb * QB, bh);
         }
       }
-      for (int32_t i = 0; i < ns && ok; ++i) {
-        const int s = kc % KS;
-        if (!wait(smem_u32(&ctrl.k_empty[s]), ((kc / KS) & 1) ^ 1, 2)) { ok = false; break; }
-        load_kv_step<GATHER, PERM>(rq, bh, begin, n, layout, i, &rq.tk, rq.kg,
-                                   base + OFF_K + s * KV_BYTES, smem_u32(&ctrl.k_full[s]), lane);
-        ++kc;
-      }
+      ok = stream_item<GATHER, PERM>(rq, bh, begin, n, layout, ns, &rq.tk, rq.kg, base + OFF_K,
+                                     ctrl.k_full, ctrl.k_empty, kc, 2, lane, wait);
     }
     cp_async_wait_all();
     if (*abort_flag) {
       // let issued copies land before the CTA exits (the last slots of the ring)
       volatile int32_t dummy = 0;
-      for (uint32_t k = (kc > KS ? kc - KS : 0); k < kc; ++k)
-        mbar_wait(smem_u32(&ctrl.k_full[k % KS]), (k / KS) & 1, &dummy, p.err);
+      for (int s = 0; s < KS; ++s)
+        if (kc[s]) mbar_wait(smem_u32(&ctrl.k_full[s]), (kc[s] - 1) & 1, &dummy, p.err);
       if (qc) mbar_wait(smem_u32(&ctrl.q_full), (qc - 1) & 1, &dummy, p.err);
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------- V producer
-    uint32_t vc = 0, seq = 0;
+    uint32_t vc[2] = {0u, 0u}, seq = 0;
     bool ok = true;
     while (ok) {
       const int slot = seq & 1;
@@ -379,25 +454,25 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
       const int4 i1 = __ldg(&rq.items[2 * li + 1]);
       const int32_t bh = i0.x, begin = i0.z, n = i0.w - i0.z, layout = i1.x;
       const int32_t ns = (n + 1) >> 1;
-      for (int32_t j2 = 0; j2 < ns && ok; ++j2) {
-        const int s = vc % VS;
-        if (!wait(smem_u32(&ctrl.v_empty[s]), ((vc / VS) & 1) ^ 1, 3)) { ok = false; break; }
-        load_kv_step<GATHER, PERM>(rq, bh, begin, n, layout, j2, &rq.tv, rq.vg,
-                                   base + OFF_V + s * KV_BYTES, smem_u32(&ctrl.v_full[s]), lane);
-        ++vc;
-      }
+      ok = stream_item<GATHER, PERM>(rq, bh, begin, n, layout, ns, &rq.tv, rq.vg, base + OFF_V,
+                                     ctrl.v_full, ctrl.v_empty, vc, 3, lane, wait);
     }
     cp_async_wait_all();
     if (*abort_flag) {
       volatile int32_t dummy = 0;
-      for (uint32_t k = (vc > VS ? vc - VS : 0); k < vc; ++k)
-        mbar_wait(smem_u32(&ctrl.v_full[k % VS]), (k / VS) & 1, &dummy, p.err);
+      for (int s = 0; s < VS; ++s)
+        if (vc[s]) mbar_wait(smem_u32(&ctrl.v_full[s]), (vc[s] - 1) & 1, &dummy, p.err);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 11) {
+    // ------------------------------------------------ MMA issuers, one per group
+    // Issuer g takes its group's steps of the item (item steps j = g, g + 2, ...;
+    // group step t is item step 2 t + g) in the order QK(t), PV(t - 1): the PV of
+    // group step t - 2 is issued before QK(t) reuses that step's S^T buffer.
+    // Two issuing threads keep the tensor pipe fed while either one waits.
     if (lane == 0) {
-      uint32_t kc = 0, vc = 0, qc = 0, seq = 0, oc = 0;
-      uint32_t gq[2] = {0u, 0u}, gp[2] = {0u, 0u};   // QKs / PVs issued per group
+      const int g = warp == 1 ? 0 : 1;
+      uint32_t kc = 0, vc = 0, qc = 0, seq = 0, oc = 0;   // this group's K / V slot loads, items
+      uint32_t gq = 0, gp = 0;                            // QKs / PVs issued for the group
       int64_t tiles = 0;
       bool ok = true;
       if (p.test_stall) ok = wait(smem_u32(&ctrl.never), 0, 4);
@@ -413,22 +488,31 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
         const int4 i0 = __ldg(&rq.items[2 * li]);
         const int4 i1 = __ldg(&rq.items[2 * li + 1]);
         const int32_t n = i0.w - i0.z, ns = (n + 1) >> 1;
-        tiles += n;
+        if (g == 0) tiles += n;
         if (ns == 0) continue;
         const bool gath = GATHER || (PERM && i1.x != 0);
+        const int32_t nt = (ns - g + 1) >> 1;             // this group's steps in the item
         if (!wait(smem_u32(&ctrl.q_full), qc & 1, 6)) break;
         ++qc;
+        if (nt == 0) {
+          // a one-step item leaves group 1 without work: it releases the query
+          // tile and takes the item's O^T phases without MMAs
+          mbar_arrive(smem_u32(&ctrl.q_empty));
+          if (!wait(smem_u32(&ctrl.o_empty), (oc & 1) ^ 1, 10)) break;
+          ++oc;
+          mbar_arrive(smem_u32(&ctrl.o_full));
+          continue;
+        }
         if (gath) fence_proxy_async_smem();
-        for (int32_t i = 0; i < ns + LAG && ok; ++i) {
-          if (i < ns) {
-            // S^T = K Q^T for step i (group i & 1)
-            const int g = i & 1, s = kc % KS;
-            if (!wait(smem_u32(&ctrl.k_full[s]), (kc / KS) & 1, 7)) { ok = false; break; }
+        for (int32_t t = 0; t <= nt && ok; ++t) {
+          if (t < nt) {
+            // S^T = K Q^T for group step t (K slot g)
+            if (!wait(smem_u32(&ctrl.k_full[g]), kc & 1, 7)) { ok = false; break; }
             ++kc;
             if (gath) fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t sK = base + OFF_K + s * KV_BYTES;
-            const uint32_t sb = gq[g] & 1;
+            const uint32_t sK = base + OFF_K + g * KV_BYTES;
+            const uint32_t sb = gq & 1;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t a = sdesc_sw128(sK + (kk >> 2) * (2 * KT * 128) + (kk & 3) * 32, 16, 1024);
@@ -436,44 +520,43 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
               mma_bf16_ss(tmem + g * TM_GROUP + sb * QB, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&ctrl.s_full[g][sb]));
-            mma_commit(smem_u32(&ctrl.k_empty[s]));
-            if (i == ns - 1) mma_commit(smem_u32(&ctrl.q_empty));
-            ++gq[g];
+            mma_commit(smem_u32(&ctrl.k_empty[g]));
+            if (t == nt - 1) mma_commit(smem_u32(&ctrl.q_empty));
+            ++gq;
           }
-          if (i >= LAG) {
-            // O^T += V^T P^T for step j = i - LAG (group j & 1)
-            const int32_t j = i - LAG;
-            const int g = j & 1, s = vc % VS;
-            const uint32_t pb = gp[g] & 1;                 // the group's P^T buffer of this step
-            if (!wait(smem_u32(&ctrl.p_full[g][pb]), (gp[g] >> 1) & 1, 8)) { ok = false; break; }
-            if (!wait(smem_u32(&ctrl.v_full[s]), (vc / VS) & 1, 9)) { ok = false; break; }
+          if (t >= 1) {
+            // O^T += V^T P^T for group step t - 1 (V slot g)
+            const int32_t tt = t - 1;
+            const uint32_t pb = gp & 1;                   // the group's P^T buffer of this step
+            if (!wait(smem_u32(&ctrl.p_full[g][pb]), (gp >> 1) & 1, 8)) { ok = false; break; }
+            if (!wait(smem_u32(&ctrl.v_full[g]), vc & 1, 9)) { ok = false; break; }
             ++vc;
             if (gath) fence_proxy_async_smem();
-            if (j == 0) {
+            if (tt == 0) {
               // the previous item's epilogue has read both groups' O^T
               if (!wait(smem_u32(&ctrl.o_empty), (oc & 1) ^ 1, 10)) { ok = false; break; }
               ++oc;
             }
             tc_fence_after();
-            const uint32_t sV = base + OFF_V + s * KV_BYTES;
+            const uint32_t sV = base + OFF_V + g * KV_BYTES;
             const uint32_t sP = base + OFF_P + (2 * g + pb) * P_BYTES;
 #pragma unroll
             for (int kk = 0; kk < (2 * KT) / 16; ++kk) {
               const uint64_t a = sdesc_sw128(sV + kk * 16 * 128, 2 * KT * 128, 1024);
               const uint64_t b = sdesc_sw128(sP + kk * 16 * 128, 2 * KT * 128, 1024);
-              mma_bf16_ss(tmem + g * TM_GROUP + TM_O, a, b, IDESC_PV, (j >= 2 || kk > 0) ? 1u : 0u);
+              mma_bf16_ss(tmem + g * TM_GROUP + TM_O, a, b, IDESC_PV, (tt > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(smem_u32(&ctrl.v_empty[s]));
+            mma_commit(smem_u32(&ctrl.v_empty[g]));
             mma_commit(smem_u32(&ctrl.pv_done[g][pb]));
-            if (j == ns - 1) mma_commit(smem_u32(&ctrl.o_full));
-            ++gp[g];
+            if (tt == nt - 1) mma_commit(smem_u32(&ctrl.o_full));
+            ++gp;
           }
         }
       }
-      if (p.tiles_done) atomicAdd(p.tiles_done, static_cast<unsigned long long>(tiles));
-      mma_commit(smem_u32(&ctrl.final_bar));
+      if (p.tiles_done && tiles) atomicAdd(p.tiles_done, static_cast<unsigned long long>(tiles));
+      mma_commit(smem_u32(&ctrl.final_bar[g]));
       volatile int32_t dummy = 0;
-      mbar_wait(smem_u32(&ctrl.final_bar), 0, &dummy, p.err);
+      mbar_wait(smem_u32(&ctrl.final_bar[g]), 0, &dummy, p.err);
     }
     __syncwarp();
   } else {
