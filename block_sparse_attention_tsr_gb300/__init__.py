@@ -85,7 +85,7 @@ class _Stats(ctypes.Structure):
 
 class _Regime(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("id", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("id", ctypes.c_int32), ("orient", ctypes.c_int32)]
 
 
 _LIB = None
@@ -382,7 +382,8 @@ def tsr_regime_load(path: Optional[str]) -> None:
 def tsr_regime_lookup(kind: int, bq: int, bk: int, N: int, density: float) -> dict:
     r = _Regime()
     _check(lib().tsr_regime_lookup(kind, bq, bk, N, density, ctypes.byref(r)))
-    return {"bn": r.bn, "stages": r.stages, "ctas_per_sm": r.ctas_per_sm, "id": r.id}
+    return {"bn": r.bn, "stages": r.stages, "ctas_per_sm": r.ctas_per_sm, "id": r.id,
+            "orient": r.orient}
 
 
 def tsr_abi_version() -> int:

@@ -50,7 +50,9 @@ int num_sms(int device) {
 // ----------------------------------------------------------- regime table
 //
 // One row per line: kind bq bk n_min n_max dens_min dens_max d  bn stages ctas
-// ("*" = any).  The first matching row wins.  The rows shipped with the
+// [orient] ("*" = any; a row without the orientation field, or with "*" there,
+// names 128-row tiles).  The first matching row wins.  A key-major row
+// (orient 2) names the one key-major kernel: d = 128, bn 64, stages 2, ctas 1.  The rows shipped with the
 // library come from timing every kernel variant on this GPU over synthetic
 // masks of each class (the table file next to the library); the built-in rows
 // below are the fallback when no file is loaded.
@@ -60,7 +62,7 @@ struct RegimeRow {
   int kind, bq, bk;
   int64_t n_min, n_max;
   double d_min, d_max;
-  int d, bn, stages, ctas;
+  int d, bn, stages, ctas, orient;
 };
 
 const char* kBuiltinTable =
@@ -105,33 +107,43 @@ bool parse_table(const std::string& text, std::vector<RegimeRow>* out, std::stri
     std::string tok;
     while (ls >> tok) f.push_back(tok);
     if (f.empty()) continue;
-    if (f.size() != 11) {
-      *why = "line " + std::to_string(lineno) + ": expected 11 fields";
+    if (f.size() != 11 && f.size() != 12) {
+      *why = "line " + std::to_string(lineno) + ": expected 11 or 12 fields";
       return false;
     }
-    int64_t kind, bq, bk, nmin, nmax, d, bn, st, ct;
+    int64_t kind, bq, bk, nmin, nmax, d, bn, st, ct, orient = TSR_ORIENT_ROWS;
     double dmin, dmax;
     if (!parse_field_i(f[0], &kind) || !parse_field_i(f[1], &bq) || !parse_field_i(f[2], &bk) ||
         !parse_field_i(f[3], &nmin) || !parse_field_i(f[4], &nmax) ||
         !parse_field_d(f[5], &dmin) || !parse_field_d(f[6], &dmax) || !parse_field_i(f[7], &d) ||
         !parse_field_i(f[8], &bn) || !parse_field_i(f[9], &st) || !parse_field_i(f[10], &ct) ||
-        bn < 0 || st < 0 || ct < 0) {
+        bn < 0 || st < 0 || ct < 0 || (f.size() == 12 && !parse_field_i(f[11], &orient))) {
       *why = "line " + std::to_string(lineno) + ": bad field";
+      return false;
+    }
+    if (orient < 0) orient = TSR_ORIENT_ROWS;
+    if (orient != TSR_ORIENT_ROWS && orient != TSR_ORIENT_KEYS) {
+      *why = "line " + std::to_string(lineno) + ": orientation must be 1 or 2";
       return false;
     }
     rows.push_back(RegimeRow{static_cast<int>(kind), static_cast<int>(bq), static_cast<int>(bk),
                              nmin, nmax, dmin, dmax, static_cast<int>(d), static_cast<int>(bn),
-                             static_cast<int>(st), static_cast<int>(ct)});
+                             static_cast<int>(st), static_cast<int>(ct), static_cast<int>(orient)});
   }
   *out = rows;
   return true;
 }
 
 bool rows_valid(const std::vector<RegimeRow>& rows) {
-  for (const RegimeRow& r : rows)
+  for (const RegimeRow& r : rows) {
+    if (r.orient == TSR_ORIENT_KEYS) {
+      if (r.d != 128 || r.bn != 64 || r.stages != 2 || r.ctas != 1) return false;
+      continue;
+    }
     if ((r.bn != 64 && r.bn != 128) || (r.d != 64 && r.d != 128) ||
         !variant_exists(r.d, r.bn, r.stages, r.ctas, r.kind == TSR_MASK_KEYLIST))
       return false;
+  }
   return true;
 }
 
@@ -169,9 +181,9 @@ Regime regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N, double den
     if (r.d_min >= 0 && density < r.d_min) continue;
     if (r.d_max >= 0 && density >= r.d_max) continue;
     if (r.d >= 0 && r.d != d) continue;
-    return Regime{r.bn, r.stages, r.ctas, static_cast<int32_t>(i)};
+    return Regime{r.bn, r.stages, r.ctas, static_cast<int32_t>(i), r.orient};
   }
-  return Regime{128, d == 64 ? 4 : 3, 1, -1};
+  return Regime{128, d == 64 ? 4 : 3, 1, -1, TSR_ORIENT_ROWS};
 }
 
 }  // namespace tsr
@@ -973,6 +985,7 @@ tsr_status tsr_regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N, do
   out->stages = r.stages;
   out->ctas_per_sm = r.ctas;
   out->id = r.id;
+  out->orient = r.orient;
   return TSR_OK;
 }
 

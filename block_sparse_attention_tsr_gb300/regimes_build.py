@@ -4,9 +4,10 @@ profiling).
 
 For every mask class -- logical block shape, density bucket, sequence-length
 bucket, head dimension -- a few seeded synthetic masks of that class are planned
-and run with every kernel variant (tile width, pipeline depth, CTAs per SM); the
-fastest variant (median over the masks of plan + forward time) becomes the row
-of that class.  Run on the target GPU:
+and run with every kernel variant (tile orientation: 128-row query tiles or
+key-major 64-query tiles; for 128-row tiles the tile width, pipeline depth and
+CTAs per SM); the fastest variant (median over the masks of plan + forward
+time) becomes the row of that class.  Run on the target GPU:
 
     python -m block_sparse_attention_tsr_gb300.regimes_build [--out PATH] [--quick]
 
@@ -33,13 +34,18 @@ import workloads as W  # noqa: E402
 SHAPES = ((32, 32), (64, 64), (128, 128), (64, 256), (256, 64))
 DENSITY_EDGES = (0.0, 0.15, 0.30, 0.45, 0.60, 1.01)
 N_BUCKETS = ((0, 8191, 4096), (8192, 1 << 24, 32760))   # (n_min, n_max, N used to profile)
-VARIANTS = {128: ((128, 3, 1), (128, 2, 1), (64, 4, 1), (64, 2, 2)),
-            64: ((128, 4, 1), (64, 4, 1), (64, 3, 2))}
+# (bn, stages, ctas per SM, orientation): 1 = 128-row query tiles, 2 = the
+# key-major kernel (d = 128 only; its ring shape is fixed)
+ROWS, KEYS = 1, 2
+VARIANTS = {128: ((128, 3, 1, ROWS), (128, 2, 1, ROWS), (64, 4, 1, ROWS), (64, 2, 2, ROWS),
+                  (64, 2, 1, KEYS)),
+            64: ((128, 4, 1, ROWS), (64, 4, 1, ROWS), (64, 3, 2, ROWS))}
 # key-list (M x 1 slice) masks: classes by slice height and listed-key fraction;
 # the gathered kernel variants
 KEYLIST_M = (64, 128)
 KEYLIST_EDGES = (0.0, 0.10, 0.20, 0.35, 0.60, 1.01)
-VARIANTS_GATHERED = {128: ((128, 3, 1), (64, 2, 2)), 64: ((128, 4, 1), (64, 3, 2))}
+VARIANTS_GATHERED = {128: ((128, 3, 1, ROWS), (64, 2, 2, ROWS), (64, 2, 1, KEYS)),
+                     64: ((128, 4, 1, ROWS), (64, 3, 2, ROWS))}
 
 
 def keylist_spec(N, M, frac, heads, seed):
@@ -53,8 +59,8 @@ def keylist_spec(N, M, frac, heads, seed):
 
 
 def time_variant(mask, q, k, v, out, lse, variant, reps):
-    bn, stages, ctas = variant
-    plan = tsr.tsr_plan(mask, {"bn": bn, "stages": stages, "ctas_per_sm": ctas})
+    bn, stages, ctas, orient = variant
+    plan = tsr.tsr_plan(mask, {"bn": bn, "stages": stages, "ctas_per_sm": ctas, "orient": orient})
     stream = torch.cuda.current_stream()
     for _ in range(2):
         plan.update(mask)
@@ -139,14 +145,14 @@ def main():
             print(f"d={d} N={F * S} svg -> {best}  " +
                   " ".join(f"{vv}:{t:.3f}ms" for vv, t in med.items()), flush=True)
     # anything else: one default row per head dimension
-    rows.append(("*", "*", "*", "*", "*", "*", "*", 128, 64, 2, 2))
-    rows.append(("*", "*", "*", "*", "*", "*", "*", 64, 64, 3, 2))
+    rows.append(("*", "*", "*", "*", "*", "*", "*", 128, 64, 2, 2, ROWS))
+    rows.append(("*", "*", "*", "*", "*", "*", "*", 64, 64, 3, 2, ROWS))
     with open(args.out, "w") as f:
         f.write("# Regime table for GB300 (sm_103a), written by regimes_build.py\n")
         f.write(f"# {time.strftime('%Y-%m-%d')}: {args.masks} seeded masks per class (banded-plus-"
                 f"random blocks; clustered key lists, one head's repeated; SVG routing), "
                 f"{args.heads} heads, median of plan + forward time\n")
-        f.write("# kind bq bk n_min n_max dens_min dens_max d bn stages ctas\n")
+        f.write("# kind bq bk n_min n_max dens_min dens_max d bn stages ctas orient\n")
         for r in rows:
             f.write(" ".join(f"{x:.2f}" if isinstance(x, float) else str(x) for x in r) + "\n")
     print(f"wrote {len(rows)} rows to {args.out} in {time.time() - t0:.0f} s")

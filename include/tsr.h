@@ -426,14 +426,20 @@ tsr_status tsr_attention_noalloc(const tsr_mask *mask, const void *q, const void
 
 /*
  * Regime table (profile-guided regime selection, Tessera abstract).
- * tsr_regime_load reads a table file (text, one regime per line; see the file
- * shipped next to the library); NULL reloads the built-in default.
- * tsr_regime_lookup returns the regime chosen for a mask class.
+ * tsr_regime_load reads a table file (text, one regime per line: kind bq bk
+ * n_min n_max dens_min dens_max d bn stages ctas [orient], "*" = any; see the
+ * file shipped next to the library); NULL reloads the built-in default.  A row
+ * without the orient field names 128-row tiles (TSR_ORIENT_ROWS); a key-major
+ * row (TSR_ORIENT_KEYS) must read d = 128, bn 64, stages 2, ctas 1, the one
+ * key-major kernel.  A table naming a kernel variant that does not exist is
+ * refused (TSR_ERR_INVALID_ARG) and the loaded table is kept.
+ * tsr_regime_lookup returns the regime chosen for a mask class (d = 128).
  */
 tsr_status tsr_regime_load(const char *path /* HOST, NULL = built-in */);
 
 typedef struct {
   int32_t bn, stages, ctas_per_sm, id;
+  int32_t orient;               /* TSR_ORIENT_ROWS or TSR_ORIENT_KEYS */
 } tsr_regime;
 
 tsr_status tsr_regime_lookup(int32_t kind, int32_t bq, int32_t bk, int32_t N,

@@ -76,9 +76,28 @@ def test_regime_table_parsing(L, tmp_path):
     tsr.tsr_regime_load(str(good))
     r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.2)
     assert (r["bn"], r["stages"], r["ctas_per_sm"], r["id"]) == (64, 4, 1, 0)
+    assert r["orient"] == tsr.ORIENT_ROWS
     r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.7)
     assert (r["bn"], r["id"]) == (128, 1)
+    # orientation column: key-major rows, and "*" / absent meaning 128-row tiles
+    good.write_text("0 64 64 * * 0 0.5 128 64 2 1 2\n0 64 64 * * 0.5 1.01 128 64 4 1 *\n"
+                    "* * * * * * * 128 128 3 1 1\n")
+    tsr.tsr_regime_load(str(good))
+    r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.2)
+    assert (r["bn"], r["stages"], r["ctas_per_sm"], r["id"], r["orient"]) == (64, 2, 1, 0, tsr.ORIENT_KEYS)
+    r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.7)
+    assert (r["bn"], r["stages"], r["id"], r["orient"]) == (64, 4, 1, tsr.ORIENT_ROWS)
+    r = tsr.tsr_regime_lookup(0, 32, 32, 32760, 0.7)
+    assert (r["bn"], r["id"], r["orient"]) == (128, 2, tsr.ORIENT_ROWS)
     bad = tmp_path / "bad.txt"
+    for row in ("* * * * * * * 128 128 3 1 2",            # key-major rows name the one kernel
+                "* * * * * * * 64 64 2 1 2",              # key-major tiles need d = 128
+                "* * * * * * * 128 64 2 1 3"):            # no such orientation
+        bad.write_text(row + "\n")
+        with pytest.raises(tsr.TsrError):
+            tsr.tsr_regime_load(str(bad))
+    r = tsr.tsr_regime_lookup(0, 64, 64, 32760, 0.2)       # a refused table leaves the last one
+    assert r["orient"] == tsr.ORIENT_KEYS
     bad.write_text("* * * * * * * 128 96 3 1\n")            # no such kernel variant
     with pytest.raises(tsr.TsrError):
         tsr.tsr_regime_load(str(bad))

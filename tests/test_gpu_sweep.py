@@ -45,7 +45,8 @@ def sampled_rows(m: int):
 
 
 def regime_opts(st):
-    return {"bn": st["bn"], "stages": st["stages"], "ctas_per_sm": st["ctas_per_sm"]}
+    return {"bn": st["bn"], "stages": st["stages"], "ctas_per_sm": st["ctas_per_sm"],
+            "orient": st["orient"]}
 
 
 @pytest.mark.parametrize("chunk", range(8))
