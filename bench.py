@@ -132,17 +132,24 @@ def read_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the attention kernels' sources (both tile orientations)."""
     h = hashlib.sha256()
-    for f in ("fwd_kernel.cuh", "ptx.cuh"):
+    for f in ("fwd_kernel.cuh", "fwd_t_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel_hash: str):
+def attention_kernel(stats) -> str:
+    """The attention kernel a plan launches: key-major plans run the
+    transposed-tile kernel."""
+    return "bsa_fwd_t_kernel" if stats and stats.get("orient") == 2 else "bsa_fwd_kernel"
+
+
+def read_traffic(kernel: str, kernel_hash: str):
     """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "bsa_fwd_kernel_video480p.json")
+    summary of the 480p workload, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_video480p.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -629,7 +636,8 @@ def main():
     peak = peaks["bf16_sustained"] if long_region else peaks["bf16"]
     achieved = flops / (fwd_avg * 1e-3) / 1e12 if fwd_avg > 0 else 0.0
     khash = kernel_source_hash()
-    traffic = read_traffic(khash)
+    kname = attention_kernel(stats)
+    traffic = read_traffic(kname, khash) if args.workload == "video480p" and args.heads == 24 else None
 
     e2e = None
     if not args.no_e2e and hi > lo:
@@ -726,7 +734,7 @@ def main():
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peaks['src']} bf16 "
                                         f"{'sustained' if long_region else 'burst'}",
-                         "kernel": "bsa_fwd_kernel", "kernel_source_hash": khash},
+                         "kernel": kname, "kernel_source_hash": khash},
             "clocks": clk.summary(*window),
             "gpu_launches": args.steps * launches_per_step(spec, stats or {}),
             "e2e": e2e,
