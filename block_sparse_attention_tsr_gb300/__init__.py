@@ -70,7 +70,7 @@ class _Request(ctypes.Structure):
 class _Opts(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("orient", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("orient", ctypes.c_int32), ("kv_split", ctypes.c_int32)]
 
 
 class _Stats(ctypes.Structure):
@@ -80,7 +80,8 @@ class _Stats(ctypes.Structure):
                 ("n_entries", ctypes.c_int64), ("n_boundary", ctypes.c_int64),
                 ("n_logical_on", ctypes.c_int64), ("n_logical_total", ctypes.c_int64),
                 ("max_item_len", ctypes.c_int64), ("regime_id", ctypes.c_int32),
-                ("orient", ctypes.c_int32)]
+                ("orient", ctypes.c_int32), ("kv_split", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class _Regime(ctypes.Structure):
@@ -235,7 +236,7 @@ class Plan:
 def _opts(opts) -> Optional[_Opts]:
     if opts is None:
         return None
-    unknown = set(opts) - {"bn", "stages", "ctas_per_sm", "flags", "orient"}
+    unknown = set(opts) - {"bn", "stages", "ctas_per_sm", "flags", "orient", "kv_split"}
     if unknown:
         raise ValueError(f"unknown plan option(s): {sorted(unknown)}")
     o = _Opts()
@@ -244,6 +245,7 @@ def _opts(opts) -> Optional[_Opts]:
     o.ctas_per_sm = int(opts.get("ctas_per_sm", 0))
     o.flags = int(opts.get("flags", 0))
     o.orient = int(opts.get("orient", 0))
+    o.kv_split = int(opts.get("kv_split", 0))
     return o
 
 

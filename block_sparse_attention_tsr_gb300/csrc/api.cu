@@ -240,7 +240,8 @@ tsr_status check_bounds(const int32_t* dev, int32_t n, int32_t N, cudaStream_t s
 void free_plan(tsr_plan_s* P) {
   if (!P) return;
   for (DevBuf* b : {&P->b_items, &P->b_entries, &P->b_descs, &P->b_cnt, &P->b_tot, &P->b_ebegin,
-                    &P->b_dbegin, &P->b_hist, &P->b_gidx})
+                    &P->b_dbegin, &P->b_hist, &P->b_gidx, &P->b_units, &P->b_part_o, &P->b_part_lse,
+                    &P->b_part_cnt})
     devbuf_free(*b);
   cudaFree(P->counter);
   cudaFree(P->err);
@@ -280,6 +281,7 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
   } else if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) {
     return s;
   }
+  if (tsr_status s = plan_split(P, P->has_opts ? &P->opts : nullptr, st)) return s;
   if (P->flags & TSR_PLAN_DEBUG_CHECKS) {
     if (tsr_status s = plan_check(P, st)) return s;
     uint32_t e = 0;
@@ -317,9 +319,9 @@ struct HostCache {
   size_t stage_cap = 0;
   std::vector<cudaEvent_t> ev;                 // 3 per head group: inputs, plan, attention
   std::vector<tsr_plan_t> plans;               // one per head group
-  std::vector<std::array<int64_t, 10>> plan_key;
+  std::vector<std::array<int64_t, 11>> plan_key;
   tsr_plan_t full_plan = nullptr;              // one plan over every head (one-plan mode)
-  std::array<int64_t, 11> full_key{};
+  std::array<int64_t, 12> full_key{};
   int32_t* counters = nullptr;                 // one work counter per head group (one-plan mode)
   size_t counters_cap = 0;
   int device = -1;
@@ -379,8 +381,10 @@ tsr_status plan_new(const tsr_mask* mask, const tsr_plan_opts* opts, int32_t gro
   if (tsr_status s = check_mask(mask)) return s;
   if (opts && opts->bn && opts->bn != 64 && opts->bn != 128)
     return fail(TSR_ERR_INVALID_ARG, "opts->bn must be 0, 64 or 128");
-  if (opts && (opts->orient < 0 || opts->orient > TSR_ORIENT_KEYS || opts->reserved != 0))
-    return fail(TSR_ERR_INVALID_ARG, "opts->orient must be 0, 1 or 2 and opts->reserved 0");
+  if (opts && (opts->orient < 0 || opts->orient > TSR_ORIENT_KEYS))
+    return fail(TSR_ERR_INVALID_ARG, "opts->orient must be 0, 1 or 2");
+  if (opts && opts->kv_split != 0 && opts->kv_split != 1 && opts->kv_split != 2 && opts->kv_split != 4)
+    return fail(TSR_ERR_INVALID_ARG, "opts->kv_split must be 0, 1, 2 or 4");
   tsr_plan_s* P = new (std::nothrow) tsr_plan_s();
   if (!P) return fail(TSR_ERR_OOM, "host allocation failed");
   struct Guard {
@@ -545,6 +549,7 @@ tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   s->max_item_len = plan->max_item_len;
   s->regime_id = plan->regime_id;
   s->orient = plan->orient;
+  s->kv_split = plan->kv_split;
   return TSR_OK;
 }
 
@@ -802,8 +807,12 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     // queued behind the next group's inputs.)  Consecutive groups alternate
     // between two attention streams, so one persistent launch's last CTAs
     // overlap the next one's first.
-    const tsr_plan_opts zero{};
-    const tsr_plan_opts& o = opts ? *opts : zero;
+    // The head-group launches overlap one another (two attention streams), so
+    // a launch's tail is covered by the next one: no automatic split-KV here
+    // (an explicit opts->kv_split is honoured).
+    tsr_plan_opts host_opts = opts ? *opts : tsr_plan_opts{};
+    if (host_opts.kv_split == 0) host_opts.kv_split = 1;
+    const tsr_plan_opts& o = host_opts;
     if (static_cast<int64_t>(hc.plans.size()) != G) {
       for (tsr_plan_t pl : hc.plans) tsr_plan_destroy(pl);
       hc.plans.assign(G, nullptr);
@@ -820,8 +829,8 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       tsr_mask& vw = views[g];
       vw.B = 1;
       vw.H = static_cast<int32_t>(gs[g + 1] - gs[g]);
-      const std::array<int64_t, 10> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
-                                            o.flags, o.orient, opts ? 1 : 0};
+      const std::array<int64_t, 11> key = {vw.kind, vw.H, vw.N, vw.d, o.bn, o.stages, o.ctas_per_sm,
+                                            o.flags, o.orient, o.kv_split, opts ? 1 : 0};
       if (mask->kind == TSR_MASK_KEYLIST) TSR_CUDA(cudaStreamWaitEvent(sp, hc.ev[3 * G + g], 0));
       tsr_status st;
       if (hc.plans[g] && hc.plan_key[g] == key) {
@@ -829,7 +838,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       } else {
         if (hc.plans[g]) tsr_plan_destroy(hc.plans[g]);
         hc.plans[g] = nullptr;
-        st = tsr_plan(&vw, opts, &hc.plans[g], sp);
+        st = tsr_plan(&vw, &host_opts, &hc.plans[g], sp);
         hc.plan_key[g] = key;
       }
       if (st != TSR_OK) return st;
@@ -875,14 +884,14 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       tsr_mask full = views[0];                  // device arrays from their start
       full.B = mask->B;
       full.H = mask->H;
-      const std::array<int64_t, 11> key = {full.kind, full.B, full.H, full.N, full.d, o.bn,
-                                            o.stages, o.ctas_per_sm, o.flags, o.orient, opts ? 1 : 0};
+      const std::array<int64_t, 12> key = {full.kind, full.B, full.H, full.N, full.d, o.bn, o.stages,
+                                            o.ctas_per_sm, o.flags, o.orient, o.kv_split, opts ? 1 : 0};
       if (hc.full_plan && hc.full_key == key) {
         s = tsr_plan_update(hc.full_plan, &full, sp);
       } else {
         if (hc.full_plan) tsr_plan_destroy(hc.full_plan);
         hc.full_plan = nullptr;
-        s = plan_new(&full, opts, 1, sp, &hc.full_plan);
+        s = plan_new(&full, &host_opts, 1, sp, &hc.full_plan);
         hc.full_key = key;
       }
       if (s == TSR_OK && hc.counters_cap < static_cast<size_t>(G)) {

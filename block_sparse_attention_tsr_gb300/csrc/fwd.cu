@@ -121,9 +121,19 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
                       encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, krows);
       if (!ok)
         return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
-      const int64_t lo = a.item_lo, hi = a.item_hi < 0 ? P->n_items : a.item_hi;
-      if (lo < 0 || hi > P->n_items || lo > hi) return fail(TSR_ERR_INTERNAL, "bad item range");
-      q.items = static_cast<const int4*>(P->items) + 2 * lo;
+      // the range is in work items; a split plan launches their units
+      const int64_t ilo = a.item_lo, ihi = a.item_hi < 0 ? P->n_items : a.item_hi;
+      if (ilo < 0 || ihi > P->n_items || ilo > ihi) return fail(TSR_ERR_INTERNAL, "bad item range");
+      const bool split = P->kv_split > 1;
+      const int64_t lo = ilo * P->kv_split, hi = ihi * P->kv_split;
+      q.items = static_cast<const int4*>(split ? P->units : P->items) + 2 * lo;
+      if (split) {
+        q.part_o = static_cast<float*>(P->b_part_o.p);
+        q.part_lse = static_cast<float*>(P->b_part_lse.p);
+        q.part_cnt = static_cast<int32_t*>(P->b_part_cnt.p);
+        if (ihi > ilo)
+          TSR_CUDA(cudaMemsetAsync(q.part_cnt + ilo, 0, sizeof(int32_t) * (ihi - ilo), stream));
+      }
       q.entries = static_cast<const int2*>(P->entries);
       q.descs = static_cast<const uint4*>(P->descs);
       q.out = static_cast<__nv_bfloat16*>(a.out);

@@ -68,6 +68,11 @@ struct ReqParams {
   const __nv_bfloat16* kg;
   const __nv_bfloat16* vg;
   const int32_t* gidx;
+  // split-KV plans: each unit's partial O (fp32 [bm][d]) and lse (base 2, [bm])
+  // by unit index, one arrival counter per work item (zeroed before the launch)
+  float* part_o;
+  float* part_lse;
+  int32_t* part_cnt;
   int32_t item_begin, N, F, S, slice_m;
 };
 
@@ -114,7 +119,9 @@ struct alignas(8) Ctrl {
   uint64_t pv_done, o_full, o_empty;
   uint64_t item_full[2], item_empty[2];
   uint64_t final_bar, never;
+  uint64_t split_bar;          // split-KV epilogue: the four softmax warps
   int32_t item_slot[2];
+  int32_t split_last;          // this CTA's unit was the last part of its item
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     mbar_init(smem_u32(&ctrl.pv_done), 1);
     mbar_init(smem_u32(&ctrl.o_full), 1);
     mbar_init(smem_u32(&ctrl.o_empty), 4);
+    mbar_init(smem_u32(&ctrl.split_bar), 4);
     mbar_init(smem_u32(&ctrl.final_bar), 1);
     mbar_init(smem_u32(&ctrl.never), 1);
     ctrl.abort_flag = 0;
@@ -519,7 +527,7 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                    // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t item_seq = 0, t_cnt = 0, o_seq = 0;
+    uint32_t item_seq = 0, t_cnt = 0, o_seq = 0, split_seq = 0;
     bool ok = true;
     while (ok) {
       const int slot = item_seq & 1;
@@ -745,6 +753,96 @@ __global__ void __launch_bounds__(192, CTAS) bsa_fwd_kernel(const __grid_constan
       const int32_t orow = (PERM && layout) ? unpermute(gr, rq.F, rq.S) : gr;
       const size_t obase = (static_cast<size_t>(bh) * rq.N + (valid ? orow : 0)) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if (i1.z > 1) {
+        // split-KV unit (part i1.w of the i1.z parts of work item i1.y): its
+        // normalised partial row O / l (fp32) and lse (base 2) go to the
+        // plan's workspace; the last part of the item to finish merges them
+        const int64_t unit = static_cast<int64_t>(i1.y) * i1.z + i1.w;
+        // layout [unit][d / 4][row] of float4: a warp's rows are adjacent
+        float4* po = reinterpret_cast<float4*>(rq.part_o + unit * kBM * D) + r;
+        if (n > 0) {
+          if (!mbar_wait(smem_u32(&ctrl.o_full), o_seq & 1, abort_flag, p.err, p.timeout_ns)) break;
+          ++o_seq;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tmem + lane_off + C::O_COL + c0, rr);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              po[(c0 / 4 + i) * kBM] =
+                  make_float4(__uint_as_float(rr[4 * i]) * inv_l, __uint_as_float(rr[4 * i + 1]) * inv_l,
+                              __uint_as_float(rr[4 * i + 2]) * inv_l, __uint_as_float(rr[4 * i + 3]) * inv_l);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl.o_empty));
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) po[i * kBM] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        rq.part_lse[unit * kBM + r] = (l > 0.f) ? m_ref + __log2f(l) : -INFINITY;
+        __threadfence();
+        // every row of the part is written: count the part
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl.split_bar));
+        if (!mbar_wait(smem_u32(&ctrl.split_bar), split_seq & 1, abort_flag, p.err, p.timeout_ns)) break;
+        ++split_seq;
+        if (r == 0) ctrl.split_last = (atomicAdd(rq.part_cnt + i1.y, 1) == i1.z - 1) ? 1 : 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl.split_bar));
+        if (!mbar_wait(smem_u32(&ctrl.split_bar), split_seq & 1, abort_flag, p.err, p.timeout_ns)) break;
+        ++split_seq;
+        if (ctrl.split_last && valid) {
+          __threadfence();
+          const int64_t u0 = static_cast<int64_t>(i1.y) * i1.z;
+          float w[4], M = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            w[q] = (q < i1.z) ? __ldcg(rq.part_lse + (u0 + q) * kBM + r) : -INFINITY;
+            M = fmaxf(M, w[q]);
+          }
+          float L = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            w[q] = (M == -INFINITY) ? 0.f : ex2_approx(w[q] - M);   // ex2(-inf) = 0
+            L += w[q];
+          }
+          const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w[q] *= inv;
+          // every part's two float4 of a chunk are loaded together (parts past
+          // i1.z load nothing and weigh 0), two chunks in flight
+          const float4* src[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            src[q] = reinterpret_cast<const float4*>(rq.part_o + (u0 + (q < i1.z ? q : 0)) * kBM * D) + r;
+          uint4* dst = reinterpret_cast<uint4*>(rq.out + obase);
+#pragma unroll 2
+          for (int c = 0; c < D / 8; ++c) {
+            float4 x[4][2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool on = q < i1.z;
+              x[q][0] = on ? __ldcg(src[q] + (2 * c) * kBM) : make_float4(0.f, 0.f, 0.f, 0.f);
+              x[q][1] = on ? __ldcg(src[q] + (2 * c + 1) * kBM) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[0] += w[q] * x[q][0].x; acc[1] += w[q] * x[q][0].y;
+              acc[2] += w[q] * x[q][0].z; acc[3] += w[q] * x[q][0].w;
+              acc[4] += w[q] * x[q][1].x; acc[5] += w[q] * x[q][1].y;
+              acc[6] += w[q] * x[q][1].z; acc[7] += w[q] * x[q][1].w;
+            }
+            dst[c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+          }
+          rq.lse[static_cast<size_t>(bh) * rq.N + orow] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        }
+        continue;
+      }
       if (n > 0) {
         // o_full completes once per non-empty item, after its last PV; the next
         // item's first PV waits for o_empty, so the phases cannot run ahead.

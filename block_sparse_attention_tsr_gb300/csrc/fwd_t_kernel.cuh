@@ -124,6 +124,7 @@ struct alignas(16) CtrlT {
   float lse2[QB];             // epilogue: lse in base-2 units, or -inf
   uint32_t tmem_base;
   int32_t abort_flag;
+  int32_t split_last;         // split-KV: this CTA's unit was the last part of its item
 };
 
 // The softmax reads 4 reference maxima at a time (16-byte loads).
@@ -877,6 +878,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
       }
       if (!pair_sync()) break;
       if (r < QB) ctrl.mref[g][r] = kMrefInit;          // for the next item
+      // split-KV unit (part i1.w of the i1.z parts of work item i1.y): the
+      // normalised partial O (fp32, [q][d]) and lse (base 2) go to the plan's
+      // workspace instead of the output, and the last part to finish merges
+      const bool split = i1.z > 1;
+      const int64_t unit = split ? static_cast<int64_t>(i1.y) * i1.z + i1.w : 0;
+      float* const part = split ? rq.part_o + unit * QB * D : nullptr;
+      if (split && ns == 0) {
+        for (int q = 32 * g; q < 32 * g + 32; ++q) part[q * D + r] = 0.f;
+      }
       if (ns > 0) {
         // O = fac0 O0 + fac1 O1 for queries [32 g, 32 g + 32), transposed into
         // the staging tile: element (q, d) at row q (256 B), 16-byte unit
@@ -895,8 +905,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
             const int q = c0 + i;
             float o = __uint_as_float(ra[i]) * ctrl.fac[0][q];
             if (ns > 1) o += __uint_as_float(rb[i]) * ctrl.fac[1][q];
-            *reinterpret_cast<__nv_bfloat16*>(stage + q * 256 + (((r >> 3) ^ (q & 7)) << 4) + (r & 7) * 2) =
-                __float2bfloat16_rn(o);
+            if (split)
+              part[q * D + r] = o;
+            else
+              *reinterpret_cast<__nv_bfloat16*>(stage + q * 256 + (((r >> 3) ^ (q & 7)) << 4) + (r & 7) * 2) =
+                  __float2bfloat16_rn(o);
           }
         }
         tc_fence_before();
@@ -904,7 +917,63 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
         if (lane == 0) mbar_arrive(smem_u32(&ctrl.o_empty));
       }
       if (!pair_sync()) break;
-      {
+      if (split) {
+        if (g == 0 && r < QB) rq.part_lse[unit * QB + r] = ctrl.lse2[r];
+        __threadfence();
+        if (!pair_sync()) break;
+        if (g == 0 && r == 0) ctrl.split_last = (atomicAdd(rq.part_cnt + i1.y, 1) == i1.z - 1) ? 1 : 0;
+        if (!pair_sync()) break;
+        if (ctrl.split_last) {
+          // merge the parts: 256 threads, row q, quarter qt (32 d values)
+          __threadfence();
+          const int t8 = g * 128 + r, q = t8 & 63, qt = t8 >> 6;
+          const int32_t tq = q0 + q;
+          if (tq < rq.N) {
+            const int64_t u0 = static_cast<int64_t>(i1.y) * i1.z;
+            float w[4], M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              w[k] = (k < i1.z) ? __ldcg(rq.part_lse + (u0 + k) * QB + q) : -INFINITY;
+              M = fmaxf(M, w[k]);
+            }
+            float L = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              w[k] = (M == -INFINITY) ? 0.f : ex2_approx(w[k] - M);   // ex2(-inf) = 0
+              L += w[k];
+            }
+            const float inv = (L > 0.f) ? __fdividef(1.f, L) : 0.f;
+            const int32_t orow = (PERM && layout) ? unpermute(tq, rq.F, rq.S) : tq;
+            uint4* dst = reinterpret_cast<uint4*>(rq.out + (static_cast<size_t>(bh) * rq.N + orow) * D + qt * 32);
+            // every part's two float4 of a chunk are loaded together (parts past
+            // i1.z load nothing and weigh 0), two chunks in flight
+            const float4* src[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              src[k] = reinterpret_cast<const float4*>(rq.part_o + ((u0 + (k < i1.z ? k : 0)) * QB + q) * D + qt * 32);
+#pragma unroll 2
+            for (int u = 0; u < 4; ++u) {
+              float4 x[4][2];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const bool on = k < i1.z;
+                x[k][0] = on ? __ldcg(src[k] + 2 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[k][1] = on ? __ldcg(src[k] + 2 * u + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+              float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float wk = w[k] * inv;
+                acc[0] += wk * x[k][0].x; acc[1] += wk * x[k][0].y; acc[2] += wk * x[k][0].z; acc[3] += wk * x[k][0].w;
+                acc[4] += wk * x[k][1].x; acc[5] += wk * x[k][1].y; acc[6] += wk * x[k][1].z; acc[7] += wk * x[k][1].w;
+              }
+              dst[u] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            }
+            if (qt == 0) rq.lse[static_cast<size_t>(bh) * rq.N + orow] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+          }
+        }
+      } else {
         // 256 threads store the 64 rows: row q, quarter qt (32 d values, 64 B)
         const int t8 = g * 128 + r, q = t8 & 63, qt = t8 >> 6;
         const int32_t tq = q0 + q;

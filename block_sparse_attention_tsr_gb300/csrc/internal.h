@@ -67,6 +67,10 @@ struct tsr_plan_impl {
   std::vector<int8_t> head_layout;  // host copy: 1 = temporal-major
   int32_t n_temporal = 0;
   int32_t group_heads = 0;    // > 0: heads per longest-first scheduling group (else sized for L2)
+  // split-KV: each work item's tile list cut into kv_split parts (1 = off); the
+  // parts are the launch's work units, written to `units` in item order
+  int32_t kv_split = 1;
+  void* units = nullptr;      // tsr_plan_item [n_items * kv_split] (kv_split > 1)
   // device buffers (owned)
   void* items = nullptr;     // tsr_plan_item [n_items]
   void* entries = nullptr;   // tsr_plan_entry [n_entries]
@@ -77,6 +81,9 @@ struct tsr_plan_impl {
   int8_t* head_kind_dev = nullptr;
   // storage reused when the plan is rebuilt for a new mask (tsr_plan_update)
   DevBuf b_items, b_entries, b_descs, b_cnt, b_tot, b_ebegin, b_dbegin, b_hist, b_gidx;
+  // split-KV storage: units, each unit's partial O (fp32 [bm][d]) and lse (base 2,
+  // [bm]), one arrival counter per work item
+  DevBuf b_units, b_part_o, b_part_lse, b_part_cnt;
   unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
   int8_t* host_kinds = nullptr;             // pinned: SVG head kinds, read after the count sync
   bool has_opts = false;
@@ -104,6 +111,11 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
                             const int32_t* cnt_b, int32_t max_len, int32_t* ebegin,
                             int32_t* dbegin, int32_t* hist, void* items, void* entries,
                             void* descs, cudaStream_t stream);
+
+// split-KV (plan.cu): the number of parts per work item (the caller's
+// opts->kv_split, else enough parts for about eight work units per CTA slot,
+// at most 4), and the units and partial-result storage of a split plan
+tsr_status plan_split(tsr_plan_impl* P, const tsr_plan_opts* opts, cudaStream_t stream);
 
 // device-side plan consistency checks (check.cu)
 tsr_status plan_check(const tsr_plan_impl* P, cudaStream_t stream);

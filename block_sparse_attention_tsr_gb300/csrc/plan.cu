@@ -525,9 +525,13 @@ int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
 
 tsr_status resolve_regime(Regime rg, const tsr_plan_opts* opts, int d, bool gathered,
                           Regime* out) {
-  // orientation: the caller's, else the table's; key-major tiles exist for
-  // d = 128 only (a table row naming them for d = 64 falls back to 128-row tiles)
-  int32_t orient = (opts && opts->orient) ? opts->orient : rg.orient;
+  // orientation: the caller's, else 128-row tiles when the caller fixes the
+  // pipeline depth or CTAs per SM (parameters of 128-row tiles only), else the
+  // table's; key-major tiles exist for d = 128 only (a table row naming them
+  // for d = 64 falls back to 128-row tiles)
+  int32_t orient = (opts && opts->orient) ? opts->orient
+                   : (opts && (opts->stages || opts->ctas_per_sm)) ? TSR_ORIENT_ROWS
+                                                                   : rg.orient;
   if (orient != TSR_ORIENT_KEYS) orient = TSR_ORIENT_ROWS;
   if (orient == TSR_ORIENT_KEYS && d != 128) {
     if (opts && opts->orient == TSR_ORIENT_KEYS)
@@ -726,6 +730,77 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   plan_emit_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(
       m, nqt, bm, rg.bn, ebegin, dbegin, static_cast<int2*>(P->entries),
       static_cast<tsr_tile_desc*>(P->descs));
+  TSR_CUDA(cudaGetLastError());
+  return TSR_OK;
+}
+
+// ------------------------------------------------------------------ split-KV
+//
+// Tessera abstract: task organisation exposes parallelism.  A request with few
+// work items (a few heads) leaves CTA slots idle while its last items run; the
+// split plan cuts each item's tile list [begin, end) into kv_split contiguous
+// parts of near-equal length (key-major plans cut on whole steps of two tiles).
+// Part p of item i is work unit i * kv_split + p: units keep the items'
+// longest-first order, and the units of one head stay one contiguous range.
+// A unit's second int4 carries (layout, i, kv_split, p); the attention kernel
+// writes the unit's normalised partial O and lse, and the last unit of an item
+// to finish merges the parts:  lse = log2 sum_p 2^lse_p,
+// O = sum_p 2^(lse_p - lse) O_p  (all parts empty: O = 0, lse = -inf).
+namespace {
+
+__global__ void split_units_kernel(const int4* items, int64_t n_items, int32_t s, int32_t step,
+                                   int4* units) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_items) return;
+  const int4 a = items[2 * i], b = items[2 * i + 1];
+  const int32_t n = a.w - a.z;
+  const int32_t steps = (n + step - 1) / step;       // whole steps of `step` tiles
+  for (int32_t p = 0; p < s; ++p) {
+    const int32_t c0 = min(n, step * static_cast<int32_t>((static_cast<int64_t>(p) * steps) / s));
+    const int32_t c1 = min(n, step * static_cast<int32_t>((static_cast<int64_t>(p + 1) * steps) / s));
+    const int64_t u = i * s + p;
+    units[2 * u] = make_int4(a.x, a.y, a.z + c0, a.z + c1);
+    units[2 * u + 1] = make_int4(b.x, static_cast<int32_t>(i), s, p);
+  }
+}
+
+}  // namespace
+
+tsr_status plan_split(tsr_plan_impl* P, const tsr_plan_opts* opts, cudaStream_t stream) {
+  int32_t s = 1;
+  if (opts && opts->kv_split) {
+    s = opts->kv_split;
+  } else {
+    // 128-row plans with fewer work items than CTA slots leave CTAs without
+    // work: cut the items until every slot has one (one 8,192-token head: 64
+    // items on 304 slots, 52 -> 31 us).  With more items than slots a split
+    // costs more than the tail it removes (each part pays the per-item
+    // pipeline start, the partial-result traffic and the merge), and so it
+    // does for key-major plans, whose items are 64 rows already (one
+    // 8,192-token head, 128 items on 152 slots: 24 -> 37 us).
+    if (P->orient != TSR_ORIENT_KEYS) {
+      const int64_t slots = static_cast<int64_t>(num_sms(P->device)) * P->ctas;
+      while (s < 4 && P->n_items * s < slots) s *= 2;
+    }
+  }
+  P->kv_split = s;
+  P->units = nullptr;
+  if (s == 1 || P->n_items == 0) {
+    P->kv_split = 1;
+    return TSR_OK;
+  }
+  const int64_t n_units = P->n_items * s;
+  if (n_units >= (int64_t{1} << 31)) return fail(TSR_ERR_UNSUPPORTED, "too many split-KV work units");
+  const size_t rows = static_cast<size_t>(n_units) * P->bm;
+  if (tsr_status st = devbuf_reserve(P->b_units, sizeof(tsr_plan_item) * n_units)) return st;
+  if (tsr_status st = devbuf_reserve(P->b_part_o, rows * P->d * sizeof(float))) return st;
+  if (tsr_status st = devbuf_reserve(P->b_part_lse, rows * sizeof(float))) return st;
+  if (tsr_status st = devbuf_reserve(P->b_part_cnt, sizeof(int32_t) * P->n_items)) return st;
+  P->units = P->b_units.p;
+  const int threads = 256;
+  split_units_kernel<<<static_cast<unsigned>((P->n_items + threads - 1) / threads), threads, 0, stream>>>(
+      static_cast<const int4*>(P->items), P->n_items, s, P->orient == TSR_ORIENT_KEYS ? 2 : 1,
+      static_cast<int4*>(P->units));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;
 }

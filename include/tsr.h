@@ -133,9 +133,17 @@ typedef struct {
   int32_t stages;    /* 0 = from the regime table; else K/V pipeline depth (2..6)    */
   int32_t ctas_per_sm; /* 0 = from the regime table; 1 or 2                           */
   int32_t flags;     /* TSR_PLAN_* bits                                              */
-  int32_t orient;    /* tile orientation (ABI version 3): 0 = from the regime table,
-                        TSR_ORIENT_ROWS or TSR_ORIENT_KEYS                          */
-  int32_t reserved;  /* must be 0                                                    */
+  int32_t orient;    /* tile orientation (ABI version 3): 0 = from the regime table
+                        (128-row tiles when stages or ctas_per_sm is set: those
+                        are parameters of 128-row tiles), TSR_ORIENT_ROWS or
+                        TSR_ORIENT_KEYS                                         */
+  int32_t kv_split;  /* split-KV (ABI version 3): each work item's key tiles cut
+                        into parts whose partial results the attention kernel
+                        merges.  0 = automatic (a 128-row plan with fewer work
+                        items than CTA slots is cut into 2 or 4 parts, until
+                        every slot has one), 1 = never, 2 or 4 = that many parts.
+                        tsr_attention_host and tsr_attention_noalloc split only
+                        when asked (noalloc: never)                          */
 } tsr_plan_opts;
 
 /* Physical tile orientations.
@@ -181,6 +189,8 @@ typedef struct {
   int64_t max_item_len;
   int32_t regime_id;                    /* row of the regime table used (-1: opts) */
   int32_t orient;                       /* TSR_ORIENT_ROWS or TSR_ORIENT_KEYS       */
+  int32_t kv_split;                     /* parts per work item (1 = not split)     */
+  int32_t reserved;
 } tsr_plan_stats;
 
 /*

@@ -65,6 +65,18 @@ def test_plan_rejects_bad_arguments_on_host(L, kw, code):
     assert len(L.tsr_last_error()) > 0
 
 
+@pytest.mark.parametrize("field,value", [("kv_split", 3), ("kv_split", -1), ("kv_split", 8),
+                                         ("orient", 3), ("bn", 96)])
+def test_plan_rejects_bad_options_on_host(L, field, value):
+    h = ctypes.c_void_p(0)
+    m = _mask(kind=0, B=1, H=1, N=128, d=128, bq=64, bk=64, blocks=16)
+    o = tsr._Opts()
+    setattr(o, field, value)
+    assert L.tsr_plan(ctypes.byref(m), ctypes.byref(o), ctypes.byref(h), None) == 1
+    assert h.value is None or h.value == 0
+    assert field.encode() in L.tsr_last_error()
+
+
 def test_forward_rejects_null_plan(L):
     assert L.tsr_bsa_forward(None, None, None, None, None, None, None) == 1
 

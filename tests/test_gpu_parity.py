@@ -226,7 +226,8 @@ def test_temporal_permute_roundtrip_bit_exact():
 def test_host_entry_point_matches_device_path():
     spec = W.tiny_block_mask(seed=2, N=1024)
     q, k, v = W.qkv(1, 2, 1024, 64, 2)
-    _, _, O, L = run(spec, 64, seed=0, qkv=(q, k, v))
+    # the host entry point does not split work items automatically
+    _, _, O, L = run(spec, 64, seed=0, qkv=(q, k, v), opts={"kv_split": 1})
     out = torch.empty_like(q).pin_memory()
     lse = torch.empty((1, 2, 1024), dtype=torch.float32).pin_memory()
     tsr.tsr_attention_host(spec.kind, 1, 2, 1024, 64, q.pin_memory(), k.pin_memory(),
@@ -395,7 +396,7 @@ def test_keylist_720p_full_size():
 def test_host_entry_point_keylist():
     spec = W.random_keylist(8, 1, 2, 900, slice_m=64, lo=0, hi=300)
     q, k, v = W.qkv(1, 2, 900, 128, 8)
-    _, _, O, L = run(spec, 128, seed=0, qkv=(q, k, v))
+    _, _, O, L = run(spec, 128, seed=0, qkv=(q, k, v), opts={"kv_split": 1})
     out = torch.empty_like(q).pin_memory()
     lse = torch.empty((1, 2, 900), dtype=torch.float32).pin_memory()
     tsr.tsr_attention_host(spec.kind, 1, 2, 900, 128, q.pin_memory(), k.pin_memory(),
@@ -415,7 +416,7 @@ def test_host_entry_point_in_head_groups(which):
     take one plan over all heads and launch each group over its item range;
     with the debug checks (every plan checked on the device, every launch's
     tile count compared) and for key lists each group has its own plan."""
-    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
+    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2, "kv_split": 1}
     if which == "uniform_debug":
         opts = dict(opts, flags=tsr.PLAN_DEBUG_CHECKS)
     if which in ("uniform", "uniform_debug"):
@@ -445,7 +446,7 @@ def test_host_entry_point_alternating_shapes():
     over all heads bit for bit (regime forced).  The block-mask, segment and
     SVG calls take the one-plan path (one plan, one launch per head group over
     its item range); the key-list call plans group by group."""
-    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2}
+    opts = {"bn": 64, "stages": 2, "ctas_per_sm": 2, "kv_split": 1}
     cases = [
         (W.video_block_mask(seed=31, H=12, N=16384), dict(bq=64, bk=64)),
         (W.segment_mask(32, 2, 5, 8000, lo=16, hi=300), {}),
