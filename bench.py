@@ -360,7 +360,7 @@ def run_sweep(args) -> None:
         tsr.tsr_plan_device_status(plan)
         st = plan.stats()
         plan.destroy()
-        return a.elapsed_time(b) / reps, (st["bn"], st["stages"], st["ctas_per_sm"])
+        return a.elapsed_time(b) / reps, (st["bn"], st["stages"], st["ctas_per_sm"], st["orient"])
 
     rows = []
     t0 = time.time()
@@ -369,7 +369,8 @@ def run_sweep(args) -> None:
         mask = tsr.make_mask(spec.kind, 1, H, N, D, **W.mask_tensors(spec, dev))
         flops = 4.0 * D * allowed_pairs(spec)
         t_lut, picked = timed(mask, None)
-        t_var = {vv: timed(mask, {"bn": vv[0], "stages": vv[1], "ctas_per_sm": vv[2]})[0]
+        t_var = {vv: timed(mask, {"bn": vv[0], "stages": vv[1], "ctas_per_sm": vv[2],
+                                  "orient": vv[3]})[0]
                  for vv in VARIANTS[D]}
         best = min(t_var, key=t_var.get)
         rows.append({"m": m, "shape": f"{spec.bq}x{spec.bk}", "rho": spec.meta["rho"],
@@ -390,6 +391,8 @@ def run_sweep(args) -> None:
                            "p90": float(np.quantile(regret, 0.9)), "max": float(regret.max()),
                            "picked_best_within_2pct": float(np.mean(regret <= 0.02))},
             "tflops_by_shape": {k: float(np.mean(v)) for k, v in sorted(shapes.items())},
+            "key_major_picked": int(sum(1 for r in rows if r["lut"][3] == 2)),
+            "key_major_best": int(sum(1 for r in rows if r["best"][3] == 2)),
             "seconds": time.time() - t0}
     if args.sweep_detail:
         line["masks"] = rows
@@ -718,7 +721,10 @@ def main():
                        "allowed_pairs": pairs,
                        "density": pairs / max(1, spec.B * spec.H * spec.N * spec.N),
                        "step": "tsr_plan_update (re-plan of the mask) + tsr_bsa_forward",
-                       "l2": "inputs (603 MB Q/K/V) exceed the 129 MB L2; no flush",
+                       "l2": (f"inputs ({3 * spec.B * (hi - lo) * spec.N * D * 2 / 1e6:.0f} MB Q/K/V) "
+                              + ("exceed the 129 MB L2; no flush"
+                                 if 3 * spec.B * (hi - lo) * spec.N * D * 2 > 129e6
+                                 else "fit the 129 MB L2; not flushed (parity-size run)")),
                        "regime": ({k2: stats[k2] for k2 in ("bm", "bn", "stages", "ctas_per_sm",
                                                              "regime_id")} if stats else None),
                        "tiles": stats["n_entries"] if stats else 0,
