@@ -273,6 +273,8 @@ def test_svg_480p_full_size():
     plan = _sampled_parity(spec, 128, seed=3)
     st = plan.stats()
     assert st["n_temporal_heads"] == 12
+    cov = check_coverage(spec, plan)                   # every head, every row, bit-exact
+    assert cov["allowed"] == 12 * (99_777_600 + 687_960)
 
 
 @pytest.mark.slow
