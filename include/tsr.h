@@ -424,12 +424,13 @@ void tsr_release_host_buffers(void);
  *   - All calls share the array and it keeps the last call's contents (the call
  *     clears what must start at zero).  Calls whose GPU work overlaps -- from two
  *     host threads or on two streams -- race on it and must be serialised.
- *   - The first call on a device looks up the array's device address (again
- *     whenever the calling thread's CUDA context has changed since, e.g. after
- *     cudaDeviceReset); make that first call before any stream capture begins.
+ *   - The first call on a device looks up the array's device address, and does
+ *     again whenever the calling thread's CUDA context has changed since (e.g.
+ *     after cudaDeviceReset).
  *   - Every call synchronises `stream` (to size the plan, and at the end to read
  *     the device error word, returned as TSR_ERR_TIMEOUT / TSR_ERR_INTERNAL).
- *   - Plans 128-row tiles (TSR_ORIENT_ROWS) whatever the regime table picks.
+ *   - Plans 128-row tiles (TSR_ORIENT_ROWS) whatever the regime table picks, and
+ *     never splits work items (kv_split 1).
  */
 tsr_status tsr_attention_noalloc(const tsr_mask *mask, const void *q, const void *k,
                                  const void *v, void *out, float *lse, void *stream);
