@@ -75,7 +75,6 @@ constexpr int KT = 64;                 // keys per plan tile (two per step)
 constexpr int KS = 2, VS = 2;          // K and V slots: slot g feeds group g's steps
 constexpr int kThreads = 384;
 constexpr float kFixThreshold = 16.0f; // base-2 units above the reference maximum
-constexpr float kClamp = 64.0f;        // exponent cap of the optimistic pass (2^64 stays finite)
 constexpr float kMrefInit = -1.0e30f;  // reference maximum of a query with no key yet
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -148,6 +147,15 @@ __device__ __forceinline__ void range64(uint32_t& w0, uint32_t& w1, int lo, int 
 
 __device__ __forceinline__ uint32_t dbyte(const uint4& a, const uint4& b, int i) {
   return fwd::desc_byte(a, b, i);
+}
+
+// y = x * s + c for two lanes at once (fma.rn.f32x2), c per lane.
+__device__ __forceinline__ void fma2c(float& y0, float& y1, float x0, float x1, float s, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 xa, sa, ca;\n\tmov.b64 xa, {%2, %3};\n\tmov.b64 sa, {%4, %4};\n\t"
+      "mov.b64 ca, {%5, %6};\n\tfma.rn.f32x2 xa, xa, sa, ca;\n\tmov.b64 {%0, %1}, xa;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c0), "f"(c1));
 }
 
 // Copy 64 rows of d = 128 bf16 values (row r from source row src(r) of a head)
@@ -697,26 +705,55 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
               if (!((w >> i) & 1u)) y[i] = -INFINITY;
           }
         };
-        // P = 2^(y - m) of one half against the reference m (shared memory),
-        // the exponent capped at kClamp; returns the largest y - m
-        auto exp_half = [&](float (&y)[32], const float* m, bool cap) -> float {
+        // P = 2^(y - m) of one half against the reference m (shared memory);
+        // returns the largest y - m
+        auto exp_half = [&](float (&y)[32], const float* m) -> float {
           float tm = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(m + i);
-            float d0 = y[i] - m4.x, d1 = y[i + 1] - m4.y, d2 = y[i + 2] - m4.z, d3 = y[i + 3] - m4.w;
+            const float d0 = y[i] - m4.x, d1 = y[i + 1] - m4.y, d2 = y[i + 2] - m4.z, d3 = y[i + 3] - m4.w;
             tm = fwd::max3f(tm, d0, d1);
             tm = fwd::max3f(tm, d2, d3);
-            if (cap) {
-              d0 = fminf(d0, kClamp);
-              d1 = fminf(d1, kClamp);
-              d2 = fminf(d2, kClamp);
-              d3 = fminf(d3, kClamp);
-            }
             y[i] = ex2_approx(d0);
             y[i + 1] = ex2_approx(d1);
             y[i + 2] = ex2_approx(d2);
             y[i + 3] = ex2_approx(d3);
+          }
+          return tm;
+        };
+        // The optimistic pass works on the raw logits: P = 2^(x * scale - m) with
+        // the scale and the reference in one FFMA per element (masked: -inf);
+        // returns the largest x * scale - m.  No clamp: a half whose largest
+        // exponent is above the threshold takes the correction, which rewrites
+        // its P^T and never uses its optimistic values
+        auto load_x = [&](int h, float (&x)[32]) {
+          uint32_t rr[32];
+          tmem_ld32(tg + sb * QB + 32 * h, rr);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(rr[i]);
+          const uint32_t w = h ? w1 : w0;
+          if (w != 0xFFFFFFFFu) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!((w >> i) & 1u)) x[i] = -INFINITY;
+          }
+        };
+        auto exp_half_x = [&](float (&x)[32], const float* m) -> float {
+          float tm = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m + i);
+            float d0, d1, d2, d3;
+            fma2c(d0, d1, x[i], x[i + 1], p.scale_log2, -m4.x, -m4.y);
+            fma2c(d2, d3, x[i + 2], x[i + 3], p.scale_log2, -m4.z, -m4.w);
+            tm = fwd::max3f(tm, d0, d1);
+            tm = fwd::max3f(tm, d2, d3);
+            x[i] = ex2_approx(d0);
+            x[i + 1] = ex2_approx(d1);
+            x[i + 2] = ex2_approx(d2);
+            x[i + 3] = ex2_approx(d3);
           }
           return tm;
         };
@@ -766,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
           for (int h = 0; h < 2; ++h) {
             float y[32];
             load_y(h, y);
-            exp_half(y, ctrl.mref[g] + 32 * h, false);
+            exp_half(y, ctrl.mref[g] + 32 * h);
             store_p(h, y);
             uint32_t rl[32];
 #pragma unroll
@@ -775,27 +812,40 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
           }
         } else {
           // optimistic pass against the current reference; the group then
-          // checks that no logit exceeded it by more than the threshold
+          // checks that no logit exceeded it by more than the threshold.  A
+          // warp adds a half's P to its row-sum shares only when no exponent
+          // of that half is above the threshold (`added`, warp-uniform)
           float tmax = -INFINITY;
+          uint32_t added = 0u;
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
             float y[32];
             uint32_t rl[32];
-            load_y(h, y);
+            load_x(h, y);
             tmem_ld32(tl + 32 * h, rl);
-            tmax = fmaxf(tmax, exp_half(y, ctrl.mref[g] + 32 * h, true));
+            const float th = exp_half_x(y, ctrl.mref[g] + 32 * h);
+            tmax = fmaxf(tmax, th);
             store_p(h, y);
             tc_wait_ld();
+            if (!__any_sync(0xFFFFFFFFu, th > kFixThreshold)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rl[i] = __float_as_uint(__uint_as_float(rl[i]) + y[i]);
-            tmem_st32(tl + 32 * h, rl);
+              for (int i = 0; i < 32; i += 2) {
+                float a = __uint_as_float(rl[i]), b = __uint_as_float(rl[i + 1]);
+                fwd::add2(a, b, y[i], y[i + 1]);
+                rl[i] = __float_as_uint(a);
+                rl[i + 1] = __float_as_uint(b);
+              }
+              tmem_st32(tl + 32 * h, rl);
+              added |= 1u << h;
+            }
           }
           if (__any_sync(0xFFFFFFFFu, tmax > kFixThreshold) && lane == 0)
             ctrl.fixflag[g][t & 1] = static_cast<int32_t>(t);
           if (!group_sync()) { ok = false; break; }
           if (ctrl.fixflag[g][t & 1] == static_cast<int32_t>(t)) {
             // correction: raise the reference to the step's exact maximum,
-            // replace this step's optimistic shares (l = (l - p_old) a + p_new),
+            // replace this step's optimistic shares (l = (l - p_old) a + p_new
+            // for the halves that added them, l a + p_new for the others),
             // rewrite P^T, and rescale O^T once the group's previous PV is done
             tc_wait_st();
             if (!raise_reference()) { ok = false; break; }
@@ -803,18 +853,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_t_kernel(const __grid_con
             for (int h = 0; h < 2; ++h) {
               float y[32], yo[32];
               uint32_t rl[32];
-              load_y(h, y);
+              load_x(h, y);
 #pragma unroll
               for (int i = 0; i < 32; ++i) yo[i] = y[i];
               tmem_ld32(tl + 32 * h, rl);
-              exp_half(yo, ctrl.mold[g] + 32 * h, true);     // the optimistic P, as added
-              exp_half(y, ctrl.mref[g] + 32 * h, false);
+              exp_half_x(yo, ctrl.mold[g] + 32 * h);          // the optimistic P, as added
+              exp_half_x(y, ctrl.mref[g] + 32 * h);
               store_p(h, y);
               tc_wait_ld();
+              const bool was_added = (added >> h) & 1u;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const float a = ctrl.alpha[g][32 * h + i];
-                rl[i] = __float_as_uint((__uint_as_float(rl[i]) - yo[i]) * a + y[i]);
+                const float lo = __uint_as_float(rl[i]);
+                rl[i] = __float_as_uint((was_added ? lo - yo[i] : lo) * a + y[i]);
               }
               tmem_st32(tl + 32 * h, rl);
             }
