@@ -812,6 +812,26 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
     // (an explicit opts->kv_split is honoured).
     tsr_plan_opts host_opts = opts ? *opts : tsr_plan_opts{};
     if (host_opts.kv_split == 0) host_opts.kv_split = 1;
+    // Key lists are planned group by group; each group takes the regime of the
+    // whole request (looked up from its total list length), so the result is
+    // the one a single plan over every head gives.
+    if (mask->kind == TSR_MASK_KEYLIST && !host_opts.orient && !host_opts.bn && !host_opts.stages &&
+        !host_opts.ctas_per_sm) {
+      const double n_lists = static_cast<double>(BH) * static_cast<double>(nqb);
+      const double density = n_lists > 0 ? static_cast<double>(mask->indptr[BH * nqb]) / n_lists / mask->N
+                                         : 0.0;
+      Regime rg;
+      if (tsr_status st = resolve_regime(regime_lookup(TSR_MASK_KEYLIST, mask->slice_m, 1, mask->N,
+                                                       density, mask->d),
+                                         nullptr, mask->d, true, &rg))
+        return st;
+      host_opts.orient = rg.orient;
+      if (rg.orient != TSR_ORIENT_KEYS) {
+        host_opts.bn = rg.bn;
+        host_opts.stages = rg.stages;
+        host_opts.ctas_per_sm = rg.ctas;
+      }
+    }
     const tsr_plan_opts& o = host_opts;
     if (static_cast<int64_t>(hc.plans.size()) != G) {
       for (tsr_plan_t pl : hc.plans) tsr_plan_destroy(pl);
