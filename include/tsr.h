@@ -143,7 +143,9 @@ typedef struct {
                         items than CTA slots is cut into 2 or 4 parts, until
                         every slot has one), 1 = never, 2 or 4 = that many parts.
                         tsr_attention_host and tsr_attention_noalloc split only
-                        when asked (noalloc: never)                          */
+                        when asked (noalloc: never).  A split plan holds
+                        n_items * kv_split * bm * d * 4 bytes of partial
+                        results (fp32) in device memory             */
 } tsr_plan_opts;
 
 /* Physical tile orientations.
