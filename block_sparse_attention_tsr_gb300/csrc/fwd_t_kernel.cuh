@@ -38,15 +38,18 @@
 // Softmax in the transposed layout.  A thread holds one key's logits for the
 // 64 queries, so reductions over keys run across the 128 threads of a group.
 // The running maximum per query is therefore not taken every step: P^T is
-// computed against a per-query reference m (shared memory), and only when a
-// logit exceeds its reference by more than 2^16 (in base-2 units) does the
-// group take the exact column maximum of the step (warp shuffles + shared
-// memory), raise m, and rescale its row sums and O^T by 2^(m_old - m_new).
-// The first step of every item starts from m = -1e30, so it always takes that
-// path.  Every thread keeps its key's share of the 64 row sums in TMEM; the
-// shares are summed over the 128 threads once per item, in the epilogue.  The
-// result is the same masked softmax; only the reference point of the
-// exponentials differs, which cancels in O = (sum_k P V) / (sum_k P).
+// computed against a per-query reference m (shared memory), and only when an
+// exponent y - m (base 2) exceeds 16 -- a logit 2^16 times its reference --
+// does the group take the exact column maximum of the step (warp shuffles +
+// shared memory), raise m, rewrite the step's P^T and rescale its row sums and
+// O^T by 2^(m_old - m_new).  A warp adds a half-step's P to its row-sum shares
+// only when none of its exponents is above 16, so the correction knows which
+// optimistic values it has to take back.  The first step of every item starts
+// from m = -1e30, so it always takes the exact path.  Every thread keeps its
+// key's share of the 64 row sums in TMEM; the shares are summed over the 128
+// threads once per item, in the epilogue.  The result is the same masked
+// softmax; only the reference point of the exponentials differs, which cancels
+// in O = (sum_k P V) / (sum_k P).
 #pragma once
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
