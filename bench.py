@@ -132,11 +132,18 @@ def read_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the attention kernels' sources (both tile orientations)."""
+    """Hash of the attention kernels' sources (both tile orientations), with
+    comments and blank lines removed: a profile stays attached to the code it
+    measured when only a comment changes."""
+    import re
     h = hashlib.sha256()
     for f in ("fwd_kernel.cuh", "fwd_t_kernel.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "block_sparse_attention_tsr_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        lines = [ln.rstrip() for ln in src.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
