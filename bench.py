@@ -48,17 +48,24 @@ def allowed_pairs_uniform(spec) -> int:
 
 
 def launches_per_step(spec, stats) -> int:
-    """Kernels of this library launched per step (re-plan + forward).  Temporal
-    SVG heads need no kernel of their own: the attention kernel applies the
-    temporal-major permutation in its loads and stores."""
+    """Kernels of this library launched per step (re-plan + forward).  SVG
+    temporal heads of radius 0 take the launch-list compaction at plan time and
+    the per-position kernel after the attention kernel; on the tiles they need
+    no kernel of their own (the attention kernel applies the temporal-major
+    permutation in its loads and stores).  A split plan adds the unit cut."""
     import workloads as W
     if spec.kind == W.MASK_KEYLIST:
         # count (validating), schedule, emit; a separate validation pass above
         # 196,608 tokens; + attention
-        return (4 if spec.N > 196608 else 3) + 1
-    n = 3 + 1                              # count, schedule, emit + attention
-    if spec.kind in (W.MASK_UNIFORM, W.MASK_SEGMENTS):
-        n += 1                             # logical-block count (mask density)
+        n = (4 if spec.N > 196608 else 3) + 1
+    else:
+        n = 3 + 1                          # count, schedule, emit + attention
+        if spec.kind in (W.MASK_UNIFORM, W.MASK_SEGMENTS):
+            n += 1                         # logical-block count (mask density)
+        if stats.get("temporal_band"):
+            n += 2                         # launch-list compaction + per-position kernel
+    if stats.get("kv_split", 1) > 1:
+        n += 1
     return n
 
 
@@ -530,16 +537,32 @@ def other_workloads(tsr, names, steps: int, warmup: int, dev, stream, peak: floa
                      "step_tflops": flops / (total_ms / steps) / 1e9,
                      "forward_tflops": flops / fwd_ms / 1e9,
                      "forward_frac_of_peak": flops / fwd_ms / 1e9 / peak,
-                     "fill": fill_of(spec, st), "tiles": st["n_entries"],
-                     "regime": {k: st[k] for k in ("bm", "bn", "stages", "ctas_per_sm", "regime_id")}}
+                     "fill": fill_of(spec, st, plan), "tiles": st["n_entries"],
+                     "regime": {k: st[k] for k in ("bm", "bn", "stages", "ctas_per_sm", "regime_id")},
+                     **({"temporal_heads": "by spatial position (F x F blocks, own kernel); "
+                                           "fill over the spatial heads' tiles"}
+                        if st.get("temporal_band") else {})}
         plan.destroy()
         del qd, kd, vd, out, lse, mask
         torch.cuda.empty_cache()
     return res
 
 
-def fill_of(spec, stats) -> float:
-    """Allowed pairs over the elements of the computed physical tiles."""
+def fill_of(spec, stats, plan=None) -> float:
+    """Allowed pairs over the elements of the computed physical tiles.  When
+    the SVG temporal heads run by spatial position (no tiles), over the spatial
+    heads' tiles only, counted from the plan's export (items of layout 0)."""
+    if stats.get("temporal_band") and plan is not None:
+        import workloads as W
+        buf = plan.export()
+        n_items = int(np.frombuffer(buf, np.int64, 1, 48)[0])
+        items = np.frombuffer(buf, np.int32, 8 * n_items, 80).reshape(n_items, 8)
+        spatial = items[:, 4] == 0
+        tiles = int((items[spatial, 3] - items[spatial, 2]).sum())
+        S, F = spec.frame_size, spec.n_frames
+        n_sp = int(sum(int(k) == W.HEAD_SPATIAL for k in spec.head_kind)) * spec.B
+        computed = tiles * stats["bm"] * stats["bn"]
+        return S * S * (2 * F - 1) * n_sp / computed if computed else None
     computed = stats["n_entries"] * stats["bm"] * stats["bn"]
     return allowed_pairs(spec) / computed if computed else None
 
@@ -736,7 +759,10 @@ def main():
                                                              "regime_id")} if stats else None),
                        "tiles": stats["n_entries"] if stats else 0,
                        "boundary_tiles": stats["n_boundary"] if stats else 0,
-                       "fill": fill_of(spec, stats) if stats else None,
+                       "fill": fill_of(spec, stats, plan) if stats else None,
+                       **({"temporal_heads": "by spatial position (F x F blocks, own kernel); "
+                                             "fill over the spatial heads' tiles"}
+                          if stats and stats.get("temporal_band") else {}),
                        "forward_ms": fwd_avg, "plan_ms": ms_step - fwd_avg,
                        **({"svg_route": route} if route else {}),
                        **({"other_workloads": others} if others else {}),

@@ -28,12 +28,14 @@ __all__ = [
     "tsr_regime_load",
     "tsr_regime_lookup", "tsr_abi_version", "UNIFORM", "SEGMENTS", "SVG", "KEYLIST",
     "ORIENT_ROWS", "ORIENT_KEYS",
-    "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL",
+    "PLAN_SYNC_CHECK", "PLAN_NO_LPT", "PLAN_TEST_STALL", "PLAN_DEBUG_CHECKS",
+    "PLAN_TEMPORAL_TILES",
 ]
 
 UNIFORM, SEGMENTS, SVG, KEYLIST = 0, 1, 2, 3
 ORIENT_ROWS, ORIENT_KEYS = 1, 2
 PLAN_SYNC_CHECK, PLAN_NO_LPT, PLAN_TEST_STALL, PLAN_DEBUG_CHECKS = 1, 2, 4, 8
+PLAN_TEMPORAL_TILES = 16
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of memory",
            5: "device wait timed out", 6: "internal error"}
 
@@ -81,7 +83,7 @@ class _Stats(ctypes.Structure):
                 ("n_logical_on", ctypes.c_int64), ("n_logical_total", ctypes.c_int64),
                 ("max_item_len", ctypes.c_int64), ("regime_id", ctypes.c_int32),
                 ("orient", ctypes.c_int32), ("kv_split", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("temporal_band", ctypes.c_int32)]
 
 
 class _Regime(ctypes.Structure):
@@ -212,7 +214,7 @@ class Plan:
     def stats(self) -> dict:
         st = _Stats()
         _check(lib().tsr_plan_get_stats(self.handle, ctypes.byref(st)))
-        return {f: getattr(st, f) for f, _ in st._fields_ if f != "reserved"}
+        return {f: getattr(st, f) for f, _ in st._fields_}
 
     def export(self) -> bytes:
         n = ctypes.c_size_t(0)

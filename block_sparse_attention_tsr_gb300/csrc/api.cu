@@ -241,7 +241,7 @@ void free_plan(tsr_plan_s* P) {
   if (!P) return;
   for (DevBuf* b : {&P->b_items, &P->b_entries, &P->b_descs, &P->b_cnt, &P->b_tot, &P->b_ebegin,
                     &P->b_dbegin, &P->b_hist, &P->b_gidx, &P->b_units, &P->b_part_o, &P->b_part_lse,
-                    &P->b_part_cnt})
+                    &P->b_part_cnt, &P->b_launch})
     devbuf_free(*b);
   cudaFree(P->counter);
   cudaFree(P->err);
@@ -267,6 +267,7 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
     // pinned host copy is checked after the planner's count synchronisation.
     P->F = mask->n_frames;
     P->S = mask->frame_size;
+    P->R = mask->temporal_radius;
     if (!P->head_kind_dev) TSR_CUDA(cudaMalloc(&P->head_kind_dev, mask->H));
     if (!P->host_kinds) TSR_CUDA(cudaMallocHost(&P->host_kinds, mask->H));
     TSR_CUDA(cudaMemcpyAsync(P->head_kind_dev, mask->head_kind, mask->H, cudaMemcpyDeviceToDevice,
@@ -281,6 +282,7 @@ tsr_status plan_fill(tsr_plan_s* P, const tsr_mask* mask, cudaStream_t st) {
   } else if (tsr_status s = plan_build(mask, P->has_opts ? &P->opts : nullptr, P, st)) {
     return s;
   }
+  if (tsr_status s = plan_launch_list(P, st)) return s;
   if (tsr_status s = plan_split(P, P->has_opts ? &P->opts : nullptr, st)) return s;
   if (P->flags & TSR_PLAN_DEBUG_CHECKS) {
     if (tsr_status s = plan_check(P, st)) return s;
@@ -550,6 +552,7 @@ tsr_status tsr_plan_get_stats(tsr_plan_t plan, tsr_plan_stats* s) {
   s->regime_id = plan->regime_id;
   s->orient = plan->orient;
   s->kv_split = plan->kv_split;
+  s->temporal_band = plan->temporal_band;
   return TSR_OK;
 }
 

@@ -92,8 +92,12 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
   const tsr_plan_impl* P0 = reqs[0].plan;
   // one launch needs one kernel variant: the same head dimension, regime and
   // gather mode for every request; temporal heads anywhere select the variant
-  // that may gather through the permutation
+  // that may gather through the permutation, unless the per-position kernel
+  // takes them
   bool temporal = false;
+  // each request's range in its launch list, and the heads whose temporal
+  // blocks the per-position kernel computes
+  int64_t lo_of[fwd::kMaxBatch], hi_of[fwd::kMaxBatch], bh_lo[fwd::kMaxBatch], bh_hi[fwd::kMaxBatch];
   for (int r = 0; r < n_req; ++r) {
     const tsr_plan_impl* P = reqs[r].plan;
     if (P->device != P0->device || P->d != P0->d || P->bn != P0->bn || P->stages != P0->stages ||
@@ -101,7 +105,27 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
       return fail(TSR_ERR_UNSUPPORTED,
                   "requests of one batch need the same d, regime (orientation, bn, stages, ctas) "
                   "and mask family (key lists or not); plan them with the same tsr_plan_opts");
-    temporal = temporal || P->n_temporal > 0;
+    temporal = temporal || (P->n_temporal > 0 && !P->temporal_band);
+    const int64_t ilo = reqs[r].item_lo, ihi = reqs[r].item_hi < 0 ? P->n_items : reqs[r].item_hi;
+    if (ilo < 0 || ihi > P->n_items || ilo > ihi) return fail(TSR_ERR_INTERNAL, "bad item range");
+    lo_of[r] = ilo;
+    hi_of[r] = ihi;
+    bh_lo[r] = bh_hi[r] = 0;
+    if (P->temporal_band) {
+      // whole heads: the plan's items are in head order (one head per
+      // scheduling group), nqt of them per head, unless the range is all items
+      const int64_t BH = static_cast<int64_t>(P->B) * P->H, nqt = (P->N + P->bm - 1) / P->bm;
+      if (ilo == 0 && ihi == P->n_items) {
+        bh_hi[r] = BH;
+      } else {
+        if (P->group_heads != 1 || ilo % nqt || ihi % nqt)
+          return fail(TSR_ERR_INTERNAL, "item range of a plan with separate temporal heads");
+        bh_lo[r] = ilo / nqt;
+        bh_hi[r] = ihi / nqt;
+      }
+      lo_of[r] = nqt * P->spatial_before[bh_lo[r]];
+      hi_of[r] = nqt * P->spatial_before[bh_hi[r]];
+    }
   }
   const int key = vkey(P0->d, P0->bn, P0->stages, P0->ctas);
   auto fill = [&](auto& prm) -> tsr_status {
@@ -121,12 +145,12 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
                       encode_tmap_3d(&q.tv, a.v, D, N, BH, 64, krows);
       if (!ok)
         return fail(TSR_ERR_CUDA, "cuTensorMapEncodeTiled failed (pointer alignment or shape)");
-      // the range is in work items; a split plan launches their units
-      const int64_t ilo = a.item_lo, ihi = a.item_hi < 0 ? P->n_items : a.item_hi;
-      if (ilo < 0 || ihi > P->n_items || ilo > ihi) return fail(TSR_ERR_INTERNAL, "bad item range");
+      // the range is in launch-list items; a split plan launches their units
+      const int64_t ilo = lo_of[r], ihi = hi_of[r];
       const bool split = P->kv_split > 1;
       const int64_t lo = ilo * P->kv_split, hi = ihi * P->kv_split;
-      q.items = static_cast<const int4*>(split ? P->units : P->items) + 2 * lo;
+      q.items = static_cast<const int4*>(split ? P->units : P->temporal_band ? P->launch : P->items) +
+                2 * lo;
       if (split) {
         q.part_o = static_cast<float*>(P->b_part_o.p);
         q.part_lse = static_cast<float*>(P->b_part_lse.p);
@@ -188,6 +212,16 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
     if (!prm) return fail(TSR_ERR_OOM, "host allocation failed");
     if (tsr_status e = fill(*prm)) return e;
     st = launch(*prm);
+  }
+  if (st == TSR_OK) {
+    for (int r = 0; r < n_req; ++r) {
+      const tsr_plan_impl* P = reqs[r].plan;
+      if (!P->temporal_band) continue;
+      if (tsr_status e = launch_svg_temporal(reqs[r].q, reqs[r].k, reqs[r].v, reqs[r].out, reqs[r].lse,
+                                             P->H, P->N, P->d, P->F, P->S, P->head_kind_dev,
+                                             bh_lo[r], bh_hi[r], stream))
+        return e;
+    }
   }
   if (st != TSR_ERR_UNSUPPORTED) return st;
   return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P0->d) + " bn=" +

@@ -60,7 +60,7 @@ struct tsr_plan_impl {
   int32_t bn = 128, stages = 3, ctas = 1, regime_id = -1;
   int32_t orient = TSR_ORIENT_ROWS, bm = kBM;   // tile orientation and query rows per tile
   int32_t gathered = 0, slice_m = 0;
-  int32_t F = 0, S = 0;
+  int32_t F = 0, S = 0, R = 0;
   int32_t flags = 0;
   int64_t n_items = 0, n_entries = 0, n_desc = 0, n_gidx = 0;
   int64_t n_logical_on = 0, n_logical_total = 0, max_item_len = 0;
@@ -70,7 +70,15 @@ struct tsr_plan_impl {
   // split-KV: each work item's tile list cut into kv_split parts (1 = off); the
   // parts are the launch's work units, written to `units` in item order
   int32_t kv_split = 1;
-  void* units = nullptr;      // tsr_plan_item [n_items * kv_split] (kv_split > 1)
+  void* units = nullptr;      // tsr_plan_item [n_launch * kv_split] (kv_split > 1)
+  // SVG temporal heads of radius 0 with at most 32 frames run as one F x F block
+  // per spatial position (svg_temporal.cu); the attention kernels then take the
+  // spatial heads' items only: `launch`, the items without the temporal heads'
+  // in their scheduled order.  Otherwise launch = items, n_launch = n_items.
+  int32_t temporal_band = 0;
+  void* launch = nullptr;
+  int64_t n_launch = 0;
+  std::vector<int64_t> spatial_before;   // [B*H + 1]: spatial heads among bh < i
   // device buffers (owned)
   void* items = nullptr;     // tsr_plan_item [n_items]
   void* entries = nullptr;   // tsr_plan_entry [n_entries]
@@ -84,6 +92,7 @@ struct tsr_plan_impl {
   // split-KV storage: units, each unit's partial O (fp32 [bm][d]) and lse (base 2,
   // [bm]), one arrival counter per work item
   DevBuf b_units, b_part_o, b_part_lse, b_part_cnt;
+  DevBuf b_launch;
   unsigned long long* host_tot = nullptr;   // pinned: 8 totals + the error word
   int8_t* host_kinds = nullptr;             // pinned: SVG head kinds, read after the count sync
   bool has_opts = false;
@@ -111,6 +120,10 @@ tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int
                             const int32_t* cnt_b, int32_t max_len, int32_t* ebegin,
                             int32_t* dbegin, int32_t* hist, void* items, void* entries,
                             void* descs, cudaStream_t stream);
+
+// The attention launch list (plan.cu): the spatial heads' items when the SVG
+// temporal heads go to the per-position kernel, else the items themselves.
+tsr_status plan_launch_list(tsr_plan_impl* P, cudaStream_t stream);
 
 // split-KV (plan.cu): the number of parts per work item (the caller's
 // opts->kv_split, else enough parts for about eight work units per CTA slot,
@@ -150,6 +163,15 @@ tsr_status resolve_regime(Regime table, const tsr_plan_opts* opts, int d, bool g
 tsr_status launch_route(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                         int32_t F, int32_t S, int32_t d, int32_t R, const int32_t* samples,
                         int32_t n_samples, float* stats, int8_t* head_kind, cudaStream_t stream);
+
+// SVG temporal heads, one F x F block per spatial position (svg_temporal.cu):
+// radius 0, 1 <= F <= 32, d in {64, 128}.  Heads bh in [bh_lo, bh_hi) whose kind
+// is temporal; the others are left alone.
+bool svg_temporal_eligible(int32_t F, int32_t R, int32_t d);
+tsr_status launch_svg_temporal(const void* q, const void* k, const void* v, void* out, float* lse,
+                               int32_t H, int32_t N, int32_t d, int32_t F, int32_t S,
+                               const int8_t* head_kind, int64_t bh_lo, int64_t bh_hi,
+                               cudaStream_t stream);
 
 // permutation (permute.cu)
 tsr_status launch_permute(const void* src, void* dst, int32_t B, int32_t H, int32_t F, int32_t S,

@@ -734,12 +734,84 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   return TSR_OK;
 }
 
+// --------------------------------------------------------- launch list (SVG)
+//
+// Sparse VideoGen digest, "Sparse VideoGen": with radius 0 a temporal head's
+// allowed pairs are the F x F blocks of the tokens at one spatial position, too
+// small for 64- or 128-row tiles.  svg_temporal.cu computes them; the attention
+// kernels take the spatial heads' items, in the order the scheduler gave them.
+namespace {
+
+// Stable compaction of the items whose head is not temporal, by one CTA: each
+// thread takes a contiguous run of items, the runs' kept counts are scanned.
+__global__ void launch_compact_kernel(const int4* items, int64_t n_items, const int8_t* head_kind,
+                                      int32_t H, int4* launch) {
+  __shared__ int64_t warp_sum[32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, n_warps = blockDim.x >> 5;
+  const int64_t per = (n_items + blockDim.x - 1) / blockDim.x;
+  const int64_t i0 = min(n_items, t * per), i1 = min(n_items, i0 + per);
+  int64_t kept = 0;
+  for (int64_t i = i0; i < i1; ++i) kept += head_kind[items[2 * i].x % H] != TSR_HEAD_TEMPORAL;
+  int64_t x = kept;                                       // inclusive scan in the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < n_warps ? warp_sum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sum[lane] = w;
+  }
+  __syncthreads();
+  int64_t at = x - kept + (warp ? warp_sum[warp - 1] : 0);
+  for (int64_t i = i0; i < i1; ++i) {
+    const int4 a = items[2 * i];
+    if (head_kind[a.x % H] == TSR_HEAD_TEMPORAL) continue;
+    launch[2 * at] = a;
+    launch[2 * at + 1] = items[2 * i + 1];
+    ++at;
+  }
+}
+
+}  // namespace
+
+tsr_status plan_launch_list(tsr_plan_impl* P, cudaStream_t stream) {
+  const int64_t BH = static_cast<int64_t>(P->B) * P->H;
+  P->temporal_band = 0;
+  P->launch = P->items;
+  P->n_launch = P->n_items;
+  P->spatial_before.clear();
+  if (P->kind != TSR_MASK_SVG || P->n_temporal == 0 || !svg_temporal_eligible(P->F, P->R, P->d) ||
+      (P->flags & (TSR_PLAN_DEBUG_CHECKS | TSR_PLAN_TEMPORAL_TILES)))
+    return TSR_OK;
+  P->spatial_before.assign(BH + 1, 0);
+  for (int64_t bh = 0; bh < BH; ++bh)
+    P->spatial_before[bh + 1] = P->spatial_before[bh] + (P->head_layout[bh % P->H] ? 0 : 1);
+  const int64_t nqt = (P->N + P->bm - 1) / P->bm;   // every head has nqt items
+  P->temporal_band = 1;
+  P->n_launch = nqt * P->spatial_before[BH];
+  if (P->n_launch == 0) return TSR_OK;
+  if (tsr_status st = devbuf_reserve(P->b_launch, sizeof(tsr_plan_item) * P->n_launch)) return st;
+  P->launch = P->b_launch.p;
+  launch_compact_kernel<<<1, 1024, 0, stream>>>(static_cast<const int4*>(P->items), P->n_items,
+                                                 P->head_kind_dev, P->H, static_cast<int4*>(P->launch));
+  TSR_CUDA(cudaGetLastError());
+  return TSR_OK;
+}
+
 // ------------------------------------------------------------------ split-KV
 //
 // Tessera abstract: task organisation exposes parallelism.  A request with few
 // work items (a few heads) leaves CTA slots idle while its last items run; the
 // split plan cuts each item's tile list [begin, end) into kv_split contiguous
 // parts of near-equal length (key-major plans cut on whole steps of two tiles).
+// The items cut are those of the launch list (without the SVG temporal heads
+// that run on their own kernel); i below indexes that list.
 // Part p of item i is work unit i * kv_split + p: units keep the items'
 // longest-first order, and the units of one head stay one contiguous range.
 // A unit's second int4 carries (layout, i, kv_split, p); the attention kernel
@@ -780,26 +852,26 @@ tsr_status plan_split(tsr_plan_impl* P, const tsr_plan_opts* opts, cudaStream_t 
     // 8,192-token head, 128 items on 152 slots: 24 -> 37 us).
     if (P->orient != TSR_ORIENT_KEYS) {
       const int64_t slots = static_cast<int64_t>(num_sms(P->device)) * P->ctas;
-      while (s < 4 && P->n_items * s < slots) s *= 2;
+      while (s < 4 && P->n_launch * s < slots) s *= 2;
     }
   }
   P->kv_split = s;
   P->units = nullptr;
-  if (s == 1 || P->n_items == 0) {
+  if (s == 1 || P->n_launch == 0) {
     P->kv_split = 1;
     return TSR_OK;
   }
-  const int64_t n_units = P->n_items * s;
+  const int64_t n_units = P->n_launch * s;
   if (n_units >= (int64_t{1} << 31)) return fail(TSR_ERR_UNSUPPORTED, "too many split-KV work units");
   const size_t rows = static_cast<size_t>(n_units) * P->bm;
   if (tsr_status st = devbuf_reserve(P->b_units, sizeof(tsr_plan_item) * n_units)) return st;
   if (tsr_status st = devbuf_reserve(P->b_part_o, rows * P->d * sizeof(float))) return st;
   if (tsr_status st = devbuf_reserve(P->b_part_lse, rows * sizeof(float))) return st;
-  if (tsr_status st = devbuf_reserve(P->b_part_cnt, sizeof(int32_t) * P->n_items)) return st;
+  if (tsr_status st = devbuf_reserve(P->b_part_cnt, sizeof(int32_t) * P->n_launch)) return st;
   P->units = P->b_units.p;
   const int threads = 256;
-  split_units_kernel<<<static_cast<unsigned>((P->n_items + threads - 1) / threads), threads, 0, stream>>>(
-      static_cast<const int4*>(P->items), P->n_items, s, P->orient == TSR_ORIENT_KEYS ? 2 : 1,
+  split_units_kernel<<<static_cast<unsigned>((P->n_launch + threads - 1) / threads), threads, 0, stream>>>(
+      static_cast<const int4*>(P->launch), P->n_launch, s, P->orient == TSR_ORIENT_KEYS ? 2 : 1,
       static_cast<int4*>(P->units));
   TSR_CUDA(cudaGetLastError());
   return TSR_OK;

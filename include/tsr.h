@@ -95,7 +95,13 @@ typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
  *           Temporal heads run in temporal-major order (t' = s * n_frames + f):
  *           the attention kernel reads their Q/K/V rows through the inverse
  *           permutation and writes O and lse back in the caller's order; nothing
- *           is copied.  Any n_frames >= 1; frame_size >= 16 when a head is
+ *           is copied.  With temporal_radius = 0, n_frames <= 32 and no
+ *           TSR_PLAN_TEMPORAL_TILES / TSR_PLAN_DEBUG_CHECKS, a temporal head is
+ *           instead computed as frame_size independent n_frames x n_frames
+ *           blocks (one per spatial index) by a kernel of its own, launched
+ *           after the attention kernel on the same stream (P rounded to bf16 for the
+ *           P V product there too).
+ *           Any n_frames >= 1; frame_size >= 16 when a head is
  *           spatial (a 128-token tile may hold at most 8 frames; smaller frames
  *           give TSR_ERR_UNSUPPORTED); temporal_radius >= 0.
  * KEYLIST : slice_m in {64, 128}.  indptr = int64 [B*H*ceil(N/slice_m) + 1] (CSR
@@ -174,7 +180,11 @@ typedef struct {
                                   TSR_ERR_INTERNAL on a violation; every
                                   tsr_bsa_forward(_batch) also counts the tiles
                                   the kernel computed and compares them with the
-                                  plan.  Both synchronise `stream`.             */
+                                  plan.  Both synchronise `stream`.  SVG temporal
+                                  heads then run on the attention tiles.        */
+#define TSR_PLAN_TEMPORAL_TILES 16  /* SVG temporal heads run on the attention tiles
+                                  (temporal-major order) even where the
+                                  per-position kernel could take them           */
 
 typedef struct tsr_plan_s *tsr_plan_t;   /* opaque, library-owned */
 
@@ -192,7 +202,10 @@ typedef struct {
   int32_t regime_id;                    /* row of the regime table used (-1: opts) */
   int32_t orient;                       /* TSR_ORIENT_ROWS or TSR_ORIENT_KEYS       */
   int32_t kv_split;                     /* parts per work item (1 = not split)     */
-  int32_t reserved;
+  int32_t temporal_band;                /* 1: SVG temporal heads run one F x F block
+                                           per spatial position, outside the
+                                           attention tiles (their items stay in
+                                           the plan and its export)              */
 } tsr_plan_stats;
 
 /*

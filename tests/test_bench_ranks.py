@@ -61,10 +61,15 @@ def test_one_rank_is_its_own_time():
 def test_launches_per_step_match_the_planner():
     """count, [logical count,] schedule, emit, attention; key lists: count,
     schedule, emit (+ a validation pass above 196,608 tokens), attention; no
-    permutation kernels (SVG temporal heads are permuted inside the loads)."""
+    permutation kernels (SVG temporal heads on the tiles are permuted inside
+    the loads; by spatial position they add the launch-list compaction and
+    their own kernel); a split plan adds the unit cut."""
     assert bench.launches_per_step(W.tiny_block_mask(), {}) == 5
+    assert bench.launches_per_step(W.tiny_block_mask(), {"kv_split": 2}) == 6
     assert bench.launches_per_step(W.segment_mask(1, 1, 1, 2048), {}) == 5
     assert bench.launches_per_step(W.svg_mask(1, 4, 4, 64), {"n_temporal_heads": 2}) == 4
+    assert bench.launches_per_step(W.svg_mask(1, 4, 4, 64),
+                                   {"n_temporal_heads": 2, "temporal_band": 1}) == 6
     kl = W.random_keylist(1, 1, 1, 1024, hi=10)
     assert bench.launches_per_step(kl, {}) == 4
     kl.N = 200000

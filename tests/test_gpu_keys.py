@@ -91,10 +91,12 @@ def test_segments():
                                          (1, 700, [0, 1, 0], 0)])
 def test_svg(F, S, kinds, r):
     """Spatial heads (TMA) and temporal heads (rows gathered through the
-    temporal-major permutation, band descriptors) in one launch; ragged N."""
+    temporal-major permutation, band descriptors) in one launch; ragged N.
+    Radius-0 heads are kept on the tiles here (TSR_PLAN_TEMPORAL_TILES)."""
     spec = W.svg_mask(2, len(kinds), n_frames=F, frame_size=S, kinds=np.array(kinds, np.int8),
                       temporal_radius=r)
-    plan, _ = full_parity(spec, seed=21 + F)
+    plan, _ = full_parity(spec, seed=21 + F, opts={"flags": tsr.PLAN_TEMPORAL_TILES})
+    assert plan.stats()["temporal_band"] == 0
     assert plan.stats()["n_temporal_heads"] == sum(kinds)
 
 

@@ -137,14 +137,17 @@ def test_svg_ragged_temporal_gather(opts, F, S):
     batches and mixed head kinds put spatial (TMA) and temporal (gathered)
     items in one launch.  Frame counts below 16 (13, 5, 1) put more than 8
     temporal segments in a 128-token tile: those tiles are masked by the band
-    rule, which has no segment limit."""
+    rule, which has no segment limit.  TSR_PLAN_TEMPORAL_TILES keeps these
+    radius-0 heads on the tiles."""
     d = 64 if opts and opts.get("stages") == 3 and opts.get("ctas_per_sm") == 2 else 128
     spec = W.svg_mask(2, 3, n_frames=F, frame_size=S, kinds=np.array([1, 0, 1], np.int8))
+    opts = dict(opts or {}, flags=tsr.PLAN_TEMPORAL_TILES)
     (q, k, v), plan, O, L = run(spec, d, seed=21, opts=opts)
     O_ref, L_ref = oracle.attention(spec, q, k, v)
     compare(O_ref, L_ref, O, L, f"svg ragged {opts}")
     check_coverage(spec, plan)
     assert plan.stats()["n_temporal_heads"] == 2
+    assert plan.stats()["temporal_band"] == 0
 
 
 @pytest.mark.parametrize("r,opts", [(1, None), (4, {"bn": 128, "stages": 3}),
@@ -268,11 +271,14 @@ def test_video_480p_block_mask_bn128():
 
 
 @pytest.mark.slow
-def test_svg_480p_full_size():
+@pytest.mark.parametrize("flags", [0, tsr.PLAN_TEMPORAL_TILES])
+def test_svg_480p_full_size(flags):
+    """Temporal heads by spatial position (the default), or on the tiles."""
     spec = W.svg_mask(1, 24, n_frames=21, frame_size=1560)
-    plan = _sampled_parity(spec, 128, seed=3)
+    plan = _sampled_parity(spec, 128, seed=3, opts={"flags": flags} if flags else None)
     st = plan.stats()
     assert st["n_temporal_heads"] == 12
+    assert st["temporal_band"] == (0 if flags else 1)
     cov = check_coverage(spec, plan)                   # every head, every row, bit-exact
     assert cov["allowed"] == 12 * (99_777_600 + 687_960)
 

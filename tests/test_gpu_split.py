@@ -90,10 +90,12 @@ def test_parts_without_tiles(orient):
 @pytest.mark.parametrize("F,S,kinds,r", [(16, 48, [0, 1, 1, 0], 0), (5, 130, [1, 1, 0], 40)])
 def test_svg(F, S, kinds, r, orient):
     """Temporal heads gather their rows through the temporal-major permutation
-    and the merged rows are stored back in frame-major order."""
+    and the merged rows are stored back in frame-major order (radius-0 heads
+    kept on the tiles by TSR_PLAN_TEMPORAL_TILES)."""
     spec = W.svg_mask(2, len(kinds), n_frames=F, frame_size=S, kinds=np.array(kinds, np.int8),
                       temporal_radius=r)
-    parity(spec, 128, 21 + F, {"orient": ORIENTS[orient], "kv_split": 2})
+    parity(spec, 128, 21 + F, {"orient": ORIENTS[orient], "kv_split": 2,
+                               "flags": tsr.PLAN_TEMPORAL_TILES})
 
 
 KEYLIST = [
