@@ -220,6 +220,17 @@ __device__ void grid_dims(const MaskDev& m, int64_t* nqs, int64_t* nks) {
   }
 }
 
+// UNIFORM masks whose query tiles lie inside one logical row block (bq a
+// multiple of the tile height) and whose 64-key sub-tiles lie inside one
+// logical column block (bk a multiple of 64): a sub-tile is allowed iff its one
+// logical block is, and full iff also inside [0, N).  The count and emit
+// kernels then read the row of logical blocks directly instead of classifying
+// segment grids (same results as classify(); the ragged last key tile still
+// goes through classify() for its descriptor).
+__device__ __forceinline__ bool aligned_uniform(const MaskDev& m, int bm, int bn) {
+  return m.kind == TSR_MASK_UNIFORM && m.bq % bm == 0 && m.bk % bn == 0;
+}
+
 // Per query tile: [0] tiles at BN=64, [1] boundary tiles at BN=64, [2] tiles at
 // BN=128, [3] boundary at BN=128.  Totals: the same four sums, then [4], [5] the
 // longest item at BN=64 / 128, [6] allowed logical blocks.
@@ -245,6 +256,29 @@ __global__ void plan_count_kernel(MaskDev m, int32_t nqt, int32_t bm, int32_t* c
     const int n_kt = kw.size();
     int e64 = 0, b64 = 0, e128 = 0, b128 = 0;
     bool bad = false;
+    if (aligned_uniform(m, bm, 64)) {
+      // 64-key sub-tiles s < ceil(N / 64), 16 consecutive ones per lane (their
+      // loads issued together); 128-key tile i = sub-tiles 2i and 2i + 1
+      const uint8_t* row = m.blocks + (static_cast<int64_t>(bh) * nqs + rs.q0 / m.bq) * nks;
+      const int n64 = (m.N + 63) >> 6, per = m.bk >> 6;
+      for (int base = 0; base < n64; base += 32 * 16) {
+        const int s0 = base + lane * 16;
+        uint32_t on = 0, full = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int sj = s0 + j;
+          if (sj < n64 && __ldg(row + sj / per) != 0) {
+            on |= 1u << j;
+            if ((sj + 1) * 64 <= m.N) full |= 1u << j;
+          }
+        }
+        const uint32_t pair_on = (on | (on >> 1)) & 0x5555u, pair_full = (full & (full >> 1)) & 0x5555u;
+        e64 += __popc(on);
+        b64 += __popc(on & ~full);
+        e128 += __popc(pair_on);
+        b128 += __popc(pair_on & ~pair_full);
+      }
+    } else
     for (int i = lane; i < n_kt; i += 32) {
       const int kt = kw.tile(i);
       const int ca = classify(m, bh, h, rs, kt * 128, 64, nqs, nks, nullptr);
@@ -321,10 +355,20 @@ __device__ void block_scan_runs(const int32_t* a, const int32_t* b, int32_t* oa,
   const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
   const int64_t per = (n + T - 1) / T;
   const int64_t lo = min(n, static_cast<int64_t>(tid) * per), hi = min(n, lo + per);
+  constexpr int kBatch = 8;                    // loads issued together (latency-bound block)
   int32_t sa = 0, sb = 0;
-  for (int64_t i = lo; i < hi; ++i) {
-    sa += a[i];
-    if (b) sb += b[i];
+  for (int64_t i0 = lo; i0 < hi; i0 += kBatch) {
+    int32_t va[kBatch], vb[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      va[j] = i0 + j < hi ? a[i0 + j] : 0;
+      vb[j] = (b && i0 + j < hi) ? b[i0 + j] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      sa += va[j];
+      sb += vb[j];
+    }
   }
   int32_t xa = sa, xb = sb;                    // inclusive scan over the warp
 #pragma unroll
@@ -358,14 +402,21 @@ __device__ void block_scan_runs(const int32_t* a, const int32_t* b, int32_t* oa,
   }
   __syncthreads();
   int32_t ra = wa[warp] + xa - sa, rb = wb[warp] + xb - sb;
-  for (int64_t i = lo; i < hi; ++i) {
-    const int32_t va = a[i];
-    oa[i] = ra;
-    ra += va;
-    if (b) {
-      const int32_t vb = b[i];
-      ob[i] = rb;
-      rb += vb;
+  for (int64_t i0 = lo; i0 < hi; i0 += kBatch) {
+    int32_t va[kBatch], vb[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      va[j] = i0 + j < hi ? a[i0 + j] : 0;
+      vb[j] = (b && i0 + j < hi) ? b[i0 + j] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (i0 + j < hi) {
+        oa[i0 + j] = ra;
+        if (b) ob[i0 + j] = rb;
+      }
+      ra += va[j];
+      rb += vb[j];
     }
   }
   __syncthreads();
@@ -386,25 +437,51 @@ __global__ void __launch_bounds__(1024) plan_schedule_kernel(
   extern __shared__ int32_t shist[];
   __shared__ int32_t wa[32], wb[32];
   block_scan_runs(cnt_e, cnt_b, ebegin, dbegin, n_items, wa, wb);
+  // item indices fit 32 bits (the planner refuses more than 2^30 items), so
+  // the divisions below are 32-bit
   const int T = blockDim.x, tid = threadIdx.x;
-  const int64_t per_group = static_cast<int64_t>(group_heads) * nqt;
+  const uint32_t per_group = static_cast<uint32_t>(group_heads) * static_cast<uint32_t>(nqt);
+  const uint32_t unqt = static_cast<uint32_t>(nqt), n32 = static_cast<uint32_t>(n_items);
   int32_t* hb = (n_buckets <= kSharedBuckets) ? shist : hist;
+  constexpr int kBatch = 4;                    // items whose loads are issued together
   if (lpt) {
     for (int64_t i = tid; i < n_buckets; i += T) hb[i] = 0;
     __syncthreads();
-    for (int64_t i = tid; i < n_items; i += T)
-      atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - cnt_e[i])], 1);
+    for (uint32_t i0 = tid; i0 < n32; i0 += kBatch * T) {
+      int32_t len[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) len[j] = i0 + j * T < n32 ? cnt_e[i0 + j * T] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const uint32_t i = i0 + j * T;
+        if (i < n32) atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - len[j])], 1);
+      }
+    }
     __syncthreads();
     block_scan_runs(hb, nullptr, hb, nullptr, n_buckets, wa, wb);   // bucket start positions
   }
-  for (int64_t i = tid; i < n_items; i += T) {
-    const int32_t len = cnt_e[i];
-    const int64_t pos =
-        lpt ? atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - len)], 1) : i;
-    const int32_t bh = static_cast<int32_t>(i / nqt), qt = static_cast<int32_t>(i % nqt);
-    const int32_t layout = (is_svg && head_kind[bh % H] == TSR_HEAD_TEMPORAL) ? 1 : 0;
-    items[2 * pos] = make_int4(bh, qt, ebegin[i], ebegin[i] + len);
-    items[2 * pos + 1] = make_int4(layout, 0, 0, 0);
+  for (uint32_t i0 = tid; i0 < n32; i0 += kBatch * T) {
+    int32_t len[kBatch], beg[kBatch];
+    int8_t kind[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const uint32_t i = i0 + j * T;
+      const bool ok = i < n32;
+      len[j] = ok ? cnt_e[i] : 0;
+      beg[j] = ok ? ebegin[i] : 0;
+      kind[j] = (ok && is_svg) ? head_kind[(i / unqt) % static_cast<uint32_t>(H)] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const uint32_t i = i0 + j * T;
+      if (i >= n32) break;
+      const int64_t pos =
+          lpt ? atomicAdd(&hb[(i / per_group) * (max_len + 1) + (max_len - len[j])], 1) : i;
+      const int32_t bh = static_cast<int32_t>(i / unqt), qt = static_cast<int32_t>(i % unqt);
+      const int32_t layout = kind[j] == TSR_HEAD_TEMPORAL ? 1 : 0;
+      items[2 * pos] = make_int4(bh, qt, beg[j], beg[j] + len[j]);
+      items[2 * pos + 1] = make_int4(layout, 0, 0, 0);
+    }
   }
 }
 
@@ -432,6 +509,42 @@ __global__ void plan_emit_kernel(MaskDev m, int32_t nqt, int32_t bm, int32_t bn,
   const KeyWindow kw = key_window(m, h, rs.q0, rs.q1, bn);
   const int n_kt = kw.size();
   int32_t e_pos = ebegin[warp], d_pos = dbegin[warp];
+  if (aligned_uniform(m, bm, bn)) {
+    // tiles kt < n_kt, 16 consecutive ones per lane (their loads issued
+    // together); an allowed tile is full inside [0, N), else it is the ragged
+    // last tile, the item's one boundary tile (classify() builds its descriptor)
+    const uint8_t* row = m.blocks + (static_cast<int64_t>(bh) * nqs + rs.q0 / m.bq) * nks;
+    const int per = m.bk / bn;
+    for (int base = 0; base < n_kt; base += 32 * 16) {
+      const int t0 = base + lane * 16;
+      uint32_t on = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (t0 + j < n_kt && __ldg(row + (t0 + j) / per) != 0) on |= 1u << j;
+      const int cnt = __popc(on);
+      int x = cnt;                                       // inclusive scan over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      int32_t at = e_pos + x - cnt;
+      while (on) {
+        const int kt = t0 + __ffs(on) - 1;
+        on &= on - 1;
+        int32_t di = -1;
+        if ((kt + 1) * bn > m.N) {
+          tsr_tile_desc d;
+          classify(m, bh, h, rs, kt * bn, bn, nqs, nks, &d);
+          di = d_pos;
+          descs[di] = d;
+        }
+        entries[at++] = make_int2(kt * bn, di);
+      }
+      e_pos += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    return;
+  }
   for (int base = 0; base < n_kt; base += 32) {
     const int kt = (base + lane < n_kt) ? kw.tile(base + lane) : 0;
     tsr_tile_desc d;
