@@ -667,10 +667,12 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
   // Heads are processed in groups: the inputs of group g + 1 are copied in while
   // group g is attended and group g - 1 is copied out (copy engines and SMs
   // overlap).  Only the first group's copy-in and the last group's copy-out are
-  // exposed, so the groups grow from one head by a factor of 1.5 (attention of
+  // exposed, so the groups grow from one head by a factor of 1.2 (attention of
   // a group then covers the copy-in of the next whenever attending a head takes
-  // at least 1.5x as long as copying it in) up to about 160 MB of Q, K and V,
-  // and the last two groups are two heads and one.
+  // at least 1.2x as long as copying it in; a 480p head of the block-mask
+  // workload is attended in ~0.146 ms and copied in over a ~208 GB/s host link
+  // in ~0.121 ms, so faster growth leaves the SMs waiting for inputs) up to about
+  // 160 MB of Q, K and V, and the last two groups are two heads and one.
   std::vector<int64_t> gs{0};
   {
     const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>((160u << 20) / (3 * row_b)));
@@ -681,7 +683,7 @@ tsr_status tsr_attention_host(const tsr_mask* mask, const tsr_plan_opts* opts, c
       const int64_t sz = std::min<int64_t>({cap, static_cast<int64_t>(std::ceil(r)), left});
       gs.push_back(gs.back() + sz);
       left -= sz;
-      r *= 1.5;
+      r *= 1.2;
     }
     if (tail) {
       gs.push_back(gs.back() + 2);

@@ -428,7 +428,7 @@ def test_host_entry_point_in_head_groups(which):
     if which == "uniform_debug":
         opts = dict(opts, flags=tsr.PLAN_DEBUG_CHECKS)
     if which in ("uniform", "uniform_debug"):
-        spec = W.video_block_mask(seed=5, H=16)      # groups of 1, 2, 3, 4, 3, 2, 1 heads
+        spec = W.video_block_mask(seed=5, H=16)      # groups of 1, 2, 2, 2, 3, 3, 2, 1 heads
         kw = dict(bq=64, bk=64, blocks=spec.blocks)
     elif which == "svg":
         spec = W.svg_mask(3, 3, n_frames=21, frame_size=1560, kinds=np.array([1, 0, 1], np.int8))
