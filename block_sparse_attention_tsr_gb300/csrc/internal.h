@@ -113,7 +113,10 @@ tsr_status plan_schedule_into(const int32_t* cnt_e, const int32_t* cnt_b, int64_
                               int32_t nqt, int32_t H, int32_t lpt, int32_t max_len,
                               int32_t group_heads, int32_t* ebegin, int32_t* dbegin,
                               int32_t* hist, void* items, cudaStream_t stream);
-int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads);
+// Heads per longest-first scheduling group: as many (b, h) as keep their K and
+// V (plus extra_per_head bytes that stream through L2 with them, e.g. gathered
+// key indices) within ~96 MB of the L2.
+int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads, double extra_per_head = 0.0);
 tsr_status plan_count_into(const MaskDev& m, int32_t nqt, int32_t* cnt, unsigned long long* tot,
                            uint32_t* err, int64_t n_grid, cudaStream_t stream);
 tsr_status plan_finish_into(const MaskDev& m, int32_t nqt, int32_t bn, const int32_t* cnt_e,

@@ -629,9 +629,9 @@ void devbuf_free(DevBuf& b) {
 }
 
 // Heads per scheduling group: as many (b, h) as keep their K and V (2 x N x d
-// bf16 each) within ~96 MB of the 126 MB L2.
-int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads) {
-  const double per_head = 2.0 * N * d * 2.0;
+// bf16 each) and the extra bytes per head within ~96 MB of the 126 MB L2.
+int32_t heads_per_group(int32_t N, int32_t d, int64_t n_heads, double extra_per_head) {
+  const double per_head = 2.0 * N * d * 2.0 + extra_per_head;
   const int64_t g = static_cast<int64_t>(96.0e6 / per_head);
   return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(g, n_heads)));
 }

@@ -591,8 +591,11 @@ tsr_status plan_build_keylist_t(const tsr_mask* mask, const tsr_plan_opts* opts,
   if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
   if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
-  const int32_t group_heads = P->group_heads > 0 ? P->group_heads
-                                                 : heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  // a head's gathered key indices stream through L2 beside its K and V
+  const int32_t group_heads =
+      P->group_heads > 0 ? P->group_heads
+                         : heads_per_group(N, P->d, static_cast<int64_t>(B) * H,
+                                           4.0 * static_cast<double>(P->n_gidx) / (static_cast<double>(B) * H));
   const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
   if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_groups * (P->max_item_len + 1) + 1)))
     return s;
@@ -714,8 +717,11 @@ tsr_status plan_build_keylist(const tsr_mask* mask, const tsr_plan_opts* opts, t
   if (tsr_status s = devbuf_reserve(P->b_gidx, sizeof(int32_t) * P->n_gidx)) return s;
   if (tsr_status s = devbuf_reserve(P->b_ebegin, sizeof(int32_t) * n_items)) return s;
   if (tsr_status s = devbuf_reserve(P->b_dbegin, sizeof(int32_t) * n_items)) return s;
-  const int32_t group_heads = P->group_heads > 0 ? P->group_heads
-                                                 : heads_per_group(N, P->d, static_cast<int64_t>(B) * H);
+  // a head's gathered key indices stream through L2 beside its K and V
+  const int32_t group_heads =
+      P->group_heads > 0 ? P->group_heads
+                         : heads_per_group(N, P->d, static_cast<int64_t>(B) * H,
+                                           4.0 * static_cast<double>(P->n_gidx) / (static_cast<double>(B) * H));
   const int64_t n_groups = (static_cast<int64_t>(B) * H + group_heads - 1) / group_heads;
   if (tsr_status s = devbuf_reserve(P->b_hist, sizeof(int32_t) * (n_groups * (P->max_item_len + 1) + 1)))
     return s;
