@@ -76,6 +76,39 @@ def test_launches_per_step_match_the_planner():
     assert bench.launches_per_step(kl, {}) == 5
 
 
+class _FakePlan:
+    """A plan whose export is built by hand in the tsr_plan_export layout: an
+    80-byte header (n_items at byte 48) and 32-byte items (bh, q_tile, begin,
+    end, layout, 0, 0, 0)."""
+
+    def __init__(self, items):
+        hdr = np.zeros(80, np.uint8)
+        hdr[:4] = np.frombuffer(b"TSRP", np.uint8)
+        hdr[48:56] = np.frombuffer(np.int64(len(items)).tobytes(), np.uint8)
+        self.buf = hdr.tobytes() + np.asarray(items, np.int32).reshape(-1, 8).tobytes()
+
+    def export(self):
+        return self.buf
+
+
+def test_fill_counts_only_the_spatial_tiles_when_temporal_heads_run_apart():
+    """With the SVG temporal heads on their own kernel, the fill is the spatial
+    heads' allowed pairs over their tiles' elements (items of layout 0 from the
+    export); temporal items (layout 1) are left out."""
+    spec = W.svg_mask(1, 2, n_frames=4, frame_size=64, kinds=np.array([0, 1], np.int8))
+    # head 0 spatial: 2 query tiles of 128 rows, 3 + 2 tiles of 64 keys;
+    # head 1 temporal: 2 items, 7 tiles, ignored
+    items = [[0, 0, 0, 3, 0, 0, 0, 0], [0, 1, 3, 5, 0, 0, 0, 0],
+             [1, 0, 5, 9, 1, 0, 0, 0], [1, 1, 9, 12, 1, 0, 0, 0]]
+    stats = {"temporal_band": 1, "bm": 128, "bn": 64, "n_entries": 12}
+    allowed = 64 * 64 * (2 * 4 - 1)                     # S^2 (2F - 1) for the spatial head
+    assert bench.fill_of(spec, stats, _FakePlan(items)) == pytest.approx(allowed / (5 * 128 * 64))
+    # on the tiles every item counts
+    stats = dict(stats, temporal_band=0)
+    assert bench.fill_of(spec, stats, _FakePlan(items)) == pytest.approx(
+        bench.allowed_pairs(spec) / (12 * 128 * 64))
+
+
 @pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 24, 30])
 def test_head_ranges_cover_every_head_once(world):
     H = 24
