@@ -745,6 +745,27 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
     TSR_CUDA(cudaMemcpyAsync(host_tot + 6, tot + 6, sizeof(unsigned long long),
                              cudaMemcpyDeviceToHost, stream));
   }
+  // A re-plan usually keeps its regime: the tiles are counted at the previous
+  // plan's tile height before the regime is known, and their totals come back
+  // with the density, so a plan whose height is unchanged synchronises once.
+  const int32_t spec_bm = (P->n_items > 0 && (P->bm == 64 || P->bm == kBM)) ? P->bm : 0;
+  const int threads = 256;
+  auto count_tiles = [&](int32_t bm_c) -> tsr_status {
+    const int32_t nqt_c = (N + bm_c - 1) / bm_c;
+    const int64_t n_items_c = static_cast<int64_t>(B) * H * nqt_c;
+    if (n_items_c > (int64_t{1} << 30)) return fail(TSR_ERR_UNSUPPORTED, "too many query tiles");
+    if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items_c)) return s;
+    const int64_t blocks_c = (n_items_c * 32 + threads - 1) / threads;
+    plan_count_kernel<<<static_cast<unsigned>(blocks_c), threads, 0, stream>>>(
+        m, nqt_c, bm_c, static_cast<int32_t*>(P->b_cnt.p), tot, P->err);
+    TSR_CUDA(cudaGetLastError());
+    TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 6, cudaMemcpyDeviceToHost,
+                             stream));
+    TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+    return TSR_OK;
+  };
+  if (spec_bm)
+    if (tsr_status s = count_tiles(spec_bm)) return s;
   TSR_CUDA(cudaStreamSynchronize(stream));
   if (m.kind == TSR_MASK_SVG) {
     for (int32_t h = 0; h < H; ++h) {
@@ -790,18 +811,19 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   P->n_items = n_items;
   if (n_items > (int64_t{1} << 30)) return fail(TSR_ERR_UNSUPPORTED, "too many query tiles");
 
-  // 3. tiles per query tile (both widths at the chosen height)
-  if (tsr_status s = devbuf_reserve(P->b_cnt, sizeof(int32_t) * 4 * n_items)) return s;
+  // 3. tiles per query tile (both widths at the chosen height), unless the
+  // speculative count above was at this height
+  if (bm != spec_bm) {
+    if (spec_bm) {
+      // the speculative totals and error bits belong to another height
+      TSR_CUDA(cudaMemsetAsync(tot, 0, sizeof(unsigned long long) * 6, stream));
+      TSR_CUDA(cudaMemsetAsync(P->err, 0, sizeof(uint32_t), stream));
+    }
+    if (tsr_status s = count_tiles(bm)) return s;
+    TSR_CUDA(cudaStreamSynchronize(stream));
+  }
   int32_t* cnt = static_cast<int32_t*>(P->b_cnt.p);
-  const int threads = 256;
   const int64_t blocks_w = (n_items * 32 + threads - 1) / threads;
-  plan_count_kernel<<<static_cast<unsigned>(blocks_w), threads, 0, stream>>>(m, nqt, bm, cnt, tot,
-                                                                             P->err);
-  TSR_CUDA(cudaGetLastError());
-  TSR_CUDA(cudaMemcpyAsync(host_tot, tot, sizeof(unsigned long long) * 6, cudaMemcpyDeviceToHost,
-                           stream));
-  TSR_CUDA(cudaMemcpyAsync(host_tot + 8, P->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
-  TSR_CUDA(cudaStreamSynchronize(stream));
   const uint32_t host_err = static_cast<uint32_t>(host_tot[8] & 0xFFFFFFFFull);
   if (host_err & DEV_ERR_UNSUPPORTED)
     return fail(TSR_ERR_UNSUPPORTED,
