@@ -246,6 +246,9 @@ void free_plan(tsr_plan_s* P) {
   cudaFree(P->counter);
   cudaFree(P->err);
   cudaFree(P->head_kind_dev);
+  if (P->band_stream) cudaStreamDestroy(P->band_stream);
+  if (P->band_fork) cudaEventDestroy(P->band_fork);
+  if (P->band_join) cudaEventDestroy(P->band_join);
   if (P->host_tot) cudaFreeHost(P->host_tot);
   if (P->host_kinds) cudaFreeHost(P->host_kinds);
   delete P;

@@ -127,6 +127,14 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
       hi_of[r] = nqt * P->spatial_before[bh_hi[r]];
     }
   }
+  // SVG temporal heads by spatial position run on a plan's own stream, forked
+  // from `stream` here (after everything queued before this call) and joined
+  // after the attention launch: launched after the persistent attention grid,
+  // their CTAs take the SMs that grid leaves idle in its tail
+  const tsr_plan_impl* Pb = nullptr;
+  for (int r = 0; r < n_req && !Pb; ++r)
+    if (reqs[r].plan->temporal_band) Pb = reqs[r].plan;
+  if (Pb) TSR_CUDA(cudaEventRecord(Pb->band_fork, stream));
   const int key = vkey(P0->d, P0->bn, P0->stages, P0->ctas);
   auto fill = [&](auto& prm) -> tsr_status {
     memset(&prm, 0, sizeof prm);
@@ -213,15 +221,18 @@ tsr_status launch_forward_batch(const FwdArgs* reqs, int n_req, cudaStream_t str
     if (tsr_status e = fill(*prm)) return e;
     st = launch(*prm);
   }
-  if (st == TSR_OK) {
+  if (st == TSR_OK && Pb) {
+    TSR_CUDA(cudaStreamWaitEvent(Pb->band_stream, Pb->band_fork, 0));
     for (int r = 0; r < n_req; ++r) {
       const tsr_plan_impl* P = reqs[r].plan;
       if (!P->temporal_band) continue;
       if (tsr_status e = launch_svg_temporal(reqs[r].q, reqs[r].k, reqs[r].v, reqs[r].out, reqs[r].lse,
                                              P->H, P->N, P->d, P->F, P->S, P->head_kind_dev,
-                                             bh_lo[r], bh_hi[r], stream))
+                                             bh_lo[r], bh_hi[r], Pb->band_stream))
         return e;
     }
+    TSR_CUDA(cudaEventRecord(Pb->band_join, Pb->band_stream));
+    TSR_CUDA(cudaStreamWaitEvent(stream, Pb->band_join, 0));
   }
   if (st != TSR_ERR_UNSUPPORTED) return st;
   return fail(TSR_ERR_UNSUPPORTED, "no kernel variant for d=" + std::to_string(P0->d) + " bn=" +

@@ -79,6 +79,10 @@ struct tsr_plan_impl {
   void* launch = nullptr;
   int64_t n_launch = 0;
   std::vector<int64_t> spatial_before;   // [B*H + 1]: spatial heads among bh < i
+  // the per-position kernel's stream, forked from the caller's stream before
+  // the attention launch and joined after it (created with the first such plan)
+  cudaStream_t band_stream = nullptr;
+  cudaEvent_t band_fork = nullptr, band_join = nullptr;
   // device buffers (owned)
   void* items = nullptr;     // tsr_plan_item [n_items]
   void* entries = nullptr;   // tsr_plan_entry [n_entries]

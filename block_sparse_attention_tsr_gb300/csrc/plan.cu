@@ -928,6 +928,9 @@ tsr_status plan_launch_list(tsr_plan_impl* P, cudaStream_t stream) {
   for (int64_t bh = 0; bh < BH; ++bh)
     P->spatial_before[bh + 1] = P->spatial_before[bh] + (P->head_layout[bh % P->H] ? 0 : 1);
   const int64_t nqt = (P->N + P->bm - 1) / P->bm;   // every head has nqt items
+  if (!P->band_stream) TSR_CUDA(cudaStreamCreateWithFlags(&P->band_stream, cudaStreamNonBlocking));
+  if (!P->band_fork) TSR_CUDA(cudaEventCreateWithFlags(&P->band_fork, cudaEventDisableTiming));
+  if (!P->band_join) TSR_CUDA(cudaEventCreateWithFlags(&P->band_join, cudaEventDisableTiming));
   P->temporal_band = 1;
   P->n_launch = nqt * P->spatial_before[BH];
   if (P->n_launch == 0) return TSR_OK;
