@@ -98,9 +98,11 @@ typedef enum { TSR_HEAD_SPATIAL = 0, TSR_HEAD_TEMPORAL = 1 } tsr_head_kind;
  *           is copied.  With temporal_radius = 0, n_frames <= 32 and no
  *           TSR_PLAN_TEMPORAL_TILES / TSR_PLAN_DEBUG_CHECKS, a temporal head is
  *           instead computed as frame_size independent n_frames x n_frames
- *           blocks (one per spatial index) by a kernel of its own, launched
- *           after the attention kernel on the same stream (P rounded to bf16 for the
- *           P V product there too).
+ *           blocks (one per spatial index) by a kernel of its own (P rounded
+ *           to bf16 for the P V product there too).  It runs on a stream the
+ *           plan owns, forked from the call's stream before the attention
+ *           launch and joined back into it after: work queued on the call's
+ *           stream afterwards sees both kernels' results.
  *           Any n_frames >= 1; frame_size >= 16 when a head is
  *           spatial (a 128-token tile may hold at most 8 frames; smaller frames
  *           give TSR_ERR_UNSUPPORTED); temporal_radius >= 0.

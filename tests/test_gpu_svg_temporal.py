@@ -1,7 +1,7 @@
 """SVG temporal heads of radius 0 by spatial position: with n_frames <= 32 each
 temporal head is frame_size independent F x F blocks, computed by their own
-kernel after the attention kernel, which then runs the spatial heads' items
-only.  Against the CPU oracle at the stated tolerances: frame counts 1 to 32,
+kernel (on a stream the plan owns, forked from the call's stream and joined
+back), while the attention kernel runs the spatial heads' items only.  Against the CPU oracle at the stated tolerances: frame counts 1 to 32,
 frame sizes that leave a ragged last CTA of positions, d = 64 and 128, both tile
 orientations, split-KV, plan updates that change the head kinds, every head
 temporal, the batched launch and the host entry point.  The attention-tile
