@@ -879,14 +879,35 @@ namespace {
 
 // Stable compaction of the items whose head is not temporal, by one CTA: each
 // thread takes a contiguous run of items, the runs' kept counts are scanned.
-__global__ void launch_compact_kernel(const int4* items, int64_t n_items, const int8_t* head_kind,
-                                      int32_t H, int4* launch) {
+// The head kinds sit in shared memory (up to kCompactMaxH heads) and each
+// thread's item loads are issued four at a time.
+constexpr int32_t kCompactMaxH = 4096;
+
+__global__ void __launch_bounds__(1024) launch_compact_kernel(const int4* items, int64_t n_items,
+                                                              const int8_t* head_kind, int32_t H,
+                                                              int4* launch) {
   __shared__ int64_t warp_sum[32];
+  __shared__ int8_t kinds[kCompactMaxH];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, n_warps = blockDim.x >> 5;
+  const bool shared_kinds = H <= kCompactMaxH;
+  if (shared_kinds)
+    for (int h = t; h < H; h += blockDim.x) kinds[h] = head_kind[h];
+  __syncthreads();
+  auto temporal = [&](int32_t bh) {
+    const int32_t h = bh % H;
+    return (shared_kinds ? kinds[h] : head_kind[h]) == TSR_HEAD_TEMPORAL;
+  };
+  constexpr int kBatch = 4;
   const int64_t per = (n_items + blockDim.x - 1) / blockDim.x;
   const int64_t i0 = min(n_items, t * per), i1 = min(n_items, i0 + per);
   int64_t kept = 0;
-  for (int64_t i = i0; i < i1; ++i) kept += head_kind[items[2 * i].x % H] != TSR_HEAD_TEMPORAL;
+  for (int64_t b = i0; b < i1; b += kBatch) {
+    int32_t bh[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) bh[j] = b + j < i1 ? items[2 * (b + j)].x : 0;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) kept += (b + j < i1 && !temporal(bh[j])) ? 1 : 0;
+  }
   int64_t x = kept;                                       // inclusive scan in the warp
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
@@ -904,12 +925,22 @@ __global__ void launch_compact_kernel(const int4* items, int64_t n_items, const 
   }
   __syncthreads();
   int64_t at = x - kept + (warp ? warp_sum[warp - 1] : 0);
-  for (int64_t i = i0; i < i1; ++i) {
-    const int4 a = items[2 * i];
-    if (head_kind[a.x % H] == TSR_HEAD_TEMPORAL) continue;
-    launch[2 * at] = a;
-    launch[2 * at + 1] = items[2 * i + 1];
-    ++at;
+  for (int64_t b = i0; b < i1; b += kBatch) {
+    int4 a[kBatch], c[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool ok = b + j < i1;
+      a[j] = ok ? items[2 * (b + j)] : make_int4(0, 0, 0, 0);
+      c[j] = ok ? items[2 * (b + j) + 1] : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (b + j < i1 && !temporal(a[j].x)) {
+        launch[2 * at] = a[j];
+        launch[2 * at + 1] = c[j];
+        ++at;
+      }
+    }
   }
 }
 
