@@ -220,11 +220,15 @@ typedef struct {
  * plan cheaply.  Splash digest, "Splash Attention": tiles with nothing to compute
  * are never loaded, and element-exact masking is applied on boundary tiles only.
  *
- * Runs as CUDA kernels on `stream`; synchronises `stream` once to size the plan.
- * On success *out receives a new plan that the caller must release with
- * tsr_plan_destroy().  The plan owns device memory (tiles, descriptors, work
- * items, temporal-major scratch) and may be used by any number of
- * tsr_bsa_forward() calls on the same device with matching B, H, N, d.
+ * Runs as CUDA kernels on `stream`; synchronises `stream` to size the plan
+ * (twice: for the mask's density, then for the tile counts; a re-plan whose
+ * tile height is unchanged, once).  On success *out receives a new plan that
+ * the caller must release with tsr_plan_destroy().  The plan owns device memory
+ * (tiles, descriptors, work items, its work counter and, for SVG plans whose
+ * temporal heads run by spatial position, a stream and two events) and may be
+ * used by any number of tsr_bsa_forward() calls on the same device with
+ * matching B, H, N, d, one after another (calls on different streams must be
+ * ordered by the caller: they share the plan's work counter).
  */
 tsr_status tsr_plan(const tsr_mask *mask, const tsr_plan_opts *opts, tsr_plan_t *out,
                     void *stream);
