@@ -136,3 +136,19 @@ def test_plan_flags_match_the_header():
     assert int(defs["TSR_PLAN_NO_LPT"]) == tsr.PLAN_NO_LPT
     assert int(defs["TSR_PLAN_TEST_STALL"]) == tsr.PLAN_TEST_STALL
     assert int(defs["TSR_PLAN_DEBUG_CHECKS"]) == tsr.PLAN_DEBUG_CHECKS
+    assert int(defs["TSR_PLAN_TEMPORAL_TILES"]) == tsr.PLAN_TEMPORAL_TILES
+    # every flag the header defines is a distinct bit the binding knows
+    assert sorted(int(v) for v in defs.values()) == [1, 2, 4, 8, 16]
+
+
+def test_plan_stats_layout_matches_the_header():
+    """The binding's tsr_plan_stats fields are the header's, in order."""
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "tsr.h")).read()
+    body = hdr[hdr.index("/* Statistics of a plan"):]
+    body = body[body.index("{") + 1:body.index("} tsr_plan_stats;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = [n for decl in body.split(";") if decl.strip()
+             for n in re.sub(r"^\s*\w+\s+", "", decl.strip()).replace(" ", "").split(",")]
+    assert names == [f for f, _ in tsr._Stats._fields_]
