@@ -2,9 +2,11 @@
 //
 // Tessera abstract: a mapping layer keeps, merges or cuts logical blocks into
 // physical tiles that suit the mask and the GPU, and a task layer groups the
-// tiles into GPU tasks.  Here every physical tile is 128 query rows (the
-// tcgen05 M = 128 datapath) by BN keys (64 or 128):
-//   * logical blocks of 128 x 128 (BN = 128) map one-to-one (kept),
+// tiles into GPU tasks.  Here a physical tile is bm query rows by BN keys: 128
+// rows (the tcgen05 M = 128 datapath with queries on M) by 64 or 128 keys, or,
+// for key-major plans, 64 rows by 64 keys (two such tiles of a query block are
+// computed together with 128 keys on M):
+//   * logical blocks of the tile's size map one-to-one (kept),
 //   * smaller blocks (32, 64, frames of 21 tokens) are merged into a tile,
 //   * larger blocks (256, 1,560-token frames) are cut into several tiles.
 // Each tile is classified from the logical segments that overlap it:
@@ -13,12 +15,14 @@
 //   boundary -> mixed, or crossing N: a 32-byte descriptor (row segments x
 //               column segments bit grid) drives element masking.
 // (Splash digest, "Splash Attention": skip empty tiles, exact masking only on
-// boundary tiles.)  The task layer gives every 128-row query tile one work item
+// boundary tiles.)  The task layer gives every bm-row query tile one work item
 // holding its tiles in key order; items are ordered longest first so that a
-// persistent grid finishes evenly, and the regime table picks the tile width and
-// pipeline depth.  Three kernels: count (both tile widths, so the regime can be
-// chosen from the counts), schedule (one block: prefix sums + longest-first
-// order), emit (tiles and descriptors).
+// persistent grid finishes evenly, and the regime table picks the orientation,
+// tile width and pipeline depth.  Three kernels: count (both tile widths at the
+// chosen height, so the regime can be checked against the counts), schedule
+// (one block: prefix sums + longest-first order), emit (tiles and
+// descriptors); then the attention launch list (without SVG temporal heads that
+// run by spatial position) and the split-KV units.
 #include <algorithm>
 #include <cstring>
 #include <string>
