@@ -18,8 +18,8 @@
 // boundary tiles.)  The task layer gives every bm-row query tile one work item
 // holding its tiles in key order; items are ordered longest first so that a
 // persistent grid finishes evenly, and the regime table picks the orientation,
-// tile width and pipeline depth.  Three kernels: count (both tile widths at the
-// chosen height, so the regime can be checked against the counts), schedule
+// tile width and pipeline depth.  Three kernels: count (both tile widths at one
+// height, so either width's totals are at hand once the regime is known), schedule
 // (one block: prefix sums + longest-first order), emit (tiles and
 // descriptors); then the attention launch list (without SVG temporal heads that
 // run by spatial position) and the split-KV units.
