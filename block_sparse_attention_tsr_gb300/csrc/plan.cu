@@ -752,7 +752,9 @@ tsr_status plan_build(const tsr_mask* mask, const tsr_plan_opts* opts, tsr_plan_
   // A re-plan usually keeps its regime: the tiles are counted at the previous
   // plan's tile height before the regime is known, and their totals come back
   // with the density, so a plan whose height is unchanged synchronises once.
-  const int32_t spec_bm = (P->n_items > 0 && (P->bm == 64 || P->bm == kBM)) ? P->bm : 0;
+  int32_t spec_bm = (P->n_items > 0 && (P->bm == 64 || P->bm == kBM)) ? P->bm : 0;
+  if (spec_bm && static_cast<int64_t>(B) * H * ((N + spec_bm - 1) / spec_bm) > (int64_t{1} << 30))
+    spec_bm = 0;                                   // too many tiles at that height: no guess
   const int threads = 256;
   auto count_tiles = [&](int32_t bm_c) -> tsr_status {
     const int32_t nqt_c = (N + bm_c - 1) / bm_c;
